@@ -1,0 +1,331 @@
+"""Pins for the CPU oracle: facts fixed by the pages and by mathematics.
+
+None of these compares the oracle with itself.  Each pin is one of: a closed
+form the pages print, a worked example the pages print, a byte count the pages
+print, a brute-force enumeration of a definition on tiny inputs, or a library
+routine that a special case reduces to.
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import moe_workloads as mw
+
+
+def _prob(oracle, T, E, R, P, k, h=8, R_src=1, elem_bytes=2, e2r=None, src_off=None):
+    return oracle.make_problem(T, h, k, E, R, P, R_src, elem_bytes, 128, e2r, src_off)
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_bf16_rne_matches_library_conversion(oracle_mod):
+    """bf16 round-to-nearest-even: the oracle's bit rule equals torch's conversion."""
+    import torch
+    rng = np.random.default_rng(7)
+    vals = [rng.standard_normal(4000).astype(np.float32),
+            (rng.standard_normal(2000) * 1e30).astype(np.float32),
+            (rng.standard_normal(2000) * 1e-38).astype(np.float32)]  # subnormals
+    # exact ties: upper bits even/odd with dropped half = 0x8000
+    ties = np.array([0x3F808000, 0x3F818000, 0xBF808000, 0x7F7F8000, 0x00018000, 0x3F80FFFF,
+                     0x3F807FFF, 0x7F7FFFFF, 0x00000000, 0x80000000, 0x7F800000, 0xFF800000],
+                    dtype=np.uint32).view(np.float32)
+    v = np.concatenate(vals + [ties])
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle_mod.f32_to_bf16(v)
+    assert np.array_equal(got, want)
+    back = oracle_mod.bf16_to_f32(got)
+    assert np.array_equal(back.view(np.uint32), got.astype(np.uint32) << 16)
+
+
+# ------------------------------------------------------- layout by brute force
+
+def _brute_layout(ids, rank_of, H, P):
+    """pos by counting (not sorting): slots with a smaller (rank, expert) key,
+    plus earlier tokens of the same expert."""
+    T, k = ids.shape
+    key = lambda e: (rank_of[e], e)  # noqa: E731
+    pos = np.zeros((T, k), np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            n = 0
+            for t2 in range(T):
+                for j2 in range(k):
+                    e2 = ids[t2, j2]
+                    if key(e2) < key(e) or (e2 == e and t2 < t):
+                        n += 1
+            pos[t, j] = n
+    mask = np.zeros((T, H), np.uint8)
+    for t in range(T):
+        for j in range(k):
+            mask[t, rank_of[ids[t, j]] // P] = 1
+    return pos, mask
+
+
+@pytest.mark.parametrize("e2r", [None, [1, 0, 1, 0], [0, 0, 1, 1], [1, 1, 1, 0]])
+def test_layout_exhaustive_tiny(oracle_mod, e2r):
+    """Every id assignment of 3 tokens x 2 distinct experts out of 4, two ranks
+    on two hosts, against the counting definition of the receive order."""
+    E, k, T, R, P = 4, 2, 3, 2, 1
+    rank_of = [e // 2 for e in range(E)] if e2r is None else e2r
+    pairs = [p for p in itertools.permutations(range(E), k)]
+    prob, keep = _prob(oracle_mod, T, E, R, P, k, e2r=e2r)
+    for combo in itertools.product(pairs, repeat=T):
+        ids = np.array(combo, np.int32)
+        lay = oracle_mod.layout(prob, ids)
+        pos, mask = _brute_layout(ids, rank_of, R // P, P)
+        assert np.array_equal(lay["pos"], pos)
+        assert np.array_equal(lay["host_mask"], mask)
+        cnt = np.bincount(ids.ravel(), minlength=E)
+        assert np.array_equal(lay["expert_count"], cnt)
+        for e in range(E):
+            assert lay["expert_offset"][e] == sum(cnt[e2] for e2 in range(E)
+                                                  if (rank_of[e2], e2) < (rank_of[e], e))
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode-EP32-r8", "decode-EP32-alt", "prefill"])
+def test_layout_invariants(oracle_mod, name):
+    w = mw.WORKLOADS[name]
+    if w.T > 1024:
+        w = mw.scaled(w, T=1024, R_src=min(w.R_src, 8))
+    ids = mw.gen_ids(w, step=3 % w.steps)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, R_src=w.R_src)
+    lay = oracle_mod.layout(prob, ids)
+    S = w.T * w.k
+    rank_of = np.arange(w.E) // (w.E // w.R)
+    assert lay["expert_count"].sum() == S
+    assert np.array_equal(lay["rank_count"], np.bincount(rank_of, weights=lay["expert_count"],
+                                                         minlength=w.R).astype(np.int64))
+    assert np.array_equal(lay["rank_offset"], np.concatenate([[0], np.cumsum(lay["rank_count"])]))
+    pos = lay["pos"].ravel()
+    assert np.array_equal(np.sort(pos), np.arange(S))            # bijection onto [0, T*k)
+    assert np.array_equal(lay["recv_src"][pos], np.arange(S))    # inverse map
+    # library routine: numpy's lexsort by (rank, expert), ties by slot index
+    flat = ids.ravel()
+    order = np.lexsort((np.arange(S), flat, rank_of[flat]))
+    assert np.array_equal(lay["recv_src"], order)
+    for e in range(w.E):  # expert segments: contiguous, ascending token order
+        seg = lay["recv_src"][lay["expert_offset"][e]:lay["expert_offset"][e] + lay["expert_count"][e]]
+        assert np.all(flat[seg] == e)
+        assert np.all(np.diff(seg // w.k) > 0)
+    assert np.array_equal(lay["host_count"], lay["host_mask"].sum(axis=0))
+    assert np.array_equal(lay["host_offset"], np.concatenate([[0], np.cumsum(lay["host_count"])]))
+
+
+def test_oracle_rejects_bad_ids(oracle_mod):
+    prob, keep = _prob(oracle_mod, 2, 4, 2, 1, 2)
+    with pytest.raises(oracle_mod.OracleError) as ei:
+        oracle_mod.layout(prob, np.array([[0, 0], [1, 2]], np.int32))
+    assert ei.value.code == oracle_mod.ERR_BAD_IDS
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.layout(prob, np.array([[0, 4], [1, 2]], np.int32))
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.stats(prob, np.array([[-1, 1], [1, 2]], np.int32))
+
+
+# ------------------------------------------- copy counts: closed forms (c0, c1, c2)
+
+def _c2(E, k, H):
+    """Mode 2 copies per token ("Balancing and Beyond", section 3.2)."""
+    return Fraction(H - 1) * (1 - Fraction(math.comb(E - E // H, k), math.comb(E, k)))
+
+
+@pytest.mark.parametrize("E,k,R,P", [(16, 2, 4, 2), (12, 3, 6, 2), (8, 2, 4, 1), (16, 3, 8, 2)])
+def test_copy_counts_exact_over_all_expert_sets(oracle_mod, E, k, R, P):
+    """Averaged over all C(E, k) expert sets, the per-token copy counts are
+    exactly c0 = k(1 - 1/EP), c1 = k(H-1)/H and c2 = (H-1)[1 - C(E-E/H, k)/C(E, k)]."""
+    H = R // P
+    subsets = np.array(list(itertools.combinations(range(E), k)), np.int32)
+    T = len(subsets)
+    prob, keep = _prob(oracle_mod, T, E, R, P, k, R_src=1)  # every token on rank 0
+    st = oracle_mod.stats(prob, subsets)
+    assert Fraction(int(st["src_mode0"][0]), T) == Fraction(k) * (1 - Fraction(1, R))
+    assert Fraction(int(st["src_mode1"][0]), T) == Fraction(k * (H - 1), H)
+    assert Fraction(int(st["src_mode2"][0]), T) == _c2(E, k, H)
+
+
+def test_copy_counts_tiny_value(oracle_mod):
+    """E=16, k=2, H=2: c1 = 1 and c2 = 23/30 exactly."""
+    assert _c2(16, 2, 2) == Fraction(23, 30)
+    subsets = np.array(list(itertools.combinations(range(16), 2)), np.int32)
+    prob, keep = _prob(oracle_mod, len(subsets), 16, 4, 2, 2, R_src=1)
+    st = oracle_mod.stats(prob, subsets)
+    assert (st["src_mode1"][0], st["src_mode2"][0]) == (120, 92)
+
+
+def test_copy_counts_deepseek_shape(oracle_mod):
+    """E=256, k=8, EP32 on four hosts: c1 = 6, c2 ~ 2.7, 55 % fewer network
+    copies ("Balancing and Beyond", section 3.2); uniform sample, 4 sigma."""
+    w = mw.Workload("u", T=20000, h=8, k=8, E=256, R=32, P=8, R_src=1, seed=11)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, R_src=1)
+    st = oracle_mod.stats(prob, ids)
+    c1 = st["src_mode1"][0] / w.T
+    c2 = st["src_mode2"][0] / w.T
+    c2_exact = float(_c2(256, 8, 4))
+    assert abs(c2_exact - 2.7107) < 1e-4
+    # per-token variances are at most k p (1 - p) = 1.5 (c1) and 0.75 (c2)
+    assert abs(c1 - 6.0) < 4 * math.sqrt(1.5 / w.T)
+    assert abs(c2 - c2_exact) < 4 * math.sqrt(0.75 / w.T)
+    assert round(1 - c2_exact / 6.0, 2) == 0.55
+
+
+def test_hybridep_rdma_send_bytes(oracle_mod):
+    """The HybridEP issue's shape (4096 tokens, h=7168, 16 ranks on 2 hosts, 8
+    local experts, top-8) prints rdma_send_bytes 117.11 MB (bf16) and 60.40 MB
+    (fp8 with scales): one copy per (token, host) over all hosts.  Uniform
+    routing; tolerance 3.5 sampling sigmas (0.25 MB)."""
+    w = mw.WORKLOADS["prefill"]
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, R_src=1)
+    lay = oracle_mod.layout(prob, ids)
+    st_bf16 = oracle_mod.stats(prob, ids)
+    probf, keepf = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, R_src=1, elem_bytes=1)
+    st_fp8 = oracle_mod.stats(probf, ids)
+    assert st_bf16["row_bytes"] == 14336 and st_fp8["row_bytes"] == 7168 + 4 * 56
+    copies = int(lay["host_count"].sum())
+    assert abs(copies * st_bf16["row_bytes"] - 117.11e6) < 0.25e6
+    assert abs(copies * st_fp8["row_bytes"] - 60.40e6) < 0.13e6
+
+
+# --------------------------------------------- "Profiling when rank unbalance"
+
+def _p1_case(oracle_mod, per_rank):
+    """16 ranks on 2 hosts, one expert per rank, k=1; a source rank sends its
+    i-th token to rank i mod 16."""
+    R, P = 16, 8
+    src_off = np.concatenate([[0], np.cumsum(per_rank)]).astype(np.int32)
+    ids = np.concatenate([np.arange(n) % R for n in per_rank]).astype(np.int32)[:, None]
+    prob, keep = _prob(oracle_mod, int(src_off[-1]), R, R, P, 1, R_src=R, src_off=src_off)
+    return oracle_mod.stats(prob, ids)
+
+
+def test_p1_unbalanced_receive_counts(oracle_mod):
+    """Host-0 ranks hold 384 tokens, host-1 ranks 64: a host-1 rank receives
+    (384/16)*8 = 192 from host 0 and (64/16)*7 = 28 from its own host, 220 in
+    all; each host-0 GPU sends 192 tokens over the network."""
+    st = _p1_case(oracle_mod, [384] * 8 + [64] * 8)
+    for r in range(8, 16):
+        assert st["recv_remote"][r] == 192
+        assert st["recv_local"][r] == 28
+        assert st["recv_remote"][r] + st["recv_local"][r] == 220
+    for r in range(8):
+        assert st["src_mode1"][r] == 192
+
+
+def test_p1_balanced_receive_counts(oracle_mod):
+    """224 tokens per rank: (224/16)*15 = 210 received from other ranks, 112 of
+    them over the network; each GPU sends 112 over the network."""
+    st = _p1_case(oracle_mod, [224] * 16)
+    for r in range(16):
+        assert st["recv_remote"][r] + st["recv_local"][r] == 210
+        assert st["recv_remote"][r] == 112
+        assert st["src_mode1"][r] == 112
+
+
+# ------------------------------------------------------------- imbalance ratio
+
+def test_imbalance_ratio_special_cases(oracle_mod):
+    E, k, T = 16, 2, 64
+    prob, keep = _prob(oracle_mod, T, E, 4, 2, k, R_src=1)
+    same = np.tile(np.array([[3, 9]], np.int32), (T, 1))
+    assert oracle_mod.stats(prob, same)["imbalance_ratio"] == E / k
+    rr = (np.arange(T * k) % E).astype(np.int32).reshape(T, k)
+    st = oracle_mod.stats(prob, rr)
+    assert st["imbalance_ratio"] == 1.0 and st["rank_imbalance"] == 1.0
+
+
+def test_bytes_formulas(oracle_mod):
+    """tokens x k x h x 2 B per rank and direction, copies x row bytes per mode."""
+    w = mw.scaled(mw.WORKLOADS["decode-EP32-r8"], T=512, R_src=32)
+    ids = mw.gen_ids(w)
+    for eb in (2, 1):
+        prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, R_src=w.R_src, elem_bytes=eb)
+        st = oracle_mod.stats(prob, ids)
+        rho = w.h * 2 if eb == 2 else w.h + 4 * (w.h // 128)
+        assert st["row_bytes"] == rho
+        assert np.all(st["src_naive_bytes"] == st["src_tokens"] * w.k * w.h * 2)
+        assert np.all(st["src_copies"] == st["src_tokens"] * w.k)
+        for m in (0, 1, 2):
+            assert np.all(st[f"src_mode{m}_bytes"] == st[f"src_mode{m}"] * rho)
+        assert np.all(st["src_mode2"] <= st["src_mode1"])
+        assert np.all(st["src_mode1"] <= st["src_mode0"])
+        assert st["recv_slots"].sum() == w.T * w.k
+        assert np.array_equal(st["recv_self"] + st["recv_local"] + st["recv_remote"], st["recv_slots"])
+        assert st["recv_relay"].sum() == st["sum_mode2_copies"]
+
+
+# -------------------------------------------------------- dispatch and combine
+
+def test_dispatch_moves_rows(oracle_mod):
+    w = mw.scaled(mw.WORKLOADS["tiny"], T=64)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, R_src=w.R_src)
+    lay = oracle_mod.layout(prob, ids)
+    x = mw.gen_x_bf16(w)
+    recv = oracle_mod.dispatch(prob, lay["pos"], x)
+    assert np.array_equal(recv[lay["pos"]], np.repeat(x[:, None, :], w.k, axis=1))
+    wf = mw.scaled(w, dtype="fp8")
+    probf, keepf = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, R_src=w.R_src, elem_bytes=1)
+    q, sc = mw.gen_x_fp8(wf)
+    rq, rs = oracle_mod.dispatch(probf, lay["pos"], q, sc)
+    src_tok = lay["recv_src"] // w.k
+    assert np.array_equal(rq, q[src_tok]) and np.array_equal(rs, sc[src_tok])
+
+
+@pytest.mark.parametrize("k", [2, 8])
+def test_combine_unit_weights_identity_experts(oracle_mod, k):
+    """Permute then unpermute with identity experts and unit weights returns
+    k * x exactly (k a power of two)."""
+    w = mw.Workload("rt", T=96, h=256, k=k, E=32, R=8, P=4, R_src=1)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h)
+    lay = oracle_mod.layout(prob, ids)
+    x = mw.gen_x_bf16(w)
+    recv = oracle_mod.dispatch(prob, lay["pos"], x)
+    out = oracle_mod.combine(prob, lay["pos"], recv, np.ones((w.T, k), np.float32))
+    want = mw.f32_to_bf16_bits(mw.bf16_bits_to_f32(x) * np.float32(k))
+    assert np.array_equal(out, want)
+
+
+def test_combine_k1_is_a_gather(oracle_mod):
+    w = mw.Workload("k1", T=50, h=64, k=1, E=8, R=4, P=2, R_src=1)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, 1, h=w.h)
+    lay = oracle_mod.layout(prob, ids)
+    y = mw.gen_y_host(w)
+    out = oracle_mod.combine(prob, lay["pos"], y, np.ones((w.T, 1), np.float32))
+    assert np.array_equal(out, y[lay["pos"][:, 0]])
+
+
+def test_combine_error_bound_against_fp64(oracle_mod):
+    """|out - sum_j w_j y_j| <= 2^-8 |exact| + (1 + 2^-8) k 2^-24 sum_j |w_j y_j|:
+    half a bf16 ulp for the final rounding plus the fp32 fma chain."""
+    w = mw.Workload("c", T=128, h=512, k=8, E=64, R=8, P=4, R_src=1)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h)
+    lay = oracle_mod.layout(prob, ids)
+    y = mw.gen_y_host(w)
+    g = mw.gen_gates(w)
+    out = mw.bf16_bits_to_f32(oracle_mod.combine(prob, lay["pos"], y, g)).astype(np.float64)
+    yf = mw.bf16_bits_to_f32(y).astype(np.float64)[lay["pos"]]           # [T, k, h]
+    terms = g.astype(np.float64)[:, :, None] * yf
+    exact = terms.sum(axis=1)
+    bound = 2.0 ** -8 * np.abs(exact) + (1 + 2.0 ** -8) * w.k * 2.0 ** -24 * np.abs(terms).sum(axis=1)
+    assert np.all(np.abs(out - exact) <= bound)
+
+
+def test_combine_sums_in_ascending_slot_order(oracle_mod):
+    """y rows 2^24, 1, -2^24 with unit weights: ascending slot order gives
+    (2^24 + 1) - 2^24 = 0 in fp32 (the tie rounds to even), any order that
+    adds the two large terms first gives 1."""
+    prob, keep = _prob(oracle_mod, 1, 3, 3, 1, 3, h=8)
+    pos = np.array([[0, 1, 2]], np.int32)
+    y = mw.f32_to_bf16_bits(np.array([[2.0 ** 24] * 8, [1.0] * 8, [-(2.0 ** 24)] * 8], np.float32))
+    out = oracle_mod.combine(prob, pos, y, np.ones((1, 3), np.float32))
+    assert np.all(out == 0)
+    out_rev = oracle_mod.combine(prob, np.array([[0, 2, 1]], np.int32), y, np.ones((1, 3), np.float32))
+    assert np.all(mw.bf16_bits_to_f32(out_rev) == 1.0)
