@@ -1,0 +1,429 @@
+"""Benchmark: one MoE layer's layout + stats + dispatch + combine on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: moe_layout,
+moe_stats, moe_dispatch, moe_combine (five kernels), inputs resident in HBM.
+The headline value is the effective HBM bandwidth of dispatch + combine: their
+algorithmic bytes (read each token row once and write k copies; read k rows
+and write one) divided by the whole step's time, layout and stats included.
+The default workload is the largest one, "prefill-fp8" (T=16384, h=7168,
+top-8 of 128 experts, fp8 e4m3 rows with fp32 scales, Zipf s=1.0 routing).
+
+--impl reference times the single-threaded CPU oracle on a bounded sample of
+the same workload (the slow plain definition, as it stands).
+With N > 1 (torchrun), every rank runs an independent replica: the path has
+no exchange step on one GPU, so the job total is N x the per-rank work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine µs and effective HBM GB/s (fraction of GB300 peak) per layer"
+FALLBACK_HBM_GBS = 6800.0
+KERNELS_PER_STEP = 5  # count, rank, stats, dispatch, combine
+
+
+def algorithmic_bytes(w, tokens=None):
+    """Dispatch reads each row once and writes k copies (payload + fp8 scales);
+    combine reads k bf16 rows and writes one."""
+    T = w.T if tokens is None else tokens
+    rho = w.h + 4 * (w.h // w.scale_group) if w.dtype == "fp8" else 2 * w.h
+    dispatch = T * rho * (1 + w.k)
+    combine = T * w.k * 2 * w.h + T * 2 * w.h
+    return dispatch, combine
+
+
+def read_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            stack = [d]
+            while stack:
+                cur = stack.pop()
+                if isinstance(cur, dict):
+                    for k, v in cur.items():
+                        if k == "hbm_gbs" and isinstance(v, (int, float)):
+                            return float(v), "measured"
+                        stack.append(v)
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_moe_layout_04_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (profiles/dram_traffic.txt lines:
+    <kernel> <workload> <bytes_per_launch> <source hash>)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    for line in open(path):
+        f = line.split()
+        if len(f) == 4 and f[0] == kernel and f[1] == workload and f[3] == cur:
+            return int(float(f[2]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        note = "sampled during the timed region"
+        if not inside and self.rows:
+            near = min(self.rows, key=lambda tr: min(abs(tr[0] - t0), abs(tr[0] - t1)))
+            inside, note = [near[1]], "timed region shorter than the 200 ms sampling period: nearest sample"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in inside for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- oracle (CPU)
+
+def oracle_pass(w, tokens, ids, gates, xin, y):
+    """One pass of the oracle over the first `tokens` tokens of a workload."""
+    import oracle
+    eb = 1 if w.dtype == "fp8" else 2
+    prob, keep = oracle.make_problem(tokens, w.h, w.k, w.E, w.R, w.P, 1, eb, w.scale_group)
+    lay = oracle.layout(prob, ids[:tokens])
+    oracle.stats(prob, ids[:tokens])
+    if w.dtype == "fp8":
+        oracle.dispatch(prob, lay["pos"], xin[0][:tokens], xin[1][:tokens])
+    else:
+        oracle.dispatch(prob, lay["pos"], xin[:tokens])
+    oracle.combine(prob, lay["pos"], y, gates[:tokens])
+
+
+def oracle_inputs(w, tokens):
+    import moe_workloads as mw
+    ids = mw.gen_ids(w)
+    gates = mw.gen_gates(w)
+    xin = mw.gen_x_fp8(w, rows=tokens) if w.dtype == "fp8" else mw.gen_x_bf16(w, rows=tokens)
+    y = mw.gen_y_host(w, rows=tokens * w.k)
+    return ids, gates, xin, y
+
+
+def cpu_baseline(w, seconds=10.0):
+    """The oracle as it stands, single-threaded, on a token sample sized to run
+    about `seconds`."""
+    import oracle
+    oracle.build()
+    probe = 64
+    ids, gates, xin, y = oracle_inputs(w, probe)
+    t0 = time.perf_counter()
+    oracle_pass(w, probe, ids, gates, xin, y)
+    per_tok = (time.perf_counter() - t0) / probe
+    tokens = int(max(probe, min(w.T, seconds / max(per_tok, 1e-9))))
+    ids, gates, xin, y = oracle_inputs(w, tokens)
+    t0 = time.perf_counter()
+    oracle_pass(w, tokens, ids, gates, xin, y)
+    dt = time.perf_counter() - t0
+    d, c = algorithmic_bytes(w, tokens)
+    return {"value": round((d + c) / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {tokens} of {w.T} tokens of {w.name}: layout+stats+dispatch+combine, "
+                      f"one pass, {dt:.2f} s"}
+
+
+def run_reference(args, w):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    probe = 32
+    ids, gates, xin, y = oracle_inputs(w, probe)
+    t0 = time.perf_counter()
+    oracle_pass(w, probe, ids, gates, xin, y)
+    per_tok = (time.perf_counter() - t0) / probe
+    budget = 90.0  # seconds for the whole warm-up + timed run
+    tokens = int(max(8, min(w.T, budget / (args.steps + args.warmup) / max(per_tok, 1e-9))))
+    ids, gates, xin, y = oracle_inputs(w, tokens)
+    for _ in range(args.warmup):
+        oracle_pass(w, tokens, ids, gates, xin, y)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_pass(w, tokens, ids, gates, xin, y)
+    dt = (time.perf_counter() - t0) / args.steps
+    d, c = algorithmic_bytes(w, tokens)
+    value = (d + c) / dt / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: first {tokens} of {w.T} tokens of {w.name}"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": w.name, "T": w.T, "hidden": w.h, "topk": w.k, "experts": w.E, "ranks": w.R,
+            "hosts": w.H, "src_ranks": w.R_src,
+            "x": "fp8 e4m3 + fp32 scale per 128 columns" if w.dtype == "fp8" else "bf16",
+            "y_out": "bf16", "routing": w.routing + (f" s={w.zipf_s}" if w.routing == "zipf" else ""),
+            "l2": "inputs larger than L2: each step streams >1 GB (y, recv) through the 129 MB L2, "
+                  "which evicts the previous step's x"}
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as ge
+    world, rank, local = dist_setup()
+    ge.build()
+    import combine_moe_layout_04_gb300 as moe
+    import moe_workloads as mw
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fp8 = w.dtype == "fp8"
+    ids = mw.gen_ids(w)
+    gates = mw.gen_gates(w)
+    prob = moe.Problem(w.T, w.h, w.k, w.E, w.R, w.P, w.R_src,
+                       moe.MOE_DTYPE_FP8_E4M3 if fp8 else moe.MOE_DTYPE_BF16)
+    lay = moe.Layout(prob, dev)
+    ws = moe.alloc_workspace(prob, dev)
+    stats = torch.empty(moe.moe_stats_words(prob), dtype=torch.int64, device=dev)
+    ids_d = torch.from_numpy(ids).to(dev)
+    gates_d = torch.from_numpy(gates).to(dev)
+    if fp8:
+        xq, xs = mw.gen_x_fp8(w)
+        x_d, xs_d = torch.from_numpy(xq).to(dev), torch.from_numpy(xs).to(dev)
+        recv = torch.empty((w.slots, w.h), dtype=torch.uint8, device=dev)
+        recv_s = torch.empty((w.slots, w.h // w.scale_group), dtype=torch.float32, device=dev)
+    else:
+        x_d = torch.from_numpy(mw.gen_x_bf16(w).view(np.int16)).to(dev).view(torch.bfloat16)
+        xs_d, recv_s = None, None
+        recv = torch.empty((w.slots, w.h), dtype=torch.bfloat16, device=dev)
+    # Expert outputs: a separate bf16 buffer for fp8 dispatch; for bf16 the
+    # experts are identities and combine reads the receive buffer.
+    y_d = mw.gen_y_device(w, dev) if fp8 else recv
+    out = torch.empty((w.T, w.h), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_layout(prob, ids_d, ws, lay, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.moe_stats(prob, lay, ws, stats, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        moe.moe_dispatch(prob, lay, x_d, xs_d, recv, recv_s, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        moe.moe_combine(prob, lay, y_d, gates_d, out, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    rc, bits = moe.moe_status(ws, stream)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"device status {bits:#x}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    time.sleep(0.5)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    h1 = time.time()
+    time.sleep(0.3)
+    sampler.stop()
+    ms_total = max_over_ranks(start.elapsed_time(end), world)
+    ms_step = ms_total / args.steps
+    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs])  # ms
+    layout_us, stats_us, dispatch_us, combine_us = (per.mean(axis=0) * 1e3).tolist()
+
+    d_bytes, c_bytes = algorithmic_bytes(w)
+    peak, peak_src = read_peak()
+    value = world * (d_bytes + c_bytes) / (ms_step * 1e-3) / 1e9
+    dc_us = dispatch_us + combine_us
+    dc_gbs = (d_bytes + c_bytes) / (dc_us * 1e-6) / 1e9
+    comb_gbs = c_bytes / (combine_us * 1e-6) / 1e9
+    traffic = read_traffic("combine_kernel", w.name)
+
+    # End to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the four calls, D2H of the combined output
+    # and the statistics record.
+    e2e_steps = min(args.steps, 30)
+    h_ids = torch.from_numpy(ids).pin_memory()
+    h_gates = torch.from_numpy(gates).pin_memory()
+    h_x = x_d.cpu().pin_memory()
+    h_xs = xs_d.cpu().pin_memory() if fp8 else None
+    h_y = y_d.cpu().pin_memory() if fp8 else None
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_stats = torch.empty(stats.shape, dtype=stats.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_gates, h_x, h_xs, h_y) if t is not None)
+    d2h = h_out.numel() * h_out.element_size() + h_stats.numel() * h_stats.element_size()
+
+    def e2e_step():
+        ids_d.copy_(h_ids, non_blocking=True)
+        gates_d.copy_(h_gates, non_blocking=True)
+        x_d.copy_(h_x, non_blocking=True)
+        if fp8:
+            xs_d.copy_(h_xs, non_blocking=True)
+            y_d.copy_(h_y, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_stats.copy_(stats, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    st = moe.decode_stats(prob, h_stats.numpy())
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(w),
+        "dispatch_us": round(dispatch_us, 2), "combine_us": round(combine_us, 2),
+        "layout_us": round(layout_us, 2), "stats_us": round(stats_us, 2), "dc_us": round(dc_us, 2),
+        "dc_gbs": round(dc_gbs, 1), "dc_frac_of_peak": round(dc_gbs / peak, 4),
+        "step_frac_of_peak": round(value / world / peak, 4),
+        "algorithmic_bytes": {"dispatch": d_bytes, "combine": c_bytes},
+        "imbalance_ratio": round(st["imbalance_ratio"], 4),
+        "roofline": {"bound": "hbm", "kernel": "combine_kernel", "achieved": round(comb_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(comb_gbs / peak, 4),
+                     "traffic": traffic, "peak_source": peak_src},
+        "e2e": {"value": round(world * (d_bytes + c_bytes) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": sampler.summary(h0, h1),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="prefill-fp8")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    import moe_workloads as mw
+    w = mw.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,239 @@
+"""Python binding of libmoe_layout.so: MoE token layout, dispatch and combine on GB300.
+
+Argument marshalling only.  Every step runs in the library's CUDA kernels
+(``csrc/``); PyTorch provides device memory and streams.  The entry points
+mirror the C-ABI declared in ``include/moe_layout.h``:
+
+    moe_workspace_bytes, moe_layout, moe_stats_words, moe_stats,
+    moe_dispatch, moe_combine, moe_status, moe_status_string
+
+``Problem`` and ``Layout`` are conveniences that build the C structs and
+allocate the caller-owned device buffers.  If the shared library has not been
+built, every call raises ``MoeLibraryMissing``; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_layout.so")
+
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_BAD_IDS, MOE_ERR_ALIGN = 0, 1, 2, 3, 4
+MOE_DTYPE_BF16, MOE_DTYPE_FP8_E4M3 = 0, 1
+MOE_STATUS_ID_RANGE, MOE_STATUS_ID_REPEAT, MOE_STATUS_PLACEMENT, MOE_STATUS_SRC_OFFSET = 1, 2, 4, 8
+MOE_FP8_GROUP = 128
+MOE_STATS_HEADER_WORDS = 32
+
+# Header word names in index order (include/moe_layout.h, MOE_ST_*).
+STATS_HEADER = ("status", "T", "slots", "row_bytes", "max_expert_count", "argmax_expert",
+                "min_expert_count", "max_rank_slots", "max_rank_tokens",
+                "sum_mode0_copies", "sum_mode1_copies", "sum_mode2_copies",
+                "max_src_mode1_copies", "max_src_mode2_copies", "max_recv_remote", "max_recv_relay",
+                "sum_naive_bytes", "sum_mode0_bytes", "sum_mode1_bytes", "sum_mode2_bytes",
+                "imbalance_ratio", "rank_imbalance", "num_hosts")
+STATS_SRC = ("src_tokens", "src_copies", "src_mode0", "src_mode1", "src_mode2",
+             "src_naive_bytes", "src_mode0_bytes", "src_mode1_bytes", "src_mode2_bytes")
+STATS_DST = ("recv_slots", "recv_tokens", "recv_self", "recv_local", "recv_remote", "recv_relay")
+EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
+            "moe_combine", "moe_status", "moe_status_string")
+
+
+class MoeLibraryMissing(RuntimeError):
+    pass
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {moe_status_string(code)} (code {code})")
+        self.code = code
+
+
+class _ProblemC(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("num_experts", ctypes.c_int32), ("num_ranks", ctypes.c_int32),
+                ("ranks_per_host", ctypes.c_int32), ("num_src_ranks", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("expert_to_rank", ctypes.c_void_p),
+                ("src_rank_offsets", ctypes.c_void_p)]
+
+
+_LAYOUT_FIELDS = ("expert_count", "expert_offset", "rank_count", "rank_offset", "host_count",
+                  "host_offset", "host_mask", "pos", "recv_src")
+
+
+class _LayoutC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _LAYOUT_FIELDS]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libmoe_layout.so (raises MoeLibraryMissing if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise MoeLibraryMissing(f"{path} is not built; run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    P, L = ctypes.POINTER(_ProblemC), ctypes.POINTER(_LayoutC)
+    lib.moe_workspace_bytes.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_workspace_bytes.restype = i
+    lib.moe_layout.argtypes = [P, vp, vp, L, vp]
+    lib.moe_layout.restype = i
+    lib.moe_stats_words.argtypes = [P]
+    lib.moe_stats_words.restype = ctypes.c_size_t
+    lib.moe_stats.argtypes = [P, L, vp, vp, vp]
+    lib.moe_stats.restype = i
+    lib.moe_dispatch.argtypes = [P, L, vp, vp, vp, vp, vp]
+    lib.moe_dispatch.restype = i
+    lib.moe_combine.argtypes = [P, L, vp, vp, vp, vp]
+    lib.moe_combine.restype = i
+    lib.moe_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.moe_status.restype = i
+    lib.moe_status_string.argtypes = [i]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+@dataclass
+class Problem:
+    """One layer's routing problem (see include/moe_layout.h, moe_problem)."""
+    num_tokens: int
+    hidden: int
+    topk: int
+    num_experts: int
+    num_ranks: int
+    ranks_per_host: int
+    num_src_ranks: int = 1
+    dtype: int = MOE_DTYPE_BF16
+    expert_to_rank: object = None      # device int32 tensor [E] or None
+    src_rank_offsets: object = None    # device int32 tensor [R_src + 1] or None
+
+    @property
+    def num_hosts(self) -> int:
+        return self.num_ranks // self.ranks_per_host
+
+    @property
+    def row_bytes(self) -> int:
+        if self.dtype == MOE_DTYPE_FP8_E4M3:
+            return self.hidden + 4 * (self.hidden // MOE_FP8_GROUP)
+        return 2 * self.hidden
+
+    def c(self) -> _ProblemC:
+        return _ProblemC(self.num_tokens, self.hidden, self.topk, self.num_experts, self.num_ranks,
+                         self.ranks_per_host, self.num_src_ranks, self.dtype,
+                         _ptr(self.expert_to_rank), _ptr(self.src_rank_offsets))
+
+
+class Layout:
+    """Caller-owned device arrays of a layout (moe_layout_t)."""
+
+    def __init__(self, problem: Problem, device="cuda"):
+        import torch
+        p = problem
+        i32 = dict(dtype=torch.int32, device=device)
+        self.expert_count = torch.empty(p.num_experts, **i32)
+        self.expert_offset = torch.empty(p.num_experts + 1, **i32)
+        self.rank_count = torch.empty(p.num_ranks, **i32)
+        self.rank_offset = torch.empty(p.num_ranks + 1, **i32)
+        self.host_count = torch.empty(p.num_hosts, **i32)
+        self.host_offset = torch.empty(p.num_hosts + 1, **i32)
+        self.host_mask = torch.empty((p.num_tokens, p.num_hosts), dtype=torch.uint8, device=device)
+        self.pos = torch.empty((p.num_tokens, p.topk), **i32)
+        self.recv_src = torch.empty(p.num_tokens * p.topk, **i32)
+
+    def c(self) -> _LayoutC:
+        return _LayoutC(*[getattr(self, n).data_ptr() for n in _LAYOUT_FIELDS])
+
+    def to_host(self) -> dict:
+        return {n: getattr(self, n).cpu().numpy() for n in _LAYOUT_FIELDS}
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def moe_status_string(code: int) -> str:
+    return load_library().moe_status_string(int(code)).decode()
+
+
+def moe_workspace_bytes(problem: Problem) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().moe_workspace_bytes(ctypes.byref(problem.c()), ctypes.byref(n)),
+           "moe_workspace_bytes")
+    return n.value
+
+
+def alloc_workspace(problem: Problem, device="cuda"):
+    import torch
+    return torch.empty(moe_workspace_bytes(problem), dtype=torch.uint8, device=device)
+
+
+def moe_layout(problem: Problem, ids, workspace, layout: Layout, stream=None):
+    _check(load_library().moe_layout(ctypes.byref(problem.c()), _ptr(ids), _ptr(workspace),
+                                     ctypes.byref(layout.c()), _stream(stream)), "moe_layout")
+
+
+def moe_stats_words(problem: Problem) -> int:
+    return int(load_library().moe_stats_words(ctypes.byref(problem.c())))
+
+
+def moe_stats(problem: Problem, layout: Layout, workspace, stats, stream=None):
+    _check(load_library().moe_stats(ctypes.byref(problem.c()), ctypes.byref(layout.c()),
+                                    _ptr(workspace), _ptr(stats), _stream(stream)), "moe_stats")
+
+
+def moe_dispatch(problem: Problem, layout: Layout, x, x_scales, recv, recv_scales, stream=None):
+    _check(load_library().moe_dispatch(ctypes.byref(problem.c()), ctypes.byref(layout.c()), _ptr(x),
+                                       _ptr(x_scales), _ptr(recv), _ptr(recv_scales), _stream(stream)),
+           "moe_dispatch")
+
+
+def moe_combine(problem: Problem, layout: Layout, y, weights, out, stream=None):
+    _check(load_library().moe_combine(ctypes.byref(problem.c()), ctypes.byref(layout.c()), _ptr(y),
+                                      _ptr(weights), _ptr(out), _stream(stream)), "moe_combine")
+
+
+def moe_status(workspace, stream=None):
+    """Synchronises the stream; returns (code, status_bits)."""
+    bits = ctypes.c_uint32(0)
+    rc = load_library().moe_status(_ptr(workspace), ctypes.byref(bits), _stream(stream))
+    return rc, bits.value
+
+
+def decode_stats(problem: Problem, stats_host) -> dict:
+    """Names the words of a statistics record copied to the host (numpy int64)."""
+    import numpy as np
+    s = np.asarray(stats_host, dtype=np.int64)
+    out = {}
+    for i, n in enumerate(STATS_HEADER):
+        out[n] = int(s[i])
+    for n in ("imbalance_ratio", "rank_imbalance"):
+        out[n] = float(np.array([out[n]], np.int64).view(np.float64)[0])
+    base = MOE_STATS_HEADER_WORDS
+    rs, r = problem.num_src_ranks, problem.num_ranks
+    for i, n in enumerate(STATS_SRC):
+        out[n] = s[base + i * rs: base + (i + 1) * rs].copy()
+    base += len(STATS_SRC) * rs
+    for i, n in enumerate(STATS_DST):
+        out[n] = s[base + i * r: base + (i + 1) * r].copy()
+    return out

@@ -1,0 +1,181 @@
+// moe_api.cu -- the extern "C" entry points of libmoe_layout.so: argument
+// checks on the host, then kernel launches on the caller's stream.  The
+// library allocates no memory and keeps no state between calls.
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe_internal.cuh"
+
+namespace {
+
+using moe::WsLayout;
+
+struct Dims {
+    int T, h, k, E, R, P, H, Rs;
+    bool fp8;
+};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_problem(const moe_problem* p, Dims* d) {
+    if (p == nullptr) return MOE_ERR_INVALID;
+    d->T = p->num_tokens; d->h = p->hidden; d->k = p->topk; d->E = p->num_experts;
+    d->R = p->num_ranks; d->P = p->ranks_per_host; d->Rs = p->num_src_ranks;
+    d->fp8 = p->dtype == MOE_DTYPE_FP8_E4M3;
+    if (p->dtype != MOE_DTYPE_BF16 && p->dtype != MOE_DTYPE_FP8_E4M3) return MOE_ERR_INVALID;
+    if (d->T < 0 || d->h <= 0) return MOE_ERR_INVALID;
+    if (d->k < 1 || d->k > MOE_MAX_TOPK) return MOE_ERR_INVALID;
+    if (d->E < 1 || d->E > MOE_MAX_EXPERTS) return MOE_ERR_INVALID;
+    if (d->R < 1 || d->R > MOE_MAX_RANKS || d->P < 1 || d->R % d->P != 0) return MOE_ERR_INVALID;
+    d->H = d->R / d->P;
+    if (d->H > MOE_MAX_HOSTS) return MOE_ERR_INVALID;
+    if (d->Rs < 1 || d->Rs > d->R) return MOE_ERR_INVALID;
+    if ((long long)d->T * d->k >= (1LL << 31)) return MOE_ERR_INVALID;
+    if (p->expert_to_rank == nullptr && d->E % d->R != 0) return MOE_ERR_INVALID;
+    if (p->src_rank_offsets == nullptr && d->T % d->Rs != 0) return MOE_ERR_INVALID;
+    if (d->fp8 ? (d->h % MOE_FP8_GROUP != 0) : (d->h % 8 != 0)) return MOE_ERR_INVALID;
+    if (!aligned(p->expert_to_rank, 4) || !aligned(p->src_rank_offsets, 4)) return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+// Arrays sized by T may be NULL when T == 0.
+bool layout_complete(const moe_layout_t* l, int T) {
+    if (!l || !l->expert_count || !l->expert_offset || !l->rank_count || !l->rank_offset ||
+        !l->host_count || !l->host_offset)
+        return false;
+    return T == 0 || (l->host_mask && l->pos && l->recv_src);
+}
+
+WsLayout ws_layout(const Dims& d) { return moe::make_ws_layout(d.T, d.E, d.R, d.H, d.Rs); }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int64_t row_bytes(const Dims& d) {
+    return d.fp8 ? (int64_t)d.h + 4LL * (d.h / MOE_FP8_GROUP) : 2LL * d.h;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_workspace_bytes(const moe_problem* problem, size_t* bytes) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (bytes == nullptr) return MOE_ERR_INVALID;
+    *bytes = ws_layout(d).total;
+    return MOE_OK;
+}
+
+size_t moe_stats_words(const moe_problem* problem) {
+    Dims d;
+    if (check_problem(problem, &d) != MOE_OK) return 0;
+    return MOE_STATS_HEADER_WORDS + (size_t)MOE_SRC_FIELDS * d.Rs + (size_t)MOE_DST_FIELDS * d.R;
+}
+
+int moe_layout(const moe_problem* problem, const int32_t* ids, void* workspace,
+               const moe_layout_t* layout, moe_stream_t stream) {
+    Dims d;
+    int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (!layout_complete(layout, d.T) || workspace == nullptr || (d.T > 0 && ids == nullptr))
+        return MOE_ERR_INVALID;
+    if (!aligned(workspace, 256) || !aligned(ids, 4)) return MOE_ERR_ALIGN;
+    moe::LayoutArgs a{};
+    a.ids = ids;
+    a.expert_to_rank = problem->expert_to_rank;
+    a.src_offsets = problem->src_rank_offsets;
+    a.T = d.T; a.k = d.k; a.E = d.E; a.R = d.R; a.P = d.P; a.H = d.H; a.Rs = d.Rs;
+    a.ws = static_cast<uint8_t*>(workspace);
+    a.wl = ws_layout(d);
+    a.out = *layout;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rc = cuda_status(cudaMemsetAsync(workspace, 0, a.wl.acc_bytes, s));
+    if (rc != MOE_OK) return rc;
+    return cuda_status(moe::launch_layout(a, s));
+}
+
+int moe_stats(const moe_problem* problem, const moe_layout_t* layout, const void* workspace,
+              int64_t* stats, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (!layout_complete(layout, d.T) || workspace == nullptr || stats == nullptr) return MOE_ERR_INVALID;
+    if (!aligned(workspace, 256) || !aligned(stats, 8)) return MOE_ERR_ALIGN;
+    moe::StatsArgs a{};
+    a.ws = static_cast<const uint8_t*>(workspace);
+    a.wl = ws_layout(d);
+    a.expert_count = layout->expert_count;
+    a.rank_count = layout->rank_count;
+    a.stats = stats;
+    a.T = d.T; a.k = d.k; a.h = d.h; a.E = d.E; a.R = d.R; a.P = d.P; a.H = d.H; a.Rs = d.Rs;
+    a.row_bytes = row_bytes(d);
+    return cuda_status(moe::launch_stats(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_dispatch(const moe_problem* problem, const moe_layout_t* layout, const void* x,
+                 const float* x_scales, void* recv, float* recv_scales, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (layout == nullptr) return MOE_ERR_INVALID;
+    if (d.T == 0) return MOE_OK;
+    if (layout->pos == nullptr || x == nullptr || recv == nullptr) return MOE_ERR_INVALID;
+    if (d.fp8 && (x_scales == nullptr || recv_scales == nullptr)) return MOE_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(layout->pos, 4)) return MOE_ERR_ALIGN;
+    if (d.fp8 && (!aligned(x_scales, 4) || !aligned(recv_scales, 4))) return MOE_ERR_ALIGN;
+    moe::MoveArgs m{};
+    m.pos = layout->pos;
+    m.T = d.T;
+    m.k = d.k;
+    m.nvec = (int)((d.fp8 ? (int64_t)d.h : 2LL * d.h) / 16);
+    const int groups = d.fp8 ? d.h / MOE_FP8_GROUP : 0;
+    return cuda_status(moe::launch_dispatch(m, x, x_scales, recv, recv_scales, groups,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_combine(const moe_problem* problem, const moe_layout_t* layout, const void* y,
+                const float* weights, void* out, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (layout == nullptr) return MOE_ERR_INVALID;
+    if (d.T == 0) return MOE_OK;
+    if (layout->pos == nullptr || y == nullptr || weights == nullptr || out == nullptr) return MOE_ERR_INVALID;
+    if (!aligned(y, 16) || !aligned(out, 16) || !aligned(weights, 4) || !aligned(layout->pos, 4))
+        return MOE_ERR_ALIGN;
+    moe::MoveArgs m{};
+    m.pos = layout->pos;
+    m.T = d.T;
+    m.k = d.k;
+    m.nvec = d.h / 8;  // combine is bf16 in and out
+    return cuda_status(moe::launch_combine(m, y, weights, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream) {
+    if (workspace == nullptr || status_bits == nullptr) return MOE_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t bits = 0;
+    // The status word sits at offset 0 of every workspace.
+    cudaError_t e = cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    *status_bits = bits;
+    if (bits & (MOE_STATUS_ID_RANGE | MOE_STATUS_ID_REPEAT)) return MOE_ERR_BAD_IDS;
+    if (bits & (MOE_STATUS_PLACEMENT | MOE_STATUS_SRC_OFFSET)) return MOE_ERR_INVALID;
+    return MOE_OK;
+}
+
+const char* moe_status_string(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID: return "invalid argument";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_BAD_IDS: return "expert id out of range or repeated within a token";
+        case MOE_ERR_ALIGN: return "misaligned buffer";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

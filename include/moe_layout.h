@@ -1,0 +1,214 @@
+/*
+ * moe_layout.h -- C-ABI of the GB300 (sm_103a) MoE token layout, dispatch
+ * and combine library (libmoe_layout.so).
+ *
+ * What it computes.  The expert-parallel all-to-all of an MoE layer sends each
+ * token to its top-k experts and brings the k expert outputs back as a
+ * gate-weighted sum ("Balancing and Beyond: Communication-Centric
+ * Optimizations in Expert Parallelism", section 1; the HybridEP issue "Poor
+ * HybridEP performance on dual-node 16x B300 GPUs" names the single-GPU halves
+ * dispatch_with_permute and combine_with_unpermute).  Here the logical EP
+ * ranks and hosts are partitions of one GPU's memory:
+ *
+ *   rank(e) = expert_to_rank ? expert_to_rank[e] : e / (E / R)
+ *   host(r) = r / P,  local index li(r) = r % P,  H = R / P
+ *   src(t)  = source rank of token t (tokens split over ranks 0..R_src-1)
+ *
+ * Call order per MoE layer: moe_layout -> (moe_stats) -> moe_dispatch ->
+ * [experts] -> moe_combine.  All calls are asynchronous on the given stream;
+ * only moe_status synchronises it.
+ *
+ * Memory.  The caller allocates every buffer (device memory unless stated)
+ * and the workspace; the library allocates nothing, keeps no state between
+ * calls and never frees.  Inputs must stay valid until the stream has run the
+ * work.  A workspace may be reused by later calls on the same stream; two
+ * calls that may run concurrently need two workspaces.
+ *
+ * Errors.  Every entry point returns a moe_status code.  Arguments that the
+ * host can check (sizes, NULL or misaligned pointers) are rejected before any
+ * work is enqueued.  Data-dependent faults found on the device (an expert id
+ * out of [0, E), an id repeated within a token, a placement entry out of
+ * [0, R), bad source offsets) never fault the GPU: they set bits of a status
+ * word in the workspace, the affected slot is placed as if it were expert 0 so
+ * that every write stays in bounds, and moe_status reports them.
+ */
+#ifndef MOE_LAYOUT_H
+#define MOE_LAYOUT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = 1,   /* bad sizes, NULL pointers, bad placement/offsets */
+    MOE_ERR_CUDA = 2,      /* a CUDA launch or copy failed */
+    MOE_ERR_BAD_IDS = 3,   /* an expert id out of [0, E) or repeated in a row */
+    MOE_ERR_ALIGN = 4      /* a row buffer is not 16-byte aligned */
+} moe_status_code;
+
+typedef enum {
+    MOE_DTYPE_BF16 = 0,      /* rows of h bf16 values */
+    MOE_DTYPE_FP8_E4M3 = 1   /* rows of h e4m3 bytes + h/128 fp32 scales */
+} moe_dtype;
+
+/* Device status-word bits reported by moe_status. */
+#define MOE_STATUS_ID_RANGE   0x1u   /* id < 0 or id >= E */
+#define MOE_STATUS_ID_REPEAT  0x2u   /* the same id twice in one token */
+#define MOE_STATUS_PLACEMENT  0x4u   /* expert_to_rank[e] outside [0, R) */
+#define MOE_STATUS_SRC_OFFSET 0x8u   /* src_rank_offsets not ascending 0..T */
+
+/* Limits checked on the host. */
+#define MOE_MAX_TOPK     32
+#define MOE_MAX_EXPERTS  1024
+#define MOE_MAX_RANKS    1024
+#define MOE_MAX_HOSTS    64
+#define MOE_FP8_GROUP    128   /* columns per fp32 scale */
+
+/* The problem, fixed for one layer.  Sizes:
+ *   num_tokens T >= 0, hidden h > 0 (bf16: h % 8 == 0; fp8: h % 128 == 0),
+ *   topk k in [1, 32], num_experts E in [1, 1024], num_ranks R in [1, 1024],
+ *   ranks_per_host P with R % P == 0 and R / P <= 64,
+ *   num_src_ranks R_src in [1, R], T * k < 2^31.
+ * expert_to_rank: device int32 [E] or NULL (then E % R == 0, contiguous
+ *   blocks of E/R experts per rank).
+ * src_rank_offsets: device int32 [R_src + 1], ascending, 0 .. T, or NULL
+ *   (then T % R_src == 0 and each source rank owns T / R_src tokens). */
+typedef struct moe_problem {
+    int32_t num_tokens;
+    int32_t hidden;
+    int32_t topk;
+    int32_t num_experts;
+    int32_t num_ranks;
+    int32_t ranks_per_host;
+    int32_t num_src_ranks;
+    int32_t dtype;                      /* moe_dtype */
+    const int32_t* expert_to_rank;      /* device [E] or NULL */
+    const int32_t* src_rank_offsets;    /* device [R_src + 1] or NULL */
+} moe_problem;
+
+/* Layout outputs, all caller-allocated device arrays (int32 unless noted).
+ * Receive order: the T*k slots (t, j) stably sorted by (rank(e), e), so each
+ * rank's rows and, inside it, each expert's rows are contiguous and an
+ * expert's rows keep ascending token order. */
+typedef struct moe_layout_t {
+    int32_t* expert_count;   /* [E]   slots routed to expert e */
+    int32_t* expert_offset;  /* [E+1] first receive row of expert e; [E] = T*k */
+    int32_t* rank_count;     /* [R]   slots received by rank r */
+    int32_t* rank_offset;    /* [R+1] exclusive scan of rank_count */
+    int32_t* host_count;     /* [H]   tokens with host_mask[t][H] = 1 (one
+                                      network copy per token and host) */
+    int32_t* host_offset;    /* [H+1] exclusive scan of host_count */
+    uint8_t* host_mask;      /* [T, H] u8: 1 iff some slot of t goes to host H */
+    int32_t* pos;            /* [T, k] receive row of slot (t, j) */
+    int32_t* recv_src;       /* [T*k]  t*k + j of the slot held by each row */
+} moe_layout_t;
+
+/* Bytes of workspace needed for a problem ("Balancing and Beyond" section
+ * 3.4 sizes receive buffers batch x k; the workspace holds only counters and
+ * per-block tables, a few hundred KB at T = 16384).  Returns MOE_ERR_INVALID
+ * for a bad problem. */
+int moe_workspace_bytes(const moe_problem* problem, size_t* bytes);
+
+/* Layout (counts, exclusive offsets, per-(token, host) de-duplication mask,
+ * stable receive positions and their inverse) of the routing ids.
+ *   ids: device int32 [T, k], k distinct experts per token
+ *        ("Balancing and Beyond" section 3.2: k distinct experts).
+ *   workspace: device, moe_workspace_bytes() bytes, 256-byte aligned; it also
+ *        keeps the counters moe_stats reads, until the next moe_layout.
+ * The mask implements Mode 2 de-redundancy (section 3.2): one copy per token
+ * and host, relayed through the same-index GPU of that host. */
+int moe_layout(const moe_problem* problem, const int32_t* ids, void* workspace,
+               const moe_layout_t* layout, moe_stream_t stream);
+
+/* Words (int64) of the statistics record of a problem:
+ * MOE_STATS_HEADER_WORDS + 9 * R_src + 6 * R. */
+size_t moe_stats_words(const moe_problem* problem);
+
+/* Statistics of the last moe_layout run with this workspace, written to a
+ * device int64 array of moe_stats_words() words (copy it to the host to read).
+ * Header word indices are MOE_ST_*; the two ratios are IEEE doubles stored in
+ * int64 words.  Then nine per-source-rank blocks of R_src words
+ * (MOE_SRC_*), then six per-destination-rank blocks of R words (MOE_DST_*).
+ * Definitions ("Balancing and Beyond": section 2 imbalance ratio = busiest
+ * expert over the layer mean; section 3.2 and Panel 1: Mode 0 sends every copy
+ * that leaves the GPU, Mode 1 one network copy per expert on another host,
+ * Mode 2 one network copy per other host holding any of the token's experts;
+ * section 1: tokens x k x h x 2 B; "Profiling when rank unbalance": tokens a
+ * rank receives from its own host and from the others):
+ *   row bytes rho = 2h (bf16) or h + 4h/128 (fp8 payload + scales);
+ *   src_modeX_bytes = src_modeX * rho; src_naive_bytes = tokens * k * h * 2;
+ *   recv_self / recv_local / recv_remote = slots rank r receives from itself /
+ *   from other ranks of its host / from other hosts; recv_relay = Mode 2
+ *   network copies landing on r as the same-index relay GPU. */
+#define MOE_STATS_HEADER_WORDS 32
+enum {
+    MOE_ST_STATUS = 0,          /* device status bits (MOE_STATUS_*) */
+    MOE_ST_TOKENS,              /* T */
+    MOE_ST_SLOTS,               /* T*k */
+    MOE_ST_ROW_BYTES,           /* rho */
+    MOE_ST_MAX_EXPERT,          /* max_e expert_count */
+    MOE_ST_ARGMAX_EXPERT,       /* smallest e attaining the max */
+    MOE_ST_MIN_EXPERT,          /* min_e expert_count */
+    MOE_ST_MAX_RANK_SLOTS,      /* max_r rank_count */
+    MOE_ST_MAX_RANK_TOKENS,     /* max_r distinct tokens received */
+    MOE_ST_SUM_MODE0,           /* sum over source ranks of Mode 0 copies */
+    MOE_ST_SUM_MODE1,
+    MOE_ST_SUM_MODE2,
+    MOE_ST_MAX_SRC_MODE1,       /* straggler view: busiest sender */
+    MOE_ST_MAX_SRC_MODE2,
+    MOE_ST_MAX_RECV_REMOTE,     /* busiest network receiver, Mode 1 */
+    MOE_ST_MAX_RECV_RELAY,      /* busiest network receiver, Mode 2 */
+    MOE_ST_SUM_NAIVE_BYTES,
+    MOE_ST_SUM_MODE0_BYTES,
+    MOE_ST_SUM_MODE1_BYTES,
+    MOE_ST_SUM_MODE2_BYTES,
+    MOE_ST_IMBALANCE_RATIO,     /* double: max expert count / (T*k/E) */
+    MOE_ST_RANK_IMBALANCE,      /* double: max rank slots / (T*k/R) */
+    MOE_ST_NUM_HOSTS            /* H */
+};
+enum { MOE_SRC_TOKENS = 0, MOE_SRC_COPIES, MOE_SRC_MODE0, MOE_SRC_MODE1, MOE_SRC_MODE2,
+       MOE_SRC_NAIVE_BYTES, MOE_SRC_MODE0_BYTES, MOE_SRC_MODE1_BYTES, MOE_SRC_MODE2_BYTES,
+       MOE_SRC_FIELDS };
+enum { MOE_DST_SLOTS = 0, MOE_DST_TOKENS, MOE_DST_SELF, MOE_DST_LOCAL, MOE_DST_REMOTE,
+       MOE_DST_RELAY, MOE_DST_FIELDS };
+
+int moe_stats(const moe_problem* problem, const moe_layout_t* layout,
+              const void* workspace, int64_t* stats, moe_stream_t stream);
+
+/* Dispatch-permute: for every slot, recv[pos[t, j]] = x[t] (a byte-exact row
+ * copy); for fp8 also recv_scales[pos[t, j]] = x_scales[t].
+ *   x: [T, h] bf16 or e4m3 bytes; x_scales: fp32 [T, h/128] (fp8) or NULL;
+ *   recv: [T*k, h]; recv_scales: fp32 [T*k, h/128] (fp8) or NULL.
+ * x and recv must be 16-byte aligned (MOE_ERR_ALIGN otherwise); scale arrays
+ * 4-byte aligned.  Only pos is read from the layout. */
+int moe_dispatch(const moe_problem* problem, const moe_layout_t* layout,
+                 const void* x, const float* x_scales,
+                 void* recv, float* recv_scales, moe_stream_t stream);
+
+/* Combine-unpermute: out[t] = bf16_rne(sum over j = 0..k-1, in ascending j,
+ * of w[t, j] * y[pos[t, j]]) with one fp32 fma per term starting from 0.0f.
+ *   y: bf16 [T*k, h] expert outputs in receive order; weights: fp32 [T, k];
+ *   out: bf16 [T, h].  y and out 16-byte aligned.  Only pos is read from the
+ * layout. */
+int moe_combine(const moe_problem* problem, const moe_layout_t* layout,
+                const void* y, const float* weights, void* out, moe_stream_t stream);
+
+/* Waits for the stream, then reads the device status bits of the workspace
+ * (the faults found by the last moe_layout).  *status_bits receives them;
+ * returns MOE_OK, MOE_ERR_BAD_IDS, MOE_ERR_INVALID or MOE_ERR_CUDA. */
+int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream);
+
+/* A short English description of a moe_status_code. */
+const char* moe_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

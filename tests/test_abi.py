@@ -1,0 +1,105 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry
+point, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_layout.h")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from combine_moe_layout_04_gb300 import _build
+    _build.build()
+    import combine_moe_layout_04_gb300 as m
+    m.load_library()
+    return m
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
+              "moe_combine", "moe_status", "moe_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(moe):
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert set(moe.EXPORTED) <= set(_declared())
+
+
+def test_status_strings(moe):
+    assert moe.moe_status_string(0) == "ok"
+    assert "misaligned" in moe.moe_status_string(moe.MOE_ERR_ALIGN)
+    assert moe.moe_status_string(1234) == "unknown status"
+
+
+def _p(moe, **kw):
+    base = dict(num_tokens=256, hidden=1024, topk=2, num_experts=16, num_ranks=4, ranks_per_host=2,
+                num_src_ranks=4, dtype=moe.MOE_DTYPE_BF16)
+    base.update(kw)
+    return moe.Problem(**base)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(topk=0), dict(topk=33), dict(num_experts=1025), dict(num_ranks=3, ranks_per_host=2),
+    dict(num_ranks=1024, ranks_per_host=8), dict(num_src_ranks=5), dict(num_experts=18),
+    dict(num_tokens=250), dict(hidden=1020), dict(dtype=1, hidden=1000), dict(dtype=7),
+    dict(num_tokens=1 << 28, topk=8, num_src_ranks=1), dict(num_tokens=-1)])
+def test_host_rejects_bad_problems(moe, bad):
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_workspace_bytes(_p(moe, **bad))
+    assert ei.value.code == moe.MOE_ERR_INVALID
+    assert moe.moe_stats_words(_p(moe, **bad)) == 0
+
+
+def test_workspace_and_stats_sizes(moe):
+    p = _p(moe)
+    n = moe.moe_workspace_bytes(p)
+    assert n % 256 == 0 and 0 < n < 1 << 20
+    assert moe.moe_stats_words(p) == 32 + 9 * 4 + 6 * 4
+    big = _p(moe, num_tokens=16384, hidden=7168, topk=8, num_experts=128, num_ranks=16,
+             ranks_per_host=8, num_src_ranks=1, dtype=moe.MOE_DTYPE_FP8_E4M3)
+    assert moe.moe_workspace_bytes(big) < 1 << 20
+
+
+class _Fake:
+    """A pointer-shaped stand-in: the host checks below must reject the call
+    from the address alone, before any device access."""
+    def __init__(self, addr):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
+
+
+def test_host_rejects_misaligned_rows(moe):
+    p = _p(moe)
+    lay = moe.Layout.__new__(moe.Layout)
+    for n in moe._LAYOUT_FIELDS:
+        setattr(lay, n, _Fake(0x10000))
+    good, odd = _Fake(0x20000), _Fake(0x20008)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_dispatch(p, lay, odd, None, good, None, stream=0)
+    assert ei.value.code == moe.MOE_ERR_ALIGN
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_combine(p, lay, good, _Fake(0x30000), odd, stream=0)
+    assert ei.value.code == moe.MOE_ERR_ALIGN
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layout(p, _Fake(0x40000), _Fake(0x50010), lay, stream=0)
+    assert ei.value.code == moe.MOE_ERR_ALIGN
+    pf = _p(moe, dtype=moe.MOE_DTYPE_FP8_E4M3)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_dispatch(pf, lay, good, None, good, None, stream=0)   # fp8 needs scales
+    assert ei.value.code == moe.MOE_ERR_INVALID
