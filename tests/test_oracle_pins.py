@@ -287,8 +287,12 @@ def test_combine_unit_weights_identity_experts(oracle_mod, k):
     x = mw.gen_x_bf16(w)
     recv = oracle_mod.dispatch(prob, lay["pos"], x)
     out = oracle_mod.combine(prob, lay["pos"], recv, np.ones((w.T, k), np.float32))
-    want = mw.f32_to_bf16_bits(mw.bf16_bits_to_f32(x) * np.float32(k))
-    assert np.array_equal(out, want)
+    want = mw.bf16_bits_to_f32(x) * np.float32(k)
+    # equal as values (an input -0.0 sums to +0.0 from the +0.0 start)
+    assert np.array_equal(mw.bf16_bits_to_f32(out), want)
+    neg0 = oracle_mod.combine(prob, lay["pos"][:1], np.full((w.slots, w.h), 0x8000, np.uint16),
+                              np.ones((1, k), np.float32))
+    assert np.all(neg0[0] == 0x0000)
 
 
 def test_combine_k1_is_a_gather(oracle_mod):
