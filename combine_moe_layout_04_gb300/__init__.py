@@ -21,7 +21,8 @@ from typing import Optional
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_layout.so")
 
-MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_BAD_IDS, MOE_ERR_ALIGN = 0, 1, 2, 3, 4
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_BAD_IDS, MOE_ERR_ALIGN, MOE_ERR_CAPACITY = 0, 1, 2, 3, 4, 5
+MOE_NOALLOC_SCRATCH_BYTES = 2 << 20
 MOE_DTYPE_BF16, MOE_DTYPE_FP8_E4M3 = 0, 1
 MOE_STATUS_ID_RANGE, MOE_STATUS_ID_REPEAT, MOE_STATUS_PLACEMENT, MOE_STATUS_SRC_OFFSET = 1, 2, 4, 8
 MOE_FP8_GROUP = 128
@@ -38,7 +39,7 @@ STATS_SRC = ("src_tokens", "src_copies", "src_mode0", "src_mode1", "src_mode2",
              "src_naive_bytes", "src_mode0_bytes", "src_mode1_bytes", "src_mode2_bytes")
 STATS_DST = ("recv_slots", "recv_tokens", "recv_self", "recv_local", "recv_remote", "recv_relay")
 EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
-            "moe_combine", "moe_status", "moe_status_string")
+            "moe_combine", "moe_status", "moe_status_string", "moe_layout_noalloc")
 
 
 class MoeLibraryMissing(RuntimeError):
@@ -94,6 +95,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_combine.restype = i
     lib.moe_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.moe_status.restype = i
+    lib.moe_layout_noalloc.argtypes = [P, vp, L, vp]
+    lib.moe_layout_noalloc.restype = i
     lib.moe_status_string.argtypes = [i]
     lib.moe_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -191,6 +194,15 @@ def alloc_workspace(problem: Problem, device="cuda"):
 def moe_layout(problem: Problem, ids, workspace, layout: Layout, stream=None):
     _check(load_library().moe_layout(ctypes.byref(problem.c()), _ptr(ids), _ptr(workspace),
                                      ctypes.byref(layout.c()), _stream(stream)), "moe_layout")
+
+
+def moe_layout_noalloc(problem: Problem, ids, layout: Layout, stream=None):
+    """moe_layout without a workspace: the library's fixed device scratch is
+    used instead (for callers that cannot allocate device memory).  Calls that
+    may overlap on the GPU share that scratch and must be serialised."""
+    _check(load_library().moe_layout_noalloc(ctypes.byref(problem.c()), _ptr(ids),
+                                             ctypes.byref(layout.c()), _stream(stream)),
+           "moe_layout_noalloc")
 
 
 def moe_stats_words(problem: Problem) -> int:

@@ -174,6 +174,7 @@ const char* moe_status_string(int code) {
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_BAD_IDS: return "expert id out of range or repeated within a token";
         case MOE_ERR_ALIGN: return "misaligned buffer";
+        case MOE_ERR_CAPACITY: return "problem too large for the fixed layout scratch";
         default: return "unknown status";
     }
 }

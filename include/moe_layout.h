@@ -50,7 +50,9 @@ typedef enum {
     MOE_ERR_INVALID = 1,   /* bad sizes, NULL pointers, bad placement/offsets */
     MOE_ERR_CUDA = 2,      /* a CUDA launch or copy failed */
     MOE_ERR_BAD_IDS = 3,   /* an expert id out of [0, E) or repeated in a row */
-    MOE_ERR_ALIGN = 4      /* a row buffer is not 16-byte aligned */
+    MOE_ERR_ALIGN = 4,     /* a row buffer is not 16-byte aligned */
+    MOE_ERR_CAPACITY = 5   /* the problem needs more scratch than
+                              moe_layout_noalloc's fixed buffer holds */
 } moe_status_code;
 
 typedef enum {
@@ -204,6 +206,34 @@ int moe_combine(const moe_problem* problem, const moe_layout_t* layout,
  * (the faults found by the last moe_layout).  *status_bits receives them;
  * returns MOE_OK, MOE_ERR_BAD_IDS, MOE_ERR_INVALID or MOE_ERR_CUDA. */
 int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream);
+
+/* Layout without a caller workspace -- this entry point has no counterpart
+ * on the pages; it exists for callers that cannot allocate device memory,
+ * such as a plugin inside an inference engine whose device memory the engine
+ * plans and owns, or a plain C caller with no device allocator (cudaMalloc
+ * also synchronises the device, which a hot path cannot afford).
+ *
+ * It computes exactly what moe_layout computes, but its scratch is a fixed
+ * MOE_NOALLOC_SCRATCH_BYTES array inside the library's own device memory,
+ * which every GPU that loads the library holds until the process exits.  It
+ * allocates nothing and frees nothing.
+ *   - Returns MOE_ERR_CAPACITY, before any work is enqueued, when the
+ *     problem's moe_workspace_bytes() exceeds MOE_NOALLOC_SCRATCH_BYTES
+ *     (2 MiB: enough for T = 65536 tokens with E = 256 experts).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls in the process share the one array per device.  Two calls
+ *     that may overlap on the GPU (different streams, or different host
+ *     threads) race on it and corrupt each other's layout; serialise them.
+ *     Each call clears the counters it needs, so stale contents from an
+ *     earlier call do no harm.
+ *   - This variant does not report the device status bits (an id out of
+ *     range or repeated still cannot write out of bounds); validate the ids
+ *     upstream, or use moe_layout with a workspace and moe_status. */
+#define MOE_NOALLOC_SCRATCH_BYTES (2u << 20)
+int moe_layout_noalloc(const moe_problem* problem, const int32_t* ids,
+                       const moe_layout_t* layout, moe_stream_t stream);
 
 /* A short English description of a moe_status_code. */
 const char* moe_status_string(int code);
