@@ -27,6 +27,7 @@ MOE_DTYPE_BF16, MOE_DTYPE_FP8_E4M3 = 0, 1
 MOE_STATUS_ID_RANGE, MOE_STATUS_ID_REPEAT, MOE_STATUS_PLACEMENT, MOE_STATUS_SRC_OFFSET = 1, 2, 4, 8
 MOE_FP8_GROUP = 128
 MOE_STATS_HEADER_WORDS = 32
+MOE_FAULT_WAIT_TIMEOUT = 1
 
 # Header word names in index order (include/moe_layout.h, MOE_ST_*).
 STATS_HEADER = ("status", "T", "slots", "row_bytes", "max_expert_count", "argmax_expert",
@@ -39,7 +40,8 @@ STATS_SRC = ("src_tokens", "src_copies", "src_mode0", "src_mode1", "src_mode2",
              "src_naive_bytes", "src_mode0_bytes", "src_mode1_bytes", "src_mode2_bytes")
 STATS_DST = ("recv_slots", "recv_tokens", "recv_self", "recv_local", "recv_remote", "recv_relay")
 EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
-            "moe_combine", "moe_status", "moe_status_string", "moe_layout_noalloc")
+            "moe_combine", "moe_status", "moe_status_string", "moe_layout_noalloc",
+            "moe_move_faults")
 
 
 class MoeLibraryMissing(RuntimeError):
@@ -97,6 +99,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_status.restype = i
     lib.moe_layout_noalloc.argtypes = [P, vp, L, vp]
     lib.moe_layout_noalloc.restype = i
+    lib.moe_move_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.moe_move_faults.restype = i
     lib.moe_status_string.argtypes = [i]
     lib.moe_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -230,6 +234,13 @@ def moe_status(workspace, stream=None):
     bits = ctypes.c_uint32(0)
     rc = load_library().moe_status(_ptr(workspace), ctypes.byref(bits), _stream(stream))
     return rc, bits.value
+
+
+def moe_move_faults(stream=None) -> int:
+    """Synchronises the stream; returns and clears the row movers' fault bits."""
+    bits = ctypes.c_uint32(0)
+    _check(load_library().moe_move_faults(ctypes.byref(bits), _stream(stream)), "moe_move_faults")
+    return bits.value
 
 
 def decode_stats(problem: Problem, stats_host) -> dict:

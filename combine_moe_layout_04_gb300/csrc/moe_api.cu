@@ -87,6 +87,8 @@ int moe_layout(const moe_problem* problem, const int32_t* ids, void* workspace,
     a.expert_to_rank = problem->expert_to_rank;
     a.src_offsets = problem->src_rank_offsets;
     a.T = d.T; a.k = d.k; a.E = d.E; a.R = d.R; a.P = d.P; a.H = d.H; a.Rs = d.Rs;
+    a.h = d.h;
+    a.row_bytes = row_bytes(d);
     a.ws = static_cast<uint8_t*>(workspace);
     a.wl = ws_layout(d);
     a.out = *layout;
@@ -103,15 +105,10 @@ int moe_stats(const moe_problem* problem, const moe_layout_t* layout, const void
     if (rc != MOE_OK) return rc;
     if (!layout_complete(layout, d.T) || workspace == nullptr || stats == nullptr) return MOE_ERR_INVALID;
     if (!aligned(workspace, 256) || !aligned(stats, 8)) return MOE_ERR_ALIGN;
-    moe::StatsArgs a{};
-    a.ws = static_cast<const uint8_t*>(workspace);
-    a.wl = ws_layout(d);
-    a.expert_count = layout->expert_count;
-    a.rank_count = layout->rank_count;
-    a.stats = stats;
-    a.T = d.T; a.k = d.k; a.h = d.h; a.E = d.E; a.R = d.R; a.P = d.P; a.H = d.H; a.Rs = d.Rs;
-    a.row_bytes = row_bytes(d);
-    return cuda_status(moe::launch_stats(a, reinterpret_cast<cudaStream_t>(stream)));
+    // The layout kernels leave the finished record in the workspace.
+    const WsLayout wl = ws_layout(d);
+    return cuda_status(moe::launch_stats_copy(static_cast<const uint8_t*>(workspace), wl, stats,
+                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_dispatch(const moe_problem* problem, const moe_layout_t* layout, const void* x,
@@ -165,6 +162,11 @@ int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream
     if (bits & (MOE_STATUS_ID_RANGE | MOE_STATUS_ID_REPEAT)) return MOE_ERR_BAD_IDS;
     if (bits & (MOE_STATUS_PLACEMENT | MOE_STATUS_SRC_OFFSET)) return MOE_ERR_INVALID;
     return MOE_OK;
+}
+
+int moe_move_faults(uint32_t* bits, moe_stream_t stream) {
+    if (bits == nullptr) return MOE_ERR_INVALID;
+    return cuda_status(moe::read_move_faults(bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 const char* moe_status_string(int code) {

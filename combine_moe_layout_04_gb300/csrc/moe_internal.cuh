@@ -5,6 +5,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
+#include <unordered_map>
 #include <cuda_runtime.h>
 
 #include "../../include/moe_layout.h"
@@ -20,44 +22,52 @@ constexpr int kRankWarps = kRankThreads / 32;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Blocks of the counting pass are gathered in groups of kLayoutGroup: the
+// ranking pass finds a block's prefix from the totals of the groups before it
+// plus at most kLayoutGroup - 1 single-block counts.
+constexpr int kLayoutGroup = 16;
+
 // Byte offsets of the workspace regions.  [0, acc_bytes) is cleared before
-// every layout; the per-block tables follow.
+// every layout; the per-block table follows.
 struct WsLayout {
-    size_t status, done;                            // u32 words
-    size_t ecount, hcount;                          // int32 [E], [H]
+    size_t status;                                  // u32 device status bits
+    size_t hcount;                                  // int32 [H]
     size_t src_tokens, src_mode0, src_mode1, src_mode2;            // int32 [R_src]
     size_t dst_tokens, dst_self, dst_local, dst_remote, dst_relay;  // int32 [R]
+    size_t group;   // int32 [G][E]  per-group expert counts, G = ceil(B / kLayoutGroup)
     size_t acc_bytes;
-    size_t agg;     // int32 [B][E]  per-block expert counts (counting pass)
-    size_t incl;    // int32 [B][E]  inclusive prefixes published by ranking blocks
-    size_t ready;   // u32   [B]     1 once a block's inclusive prefixes are visible
+    size_t agg;     // int32 [B][E]  per-block expert counts (fully rewritten each call)
+    size_t stats;   // int64 [stats_words]  statistics record of the last layout
+    size_t stats_words;
     size_t total;
     int blocks;     // B
+    int groups;     // G
 };
 
 inline WsLayout make_ws_layout(int T, int E, int R, int H, int Rs) {
     WsLayout w{};
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 16); return at; };
+    w.blocks = T > 0 ? (T + kLayoutTokensPerBlock - 1) / kLayoutTokensPerBlock : 1;
+    w.groups = (w.blocks + kLayoutGroup - 1) / kLayoutGroup;
     w.status = take(4);
-    w.done = take(4);
-    w.ecount = take(4 * (size_t)E);
     w.hcount = take(4 * (size_t)H);
-    w.src_tokens = take(4 * (size_t)Rs);
-    w.src_mode0 = take(4 * (size_t)Rs);
-    w.src_mode1 = take(4 * (size_t)Rs);
-    w.src_mode2 = take(4 * (size_t)Rs);
-    w.dst_tokens = take(4 * (size_t)R);
-    w.dst_self = take(4 * (size_t)R);
-    w.dst_local = take(4 * (size_t)R);
-    w.dst_remote = take(4 * (size_t)R);
-    w.dst_relay = take(4 * (size_t)R);
+    // The four per-source and the five per-destination arrays are contiguous.
+    w.src_tokens = take(4 * 4 * (size_t)Rs);
+    w.src_mode0 = w.src_tokens + 4 * (size_t)Rs;
+    w.src_mode1 = w.src_tokens + 8 * (size_t)Rs;
+    w.src_mode2 = w.src_tokens + 12 * (size_t)Rs;
+    w.dst_tokens = take(5 * 4 * (size_t)R);
+    w.dst_self = w.dst_tokens + 4 * (size_t)R;
+    w.dst_local = w.dst_tokens + 8 * (size_t)R;
+    w.dst_remote = w.dst_tokens + 12 * (size_t)R;
+    w.dst_relay = w.dst_tokens + 16 * (size_t)R;
+    w.group = take(4 * (size_t)w.groups * E);
     w.acc_bytes = o;
     o = align_up(o, 256);
-    w.blocks = T > 0 ? (T + kLayoutTokensPerBlock - 1) / kLayoutTokensPerBlock : 1;
     w.agg = take(4 * (size_t)w.blocks * E);
-    w.incl = take(4 * (size_t)w.blocks * E);
-    w.ready = take(4 * (size_t)w.blocks);
+    w.stats_words = MOE_STATS_HEADER_WORDS + (size_t)MOE_SRC_FIELDS * Rs + (size_t)MOE_DST_FIELDS * R;
+    w.stats = take(8 * w.stats_words);
     w.total = align_up(o, 256);
     return w;
 }
@@ -68,19 +78,11 @@ struct LayoutArgs {
     const int32_t* expert_to_rank;
     const int32_t* src_offsets;
     int T, k, E, R, P, H, Rs;
+    int h;                // hidden size, for the byte statistics
+    int64_t row_bytes;    // rho: bytes a dispatched row moves
     uint8_t* ws;
     WsLayout wl;
     moe_layout_t out;
-};
-
-struct StatsArgs {
-    const uint8_t* ws;
-    WsLayout wl;
-    const int32_t* expert_count;
-    const int32_t* rank_count;
-    int64_t* stats;
-    int T, k, h, E, R, P, H, Rs;
-    int64_t row_bytes;
 };
 
 struct MoveArgs {
@@ -99,27 +101,6 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-
-// L2-only load: never served from a possibly stale L1 line.
-__device__ __forceinline__ int32_t ld_cg(const int32_t* p) {
-    int32_t v;
-    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_cg(int32_t* p, int32_t v) {
-    asm volatile("st.global.cg.s32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-
 // Streaming 16-byte load through the non-coherent path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) {
     uint4 v;
@@ -133,6 +114,100 @@ __device__ __forceinline__ void st_v4(uint4* p, uint4 v) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// ---- bulk (TMA) copies and shared-memory barriers -------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for a barrier phase, giving up after limit_ns of wall time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u) {
+            const uint64_t now = globaltimer_ns();
+            if (it == 0u) t0 = now;
+            else if (now - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// Global -> shared bulk copy completing on a barrier (bytes: multiple of 16,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// Shared -> global bulk copy in this thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst), "r"(src_smem), "r"(bytes) : "memory");
+}
+// An L2 policy that evicts the lines it touches first (for data that is not
+// read again soon), and the bulk copies that take it.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t bar,
+                                              uint64_t pol) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void bulk_s2g_hint(void* dst, uint32_t src_smem, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 :: "l"(dst), "r"(src_smem), "r"(bytes), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue, and wait for the previous kernel's results.
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -142,13 +217,85 @@ __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Launches a kernel that may start while the previous kernel in the stream is
+// still running (programmatic dependent launch); the kernel calls pdl_wait()
+// before it reads anything the previous kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---- per-device launch facts, looked up once ------------------------------
+
+// Streaming multiprocessors of the current device.
+inline int device_sm_count() {
+    static std::mutex mu;
+    static std::unordered_map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    sms = sms > 0 ? sms : 1;
+    cache[dev] = sms;
+    return sms;
+}
+
+// Allows `kernel` at least `bytes` of dynamic shared memory on the current
+// device (the attribute is set only when it has to grow).
+inline cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    static std::mutex mu;
+    static std::unordered_map<const void*, std::unordered_map<int, size_t>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& have = done[kernel][dev];
+    if (have >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) have = bytes;
+    return e;
+}
+
+// Resident blocks per SM of `kernel` at the given block size (cached).
+inline int blocks_per_sm(const void* kernel, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::unordered_map<const void*, std::unordered_map<int, int>> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    auto& per_dev = cache[kernel];
+    auto it = per_dev.find(dev);
+    if (it != per_dev.end()) return it->second;
+    int n = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+    n = n > 0 ? n : 1;
+    per_dev[dev] = n;
+    return n;
+}
+
 // ---- launchers (defined in the kernel files) -----------------------------
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s);
-cudaError_t launch_stats(const StatsArgs& a, cudaStream_t s);
+cudaError_t launch_stats_copy(const uint8_t* ws, const WsLayout& wl, int64_t* out, cudaStream_t s);
 cudaError_t launch_dispatch(const MoveArgs& m, const void* x, const float* xs, void* recv,
                             float* rs, int groups, cudaStream_t s);
 cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, void* out,
                            cudaStream_t s);
+cudaError_t read_move_faults(uint32_t* bits, cudaStream_t s);
 
 }  // namespace moe

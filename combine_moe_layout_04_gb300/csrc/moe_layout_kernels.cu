@@ -5,20 +5,25 @@
 // ("Balancing and Beyond", section 3.2: one network copy per token and remote
 // host, relayed through the same-index GPU).  Two kernels:
 //
-//  count  one thread per token, 128 tokens per block.  Warp-aggregated
-//         (__match_any_sync) expert histogram in shared memory; host mask;
-//         the per-rank counters the statistics need.  Each block publishes its
-//         expert histogram to a [B][E] table and adds it to global totals; the
-//         last block to finish turns the totals into rank/expert/host offsets.
+//  count  one thread per token, 128 tokens per block.  A token's k ids stay in
+//         registers.  Every counter is aggregated across the warp before it
+//         touches shared memory: __match_any_sync groups equal experts and
+//         equal (category, rank) keys, ballots count hosts, shuffles reduce
+//         the per-source-rank counts.  Each block publishes its expert
+//         histogram to a [B][E] table and adds it to the totals of its group
+//         of 16 blocks (16 atomics per counter instead of B).
 //  rank   256 threads per 128-token block.  Each warp ranks a contiguous run
 //         of slots with __match_any_sync + popc (a stable rank inside the
-//         warp), warps are combined by an exclusive scan in shared memory, and
-//         blocks by a decoupled look-back over the per-block tables.  Because
-//         the count kernel has already published every block's aggregate, the
-//         look-back never waits: it walks back to the nearest block whose
-//         inclusive prefix is published and adds the aggregates in between.
-//         The kernel starts early under programmatic dependent launch and does
-//         its id-only ranking before it waits for the count kernel.
+//         warp); warps are combined by an exclusive scan in shared memory.  A
+//         block's prefix over earlier blocks is the sum of the group totals
+//         before its group and of at most 15 single-block counts, loaded in
+//         parallel: no block waits on another.  Every block derives the
+//         expert totals (the sum of the group rows) and the expert and rank
+//         offsets itself (cheap: O(E + R)); block 0 writes them out and also
+//         writes the statistics record into the workspace, so moe_stats is a
+//         plain copy.  The kernel starts early under
+//         programmatic dependent launch and ranks its slots (ids only) before
+//         it waits for the count kernel.
 //
 // No kernel here spins on a flag, so none can hang.
 
@@ -30,6 +35,7 @@ namespace moe {
 namespace {
 
 constexpr int kHostSlots = 64;  // shared-memory slots for per-host counters
+constexpr unsigned kFull = 0xffffffffu;
 
 // Exclusive scan of data[0, n) in shared memory by the whole block; returns
 // the total.  s_warp needs 32 ints.  All threads must call it.
@@ -43,7 +49,7 @@ __device__ int block_exclusive_scan(int32_t* data, int n, int32_t* s_warp) {
     int v = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, v, off);
+        const int u = __shfl_up_sync(kFull, v, off);
         if (lane >= off) v += u;
     }
     if (lane == 31) s_warp[warp] = v;
@@ -52,7 +58,7 @@ __device__ int block_exclusive_scan(int32_t* data, int n, int32_t* s_warp) {
         int w = lane < nwarps ? s_warp[lane] : 0;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, w, off);
+            const int u = __shfl_up_sync(kFull, w, off);
             if (lane >= off) w += u;
         }
         s_warp[lane] = w;
@@ -69,6 +75,18 @@ __device__ int block_exclusive_scan(int32_t* data, int n, int32_t* s_warp) {
     return total;
 }
 
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+    return v;
+}
+
+__device__ __forceinline__ int rank_of_expert(const LayoutArgs& a, int e, uint32_t* st) {
+    int r = a.expert_to_rank ? a.expert_to_rank[e] : e / (a.E / a.R);
+    if (r < 0 || r >= a.R) { *st |= MOE_STATUS_PLACEMENT; r = 0; }
+    return r;
+}
+
 __device__ __forceinline__ int src_rank_of(const LayoutArgs& a, const int32_t* s_soff, int t) {
     if (a.src_offsets == nullptr) return t / (a.T / a.Rs);
     int lo = 0, hi = a.Rs - 1;  // largest r with s_soff[r] <= t
@@ -81,64 +99,154 @@ __device__ __forceinline__ int src_rank_of(const LayoutArgs& a, const int32_t* s
 
 __device__ __forceinline__ int clamp_id(int e, int E) { return (e < 0 || e >= E) ? 0 : e; }
 
-// Last block of the count kernel: totals -> offsets and count outputs.
-__device__ void finalize_offsets(const LayoutArgs& a, int32_t* s_rank, int32_t* s_cnt,
-                                 int32_t* s_tmp, int32_t* s_warp) {
-    const int tid = threadIdx.x;
-    const int32_t* g_ecount = reinterpret_cast<const int32_t*>(a.ws + a.wl.ecount);
-    const int32_t* g_hcount = reinterpret_cast<const int32_t*>(a.ws + a.wl.hcount);
+// One atomic per group of lanes holding the same non-negative key.
+__device__ __forceinline__ void warp_count(int32_t* counters, int key) {
+    const unsigned same = __match_any_sync(kFull, key);
+    if (key >= 0 && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&counters[key], __popc(same));
+}
+
+// ---- statistics ----------------------------------------------------------
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(kFull, v, off);
+        v = o > v ? o : v;
+    }
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+    return v;
+}
+
+// Reductions of the statistics: maxima (of key values) and sums.
+enum { RMAX_EXPERT = 0, RMAX_EXPERT_MIN, RMAX_SRC_M1, RMAX_SRC_M2, RMAX_SLOTS, RMAX_TOKENS,
+       RMAX_REMOTE, RMAX_RELAY, RSUM_TOK, RSUM_M0, RSUM_M1, RSUM_M2, R_COUNT };
+constexpr int kMaxStatWarps = 32;
+
+// The statistics record of a layout, written into the workspace by one whole
+// block once the counters are complete.  ecount / rcount: expert and rank
+// slot counts (any memory the block can read).
+__device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const int32_t* rcount) {
+    __shared__ unsigned long long s_red[R_COUNT][kMaxStatWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    unsigned long long v[R_COUNT];
+#pragma unroll
+    for (int i = 0; i < R_COUNT; ++i) v[i] = 0ull;
+    auto ws32 = [&](size_t off) { return reinterpret_cast<const int32_t*>(a.ws + off); };
+
     for (int e = tid; e < a.E; e += blockDim.x) {
-        const int c = ld_cg(g_ecount + e);
-        s_cnt[e] = c;
-        a.out.expert_count[e] = c;
+        const unsigned long long c = (unsigned)ecount[e];
+        const unsigned long long key = (c << 32) | (unsigned)(a.E - 1 - e);  // ties -> smallest e
+        v[RMAX_EXPERT] = key > v[RMAX_EXPERT] ? key : v[RMAX_EXPERT];
+        const unsigned long long nkey = ~((c << 32) | (unsigned)e);          // minimum via complement
+        v[RMAX_EXPERT_MIN] = nkey > v[RMAX_EXPERT_MIN] ? nkey : v[RMAX_EXPERT_MIN];
     }
-    for (int r = tid; r < a.R; r += blockDim.x) s_tmp[r] = 0;
+    int64_t* rec = reinterpret_cast<int64_t*>(a.ws + a.wl.stats);
+    int64_t* src = rec + MOE_STATS_HEADER_WORDS;
+    int64_t* dst = src + (size_t)MOE_SRC_FIELDS * a.Rs;
+    for (int r = tid; r < a.Rs; r += blockDim.x) {
+        const int64_t tok = __ldcg(ws32(a.wl.src_tokens) + r);
+        const int64_t m0 = __ldcg(ws32(a.wl.src_mode0) + r);
+        const int64_t m1 = __ldcg(ws32(a.wl.src_mode1) + r);
+        const int64_t m2 = __ldcg(ws32(a.wl.src_mode2) + r);
+        src[MOE_SRC_TOKENS * a.Rs + r] = tok;
+        src[MOE_SRC_COPIES * a.Rs + r] = tok * a.k;
+        src[MOE_SRC_MODE0 * a.Rs + r] = m0;
+        src[MOE_SRC_MODE1 * a.Rs + r] = m1;
+        src[MOE_SRC_MODE2 * a.Rs + r] = m2;
+        // "tokens x k x h x 2 B" per rank and direction ("Balancing and
+        // Beyond", section 1); copies x row bytes per mode (section 3.2).
+        src[MOE_SRC_NAIVE_BYTES * a.Rs + r] = tok * a.k * (int64_t)a.h * 2;
+        src[MOE_SRC_MODE0_BYTES * a.Rs + r] = m0 * a.row_bytes;
+        src[MOE_SRC_MODE1_BYTES * a.Rs + r] = m1 * a.row_bytes;
+        src[MOE_SRC_MODE2_BYTES * a.Rs + r] = m2 * a.row_bytes;
+        v[RSUM_TOK] += tok;
+        v[RSUM_M0] += m0;
+        v[RSUM_M1] += m1;
+        v[RSUM_M2] += m2;
+        v[RMAX_SRC_M1] = max(v[RMAX_SRC_M1], (unsigned long long)m1);
+        v[RMAX_SRC_M2] = max(v[RMAX_SRC_M2], (unsigned long long)m2);
+    }
+    for (int r = tid; r < a.R; r += blockDim.x) {
+        const int64_t slots = rcount[r];
+        const int64_t tok = __ldcg(ws32(a.wl.dst_tokens) + r);
+        const int64_t rem = __ldcg(ws32(a.wl.dst_remote) + r);
+        const int64_t rel = __ldcg(ws32(a.wl.dst_relay) + r);
+        dst[MOE_DST_SLOTS * a.R + r] = slots;
+        dst[MOE_DST_TOKENS * a.R + r] = tok;
+        dst[MOE_DST_SELF * a.R + r] = __ldcg(ws32(a.wl.dst_self) + r);
+        dst[MOE_DST_LOCAL * a.R + r] = __ldcg(ws32(a.wl.dst_local) + r);
+        dst[MOE_DST_REMOTE * a.R + r] = rem;
+        dst[MOE_DST_RELAY * a.R + r] = rel;
+        v[RMAX_SLOTS] = max(v[RMAX_SLOTS], (unsigned long long)slots);
+        v[RMAX_TOKENS] = max(v[RMAX_TOKENS], (unsigned long long)tok);
+        v[RMAX_REMOTE] = max(v[RMAX_REMOTE], (unsigned long long)rem);
+        v[RMAX_RELAY] = max(v[RMAX_RELAY], (unsigned long long)rel);
+    }
+#pragma unroll
+    for (int i = 0; i < R_COUNT; ++i) {
+        const unsigned long long w = i < RSUM_TOK ? warp_max_u64(v[i]) : warp_sum_u64(v[i]);
+        if (lane == 0) s_red[i][warp] = w;
+    }
     __syncthreads();
-    for (int e = tid; e < a.E; e += blockDim.x) atomicAdd(&s_tmp[s_rank[e]], s_cnt[e]);
-    __syncthreads();
-    for (int r = tid; r < a.R; r += blockDim.x) a.out.rank_count[r] = s_tmp[r];
-    __syncthreads();
-    const int total = block_exclusive_scan(s_tmp, a.R, s_warp);
-    for (int r = tid; r < a.R; r += blockDim.x) a.out.rank_offset[r] = s_tmp[r];
     if (tid == 0) {
-        a.out.rank_offset[a.R] = total;
-        a.out.expert_offset[a.E] = total;
-    }
-    // Expert e starts after its rank's earlier experts.
-    for (int e = tid; e < a.E; e += blockDim.x) {
-        const int r = s_rank[e];
-        int start = s_tmp[r];
-        if (a.expert_to_rank == nullptr) {
-            for (int e2 = r * (a.E / a.R); e2 < e; ++e2) start += s_cnt[e2];
-        } else {
-            for (int e2 = 0; e2 < e; ++e2) start += (s_rank[e2] == r) ? s_cnt[e2] : 0;
+        unsigned long long r[R_COUNT];
+        for (int i = 0; i < R_COUNT; ++i) {
+            r[i] = 0ull;
+            for (int w = 0; w < nwarps; ++w)
+                r[i] = i < RSUM_TOK ? max(r[i], s_red[i][w]) : r[i] + s_red[i][w];
         }
-        a.out.expert_offset[e] = start;
-    }
-    if (tid == 0) {
-        int run = 0;
-        for (int hh = 0; hh < a.H; ++hh) {
-            const int c = ld_cg(g_hcount + hh);
-            a.out.host_count[hh] = c;
-            a.out.host_offset[hh] = run;
-            run += c;
-        }
-        a.out.host_offset[a.H] = run;
+        for (int i = 0; i < MOE_STATS_HEADER_WORDS; ++i) rec[i] = 0;
+        const int64_t S = (int64_t)a.T * a.k;
+        const int64_t emax = (int64_t)(r[RMAX_EXPERT] >> 32);
+        const unsigned long long minkey = ~r[RMAX_EXPERT_MIN];
+        rec[MOE_ST_STATUS] = (int64_t)__ldcg(reinterpret_cast<const unsigned*>(a.ws + a.wl.status));
+        rec[MOE_ST_TOKENS] = a.T;
+        rec[MOE_ST_SLOTS] = S;
+        rec[MOE_ST_ROW_BYTES] = a.row_bytes;
+        rec[MOE_ST_MAX_EXPERT] = emax;
+        rec[MOE_ST_ARGMAX_EXPERT] = a.E - 1 - (int64_t)(r[RMAX_EXPERT] & 0xffffffffull);
+        rec[MOE_ST_MIN_EXPERT] = (int64_t)(minkey >> 32);
+        rec[MOE_ST_MAX_RANK_SLOTS] = (int64_t)r[RMAX_SLOTS];
+        rec[MOE_ST_MAX_RANK_TOKENS] = (int64_t)r[RMAX_TOKENS];
+        rec[MOE_ST_SUM_MODE0] = (int64_t)r[RSUM_M0];
+        rec[MOE_ST_SUM_MODE1] = (int64_t)r[RSUM_M1];
+        rec[MOE_ST_SUM_MODE2] = (int64_t)r[RSUM_M2];
+        rec[MOE_ST_MAX_SRC_MODE1] = (int64_t)r[RMAX_SRC_M1];
+        rec[MOE_ST_MAX_SRC_MODE2] = (int64_t)r[RMAX_SRC_M2];
+        rec[MOE_ST_MAX_RECV_REMOTE] = (int64_t)r[RMAX_REMOTE];
+        rec[MOE_ST_MAX_RECV_RELAY] = (int64_t)r[RMAX_RELAY];
+        rec[MOE_ST_SUM_NAIVE_BYTES] = (int64_t)r[RSUM_TOK] * a.k * (int64_t)a.h * 2;
+        rec[MOE_ST_SUM_MODE0_BYTES] = (int64_t)r[RSUM_M0] * a.row_bytes;
+        rec[MOE_ST_SUM_MODE1_BYTES] = (int64_t)r[RSUM_M1] * a.row_bytes;
+        rec[MOE_ST_SUM_MODE2_BYTES] = (int64_t)r[RSUM_M2] * a.row_bytes;
+        // Imbalance ratio: busiest expert over the layer mean T*k/E
+        // ("Balancing and Beyond", section 2); the same for ranks.
+        const double ratio = S > 0 ? (double)emax / ((double)S / (double)a.E) : 0.0;
+        const double rratio = S > 0 ? (double)r[RMAX_SLOTS] / ((double)S / (double)a.R) : 0.0;
+        rec[MOE_ST_IMBALANCE_RATIO] = __double_as_longlong(ratio);
+        rec[MOE_ST_RANK_IMBALANCE] = __double_as_longlong(rratio);
+        rec[MOE_ST_NUM_HOSTS] = a.H;
     }
 }
 
+template <int KMAX>
 __global__ void __launch_bounds__(kCountThreads)
 layout_count_kernel(const LayoutArgs a) {
     extern __shared__ int32_t smem[];
     int32_t* s_rank = smem;                  // [E] rank of each expert
-    int32_t* s_hist = s_rank + a.E;          // [E] this block's expert counts
+    int32_t* s_host = s_rank + a.E;          // [E] host of each expert
+    int32_t* s_hist = s_host + a.E;          // [E] this block's expert counts
     int32_t* s_hc = s_hist + a.E;            // [64] tokens per host
     int32_t* s_soff = s_hc + kHostSlots;     // [Rs+1] source offsets
     int32_t* s_src = s_soff + (a.Rs + 1);    // [4][Rs] tokens, mode0, mode1, mode2
     int32_t* s_dst = s_src + 4 * a.Rs;       // [5][R] tokens, self, local, remote, relay
     __shared__ uint32_t s_status;
-    __shared__ int s_last;
-    __shared__ int32_t s_warp[32];
 
     // The rank kernel's prologue only reads ids: let it start now.
     pdl_launch_dependents();
@@ -148,9 +256,9 @@ layout_count_kernel(const LayoutArgs a) {
     if (tid == 0) s_status = 0;
     uint32_t st = 0;
     for (int e = tid; e < a.E; e += blockDim.x) {
-        int r = a.expert_to_rank ? a.expert_to_rank[e] : e / (a.E / a.R);
-        if (r < 0 || r >= a.R) { st |= MOE_STATUS_PLACEMENT; r = 0; }
+        const int r = rank_of_expert(a, e, &st);
         s_rank[e] = r;
+        s_host[e] = r / a.P;
         s_hist[e] = 0;
     }
     for (int i = tid; i < kHostSlots; i += blockDim.x) s_hc[i] = 0;
@@ -169,98 +277,166 @@ layout_count_kernel(const LayoutArgs a) {
     const int t = b * kLayoutTokensPerBlock + tid;
     const bool valid = t < a.T;
     const int rs = valid ? min(max(src_rank_of(a, s_soff, t), 0), a.Rs - 1) : 0;
-    const int own_host = rs / a.P;
-    const int32_t* row = a.ids + (size_t)(valid ? t : 0) * a.k;
-    unsigned long long hmask = 0ull;
-    int mode0 = 0, mode1 = 0;
-    for (int j = 0; j < a.k; ++j) {
-        int e = -1;
-        if (valid) {
-            const int raw = row[j];
-            if (raw < 0 || raw >= a.E) st |= MOE_STATUS_ID_RANGE;
+    const int own = rs / a.P;
+    __shared__ int s_rs0;
+    if (tid == 0) s_rs0 = rs;  // thread 0 always holds a token
+    __syncthreads();
+    // Usual case: one source rank for the whole block (every token of a rank
+    // is contiguous and a rank holds at least 128 tokens in most layouts).
+    const bool block_one_src = __syncthreads_and(!valid || rs == s_rs0);
+    const bool small_r = a.R <= 64;  // a token's ranks fit a 64-bit mask
+
+    // The token's ids, validated, then clamped into [0, E).
+    int ev[KMAX], rv[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        ev[j] = -1;
+        rv[j] = -1;
+        if (j < a.k && valid) ev[j] = a.ids[(size_t)t * a.k + j];
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (j < a.k && valid) {
+            if (ev[j] < 0 || ev[j] >= a.E) st |= MOE_STATUS_ID_RANGE;
+#pragma unroll
             for (int i = 0; i < j; ++i)
-                if (row[i] == raw) st |= MOE_STATUS_ID_REPEAT;
-            e = clamp_id(raw, a.E);
+                if (ev[i] == ev[j]) st |= MOE_STATUS_ID_REPEAT;
         }
-        // One shared-memory atomic per distinct expert in the warp.
-        const unsigned same = __match_any_sync(0xffffffffu, e);
-        if (valid && lane == __ffs(same) - 1) atomicAdd(&s_hist[e], __popc(same));
-        if (valid) {
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+        if (j < a.k && valid) ev[j] = clamp_id(ev[j], a.E);
+
+    unsigned long long hmask = 0ull, rmask = 0ull;  // hosts / ranks the token reaches
+    int mode0 = 0, mode1 = 0;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (j >= a.k) break;  // a.k is the same for the whole warp
+        const int e = ev[j];  // -1 for tokens past T
+        warp_count(s_hist, e);
+        if (e >= 0) {
             const int r = s_rank[e];
-            const int hh = r / a.P;
+            const int hh = s_host[e];
+            rv[j] = r;
             hmask |= 1ull << hh;
-            bool first = true;  // first slot of this token on rank r
-            for (int i = 0; i < j; ++i) first = first && (s_rank[clamp_id(row[i], a.E)] != r);
-            if (first) atomicAdd(&s_dst[0 * a.R + r], 1);
-            if (r == rs) atomicAdd(&s_dst[1 * a.R + r], 1);
-            else if (hh == own_host) atomicAdd(&s_dst[2 * a.R + r], 1);
-            else atomicAdd(&s_dst[3 * a.R + r], 1);
             mode0 += (r != rs);
-            mode1 += (hh != own_host);
+            mode1 += (hh != own);
+            if (small_r) {
+                rmask |= 1ull << r;
+            } else {
+                bool first = true;  // first slot of this token on rank r
+#pragma unroll
+                for (int i = 0; i < j; ++i) first = first && (rv[i] != r);
+                if (first) atomicAdd(&s_dst[r], 1);
+            }
+            if (!block_one_src) {
+                const int cat = (r == rs) ? 1 : (hh == own ? 2 : 3);  // self, local, remote
+                atomicAdd(&s_dst[cat * a.R + r], 1);
+            }
+        }
+    }
+    if (small_r) {
+        // Tokens per rank: one ballot per rank that some lane reaches.
+        unsigned long long any = rmask;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) any |= __shfl_xor_sync(kFull, any, off);
+        while (any) {
+            const int r = __ffsll((long long)any) - 1;
+            any &= any - 1;
+            const unsigned m = __ballot_sync(kFull, (rmask >> r) & 1ull);
+            if (lane == 0) atomicAdd(&s_dst[r], __popc(m));
         }
     }
     if (valid) {
         uint8_t* mrow = a.out.host_mask + (size_t)t * a.H;
         for (int hh = 0; hh < a.H; ++hh) mrow[hh] = (uint8_t)((hmask >> hh) & 1ull);
-        unsigned long long bits = hmask;
-        while (bits) {
-            const int hh = __ffsll((long long)bits) - 1;
-            bits &= bits - 1;
-            atomicAdd(&s_hc[hh], 1);
-            if (hh != own_host) atomicAdd(&s_dst[4 * a.R + hh * a.P + rs % a.P], 1);
+    }
+    for (int hh = 0; hh < a.H; ++hh) {
+        const unsigned m = __ballot_sync(kFull, valid && ((hmask >> hh) & 1ull));
+        if (lane == 0 && m) atomicAdd(&s_hc[hh], __popc(m));
+    }
+    const int mode2 = valid ? __popcll(hmask & ~(1ull << own)) : 0;
+    const int rs0 = __shfl_sync(kFull, rs, 0);
+    if (__all_sync(kFull, !valid || rs == rs0)) {
+        // The warp's tokens share one source rank.
+        const int n_tok = warp_sum(valid ? 1 : 0);
+        const int n0 = warp_sum(mode0), n1 = warp_sum(mode1), n2 = warp_sum(mode2);
+        if (lane == 0 && n_tok > 0) {
+            atomicAdd(&s_src[0 * a.Rs + rs0], n_tok);
+            atomicAdd(&s_src[1 * a.Rs + rs0], n0);
+            atomicAdd(&s_src[2 * a.Rs + rs0], n1);
+            atomicAdd(&s_src[3 * a.Rs + rs0], n2);
         }
-        const int mode2 = __popcll(hmask & ~(1ull << own_host));
+        const int own0 = rs0 / a.P;
+        for (int hh = 0; hh < a.H; ++hh) {
+            if (hh == own0) continue;
+            const unsigned m = __ballot_sync(kFull, valid && ((hmask >> hh) & 1ull));
+            if (lane == 0 && m) atomicAdd(&s_dst[4 * a.R + hh * a.P + rs0 % a.P], __popc(m));
+        }
+    } else if (valid) {
         atomicAdd(&s_src[0 * a.Rs + rs], 1);
         atomicAdd(&s_src[1 * a.Rs + rs], mode0);
         atomicAdd(&s_src[2 * a.Rs + rs], mode1);
         atomicAdd(&s_src[3 * a.Rs + rs], mode2);
+        unsigned long long bits = hmask & ~(1ull << own);
+        while (bits) {
+            const int hh = __ffsll((long long)bits) - 1;
+            bits &= bits - 1;
+            atomicAdd(&s_dst[4 * a.R + hh * a.P + rs % a.P], 1);
+        }
     }
     if (st) atomicOr(&s_status, st);
     __syncthreads();
+    if (block_one_src) {
+        // Slots by (category, destination rank) follow from the expert counts.
+        const int own_b = s_rs0 / a.P;
+        for (int e = tid; e < a.E; e += blockDim.x) {
+            const int c = s_hist[e];
+            if (c == 0) continue;
+            const int r = s_rank[e];
+            const int cat = (r == s_rs0) ? 1 : (s_host[e] == own_b ? 2 : 3);
+            atomicAdd(&s_dst[cat * a.R + r], c);
+        }
+        __syncthreads();
+    }
 
-    // Publish this block's histogram and add the counters to the totals.
+    // Publish this block's histogram; add the counters to the totals.
     int32_t* g_agg = reinterpret_cast<int32_t*>(a.ws + a.wl.agg) + (size_t)b * a.E;
-    int32_t* g_ecount = reinterpret_cast<int32_t*>(a.ws + a.wl.ecount);
+    int32_t* g_group = reinterpret_cast<int32_t*>(a.ws + a.wl.group) + (size_t)(b / kLayoutGroup) * a.E;
     for (int e = tid; e < a.E; e += blockDim.x) {
         const int v = s_hist[e];
         g_agg[e] = v;
-        if (v) atomicAdd(&g_ecount[e], v);
+        if (v) atomicAdd(&g_group[e], v);
     }
     int32_t* g_hcount = reinterpret_cast<int32_t*>(a.ws + a.wl.hcount);
     for (int hh = tid; hh < a.H; hh += blockDim.x)
         if (s_hc[hh]) atomicAdd(&g_hcount[hh], s_hc[hh]);
-    const size_t src_base[4] = {a.wl.src_tokens, a.wl.src_mode0, a.wl.src_mode1, a.wl.src_mode2};
+    int32_t* g_src = reinterpret_cast<int32_t*>(a.ws + a.wl.src_tokens);  // 4 blocks of R_src
     for (int i = tid; i < 4 * a.Rs; i += blockDim.x)
-        if (s_src[i]) atomicAdd(reinterpret_cast<int32_t*>(a.ws + src_base[i / a.Rs]) + i % a.Rs, s_src[i]);
-    const size_t dst_base[5] = {a.wl.dst_tokens, a.wl.dst_self, a.wl.dst_local, a.wl.dst_remote,
-                                a.wl.dst_relay};
+        if (s_src[i]) atomicAdd(&g_src[i], s_src[i]);
+    int32_t* g_dst = reinterpret_cast<int32_t*>(a.ws + a.wl.dst_tokens);  // 5 blocks of R
     for (int i = tid; i < 5 * a.R; i += blockDim.x)
-        if (s_dst[i]) atomicAdd(reinterpret_cast<int32_t*>(a.ws + dst_base[i / a.R]) + i % a.R, s_dst[i]);
-    if (tid == 0) {
-        reinterpret_cast<uint32_t*>(a.ws + a.wl.ready)[b] = 0u;
-        if (s_status) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), s_status);
-    }
-
-    // The last block to arrive sees every block's totals.
-    __threadfence();
-    __syncthreads();
-    if (tid == 0)
-        s_last = atomicAdd(reinterpret_cast<uint32_t*>(a.ws + a.wl.done), 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    finalize_offsets(a, s_rank, s_hist, s_dst, s_warp);
+        if (s_dst[i]) atomicAdd(&g_dst[i], s_dst[i]);
+    if (tid == 0 && s_status) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), s_status);
 }
 
 __global__ void __launch_bounds__(kRankThreads)
 layout_rank_kernel(const LayoutArgs a) {
     extern __shared__ int32_t smem[];
-    int32_t* s_whist = smem;                       // [8][E] per-warp counts -> warp prefixes
-    int32_t* s_agg = s_whist + kRankWarps * a.E;   // [E] block totals
-    int32_t* s_base = s_agg + a.E;                 // [E] first receive row of the block's slots
-    int32_t* s_lrank = s_base + a.E;               // [T_B * k] rank inside the warp's run
-    __shared__ int s_pstar;
+    int32_t* s_whist = smem;                            // [8][E] per-warp counts -> warp prefixes
+    int32_t* s_agg = s_whist + kRankWarps * a.E;        // [E] this block's counts
+    int32_t* s_tot = s_agg + a.E;                       // [E] totals over all blocks
+    int32_t* s_rank = s_tot + a.E;                      // [E] rank of each expert
+    int32_t* s_order = s_rank + a.E;                    // [E] experts in (rank, e) order
+    int32_t* s_scan = s_order + a.E;                    // [E] receive offsets, in that order
+    int32_t* s_base = s_scan + a.E;                     // [E] first receive row of the block's slots
+    int32_t* s_part = s_base + a.E;                     // [2][256] partial totals and prefixes
+    int32_t* s_rstart = s_part + 2 * kRankThreads;      // [R+1] first position of a rank in s_order
+    int32_t* s_rfill = s_rstart + (a.R + 1);            // [R]
+    int32_t* s_lrank = s_rfill + a.R;                   // [T_B * k] rank inside the warp's run
+    __shared__ int32_t s_warp[32];
 
+    pdl_launch_dependents();  // the next kernel waits for this one's results
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
     const int S = a.T * a.k;
@@ -280,17 +456,19 @@ layout_rank_kernel(const LayoutArgs a) {
         const int s = base + lane;
         const bool valid = s < w_hi;
         const int e = valid ? clamp_id(a.ids[s], a.E) : -1;
-        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const unsigned same = __match_any_sync(kFull, e);
         const int leader = __ffs(same) - 1;
         int before = 0;
         if (valid && lane == leader) {
             before = my_hist[e];
             my_hist[e] = before + __popc(same);
         }
-        before = __shfl_sync(0xffffffffu, before, leader);
+        before = __shfl_sync(kFull, before, leader);
         if (valid) s_lrank[s - s0] = before + __popc(same & lanemask_lt());
         __syncwarp();
     }
+    uint32_t st_unused = 0;
+    for (int e = tid; e < a.E; e += blockDim.x) s_rank[e] = rank_of_expert(a, e, &st_unused);
     __syncthreads();
     for (int e = tid; e < a.E; e += blockDim.x) {
         int run = 0;
@@ -303,32 +481,122 @@ layout_rank_kernel(const LayoutArgs a) {
         s_agg[e] = run;
     }
 
-    // From here on the count kernel's tables are needed.
+    // From here on the count kernel's tables are needed.  One pass of loads
+    // gives each expert's total (all group rows) and this block's prefix (the
+    // group rows before its group, then the blocks of its own group before it).
     pdl_wait();
+    const int32_t* g_group = reinterpret_cast<const int32_t*>(a.ws + a.wl.group);
     const int32_t* g_agg = reinterpret_cast<const int32_t*>(a.ws + a.wl.agg);
-    int32_t* g_incl = reinterpret_cast<int32_t*>(a.ws + a.wl.incl);
-    uint32_t* g_ready = reinterpret_cast<uint32_t*>(a.ws + a.wl.ready);
-    if (warp == 0) {
-        int pstar = -1;
-        for (int hi = b - 1; hi >= 0; hi -= 32) {
-            const int p = hi - lane;
-            const uint32_t f = p >= 0 ? ld_acquire_gpu(g_ready + p) : 0u;
-            const unsigned m = __ballot_sync(0xffffffffu, f != 0u);
-            if (m) { pstar = hi - (__ffs(m) - 1); break; }
+    {
+        const int sb = b / kLayoutGroup;
+        const int tail0 = sb * kLayoutGroup;
+        const int G = a.wl.groups;
+        const int parts = a.E >= kRankThreads ? 1 : kRankThreads / a.E;
+        for (int e0 = 0; e0 < a.E; e0 += kRankThreads) {
+            const int slot = e0 + (parts > 1 ? tid % a.E : tid);
+            const int part = parts > 1 ? tid / a.E : 0;
+            const bool active = slot < a.E && part < parts;
+            int tot = 0, pre = 0;
+            if (active) {
+#pragma unroll 4
+                for (int g = part; g < G; g += parts) {
+                    const int v = __ldcg(g_group + (size_t)g * a.E + slot);
+                    tot += v;
+                    pre += g < sb ? v : 0;
+                }
+#pragma unroll 4
+                for (int p = tail0 + part; p < b; p += parts) pre += __ldcg(g_agg + (size_t)p * a.E + slot);
+            }
+            s_part[tid] = active ? tot : 0;
+            s_part[kRankThreads + tid] = active ? pre : 0;
+            __syncthreads();
+            if (parts > 1) {
+                if (tid < a.E) {
+                    int sum_t = 0, sum_p = 0;
+                    for (int q = 0; q < parts; ++q) {
+                        sum_t += s_part[q * a.E + tid];
+                        sum_p += s_part[kRankThreads + q * a.E + tid];
+                    }
+                    s_tot[tid] = sum_t;
+                    s_base[tid] = sum_p;
+                }
+            } else if (slot < a.E) {
+                s_tot[slot] = s_part[tid];
+                s_base[slot] = s_part[kRankThreads + tid];
+            }
+            __syncthreads();
         }
-        if (lane == 0) s_pstar = pstar;
+    }
+
+    // Experts in receive order: stable by rank (identity for the default
+    // contiguous placement).
+    if (a.expert_to_rank == nullptr) {
+        const int per = a.E / a.R;
+        for (int i = tid; i < a.E; i += blockDim.x) s_order[i] = i;
+        for (int r = tid; r <= a.R; r += blockDim.x) s_rstart[r] = r * per;
+    } else {
+        for (int r = tid; r < a.R; r += blockDim.x) { s_rstart[r] = 0; s_rfill[r] = 0; }
+        __syncthreads();
+        for (int e = tid; e < a.E; e += blockDim.x) atomicAdd(&s_rstart[s_rank[e]], 1);
+        __syncthreads();
+        block_exclusive_scan(s_rstart, a.R, s_warp);
+        if (tid == 0) s_rstart[a.R] = a.E;
+        __syncthreads();
+        if (warp == 0) {
+            for (int c = 0; c < a.E; c += 32) {
+                const int e = c + lane;
+                const int r = e < a.E ? s_rank[e] : -1;
+                const unsigned same = __match_any_sync(kFull, r);
+                const int leader = __ffs(same) - 1;
+                int before = 0;
+                if (r >= 0 && lane == leader) {
+                    before = s_rfill[r];
+                    s_rfill[r] = before + __popc(same);
+                }
+                before = __shfl_sync(kFull, before, leader);
+                if (r >= 0) s_order[s_rstart[r] + before + __popc(same & lanemask_lt())] = e;
+                __syncwarp();
+            }
+        }
     }
     __syncthreads();
-    const int pstar = s_pstar;
-    for (int e = tid; e < a.E; e += blockDim.x) {
-        int excl = pstar >= 0 ? ld_cg(g_incl + (size_t)pstar * a.E + e) : 0;
-        for (int p = pstar + 1; p < b; ++p) excl += ld_cg(g_agg + (size_t)p * a.E + e);
-        st_cg(g_incl + (size_t)b * a.E + e, excl + s_agg[e]);
-        s_base[e] = ld_cg(a.out.expert_offset + e) + excl;
-    }
-    __threadfence();
+    for (int i = tid; i < a.E; i += blockDim.x) s_scan[i] = s_tot[s_order[i]];
     __syncthreads();
-    if (tid == 0) st_release_gpu(g_ready + b, 1u);
+    const int total = block_exclusive_scan(s_scan, a.E, s_warp);
+
+    for (int i = tid; i < a.E; i += blockDim.x) s_base[s_order[i]] += s_scan[i];
+    __syncthreads();
+
+    if (b == 0) {
+        for (int i = tid; i < a.E; i += blockDim.x) {
+            const int e = s_order[i];
+            a.out.expert_count[e] = s_tot[e];
+            a.out.expert_offset[e] = s_scan[i];
+        }
+        int32_t* s_rcount = s_rfill;  // free again: rank counts for the statistics
+        for (int r = tid; r < a.R; r += blockDim.x) {
+            const int lo = s_rstart[r] < a.E ? s_scan[s_rstart[r]] : total;
+            const int hi = s_rstart[r + 1] < a.E ? s_scan[s_rstart[r + 1]] : total;
+            a.out.rank_offset[r] = lo;
+            a.out.rank_count[r] = hi - lo;
+            s_rcount[r] = hi - lo;
+        }
+        if (tid == 0) {
+            a.out.expert_offset[a.E] = total;
+            a.out.rank_offset[a.R] = total;
+            const int32_t* g_hcount = reinterpret_cast<const int32_t*>(a.ws + a.wl.hcount);
+            int run = 0;
+            for (int hh = 0; hh < a.H; ++hh) {
+                const int c = __ldcg(g_hcount + hh);
+                a.out.host_count[hh] = c;
+                a.out.host_offset[hh] = run;
+                run += c;
+            }
+            a.out.host_offset[a.H] = run;
+        }
+        __syncthreads();
+        write_stats(a, s_tot, s_rfill);
+    }
 
     for (int i = tid; i < nslots; i += blockDim.x) {
         const int s = s0 + i;
@@ -340,145 +608,69 @@ layout_rank_kernel(const LayoutArgs a) {
     }
 }
 
-__global__ void __launch_bounds__(256) stats_kernel(const StatsArgs a) {
-    __shared__ unsigned long long s_emax, s_emin, s_rslots, s_rtok, s_rrem, s_rrel;
-    __shared__ unsigned long long s_sum[7], s_smax[2];
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        s_emax = 0ull; s_emin = ~0ull; s_rslots = s_rtok = s_rrem = s_rrel = 0ull;
-        for (int i = 0; i < 7; ++i) s_sum[i] = 0ull;
-        s_smax[0] = s_smax[1] = 0ull;
+// Layout with no tokens: counts and offsets are all zero.
+__global__ void layout_empty_kernel(const LayoutArgs a) {
+    for (int e = threadIdx.x; e <= a.E; e += blockDim.x) {
+        if (e < a.E) a.out.expert_count[e] = 0;
+        a.out.expert_offset[e] = 0;
+    }
+    for (int r = threadIdx.x; r <= a.R; r += blockDim.x) {
+        if (r < a.R) a.out.rank_count[r] = 0;
+        a.out.rank_offset[r] = 0;
+    }
+    for (int hh = threadIdx.x; hh <= a.H; hh += blockDim.x) {
+        if (hh < a.H) a.out.host_count[hh] = 0;
+        a.out.host_offset[hh] = 0;
     }
     __syncthreads();
-    auto ws32 = [&](size_t off) { return reinterpret_cast<const int32_t*>(a.ws + off); };
-    for (int e = tid; e < a.E; e += blockDim.x) {
-        const unsigned long long c = (unsigned)a.expert_count[e];
-        atomicMax(&s_emax, (c << 32) | (unsigned)(a.E - 1 - e));  // ties -> smallest e
-        atomicMin(&s_emin, (c << 32) | (unsigned)e);
-    }
-    int64_t* src = a.stats + MOE_STATS_HEADER_WORDS;
-    int64_t* dst = src + (size_t)MOE_SRC_FIELDS * a.Rs;
-    for (int r = tid; r < a.Rs; r += blockDim.x) {
-        const int64_t tok = ws32(a.wl.src_tokens)[r];
-        const int64_t m0 = ws32(a.wl.src_mode0)[r];
-        const int64_t m1 = ws32(a.wl.src_mode1)[r];
-        const int64_t m2 = ws32(a.wl.src_mode2)[r];
-        const int64_t naive = tok * a.k * (int64_t)a.h * 2;
-        src[MOE_SRC_TOKENS * a.Rs + r] = tok;
-        src[MOE_SRC_COPIES * a.Rs + r] = tok * a.k;
-        src[MOE_SRC_MODE0 * a.Rs + r] = m0;
-        src[MOE_SRC_MODE1 * a.Rs + r] = m1;
-        src[MOE_SRC_MODE2 * a.Rs + r] = m2;
-        src[MOE_SRC_NAIVE_BYTES * a.Rs + r] = naive;
-        src[MOE_SRC_MODE0_BYTES * a.Rs + r] = m0 * a.row_bytes;
-        src[MOE_SRC_MODE1_BYTES * a.Rs + r] = m1 * a.row_bytes;
-        src[MOE_SRC_MODE2_BYTES * a.Rs + r] = m2 * a.row_bytes;
-        atomicAdd(&s_sum[0], (unsigned long long)m0);
-        atomicAdd(&s_sum[1], (unsigned long long)m1);
-        atomicAdd(&s_sum[2], (unsigned long long)m2);
-        atomicAdd(&s_sum[3], (unsigned long long)naive);
-        atomicAdd(&s_sum[4], (unsigned long long)(m0 * a.row_bytes));
-        atomicAdd(&s_sum[5], (unsigned long long)(m1 * a.row_bytes));
-        atomicAdd(&s_sum[6], (unsigned long long)(m2 * a.row_bytes));
-        atomicMax(&s_smax[0], (unsigned long long)m1);
-        atomicMax(&s_smax[1], (unsigned long long)m2);
-    }
-    for (int r = tid; r < a.R; r += blockDim.x) {
-        const int64_t slots = a.rank_count[r];
-        const int64_t tok = ws32(a.wl.dst_tokens)[r];
-        const int64_t rem = ws32(a.wl.dst_remote)[r];
-        const int64_t rel = ws32(a.wl.dst_relay)[r];
-        dst[MOE_DST_SLOTS * a.R + r] = slots;
-        dst[MOE_DST_TOKENS * a.R + r] = tok;
-        dst[MOE_DST_SELF * a.R + r] = ws32(a.wl.dst_self)[r];
-        dst[MOE_DST_LOCAL * a.R + r] = ws32(a.wl.dst_local)[r];
-        dst[MOE_DST_REMOTE * a.R + r] = rem;
-        dst[MOE_DST_RELAY * a.R + r] = rel;
-        atomicMax(&s_rslots, (unsigned long long)slots);
-        atomicMax(&s_rtok, (unsigned long long)tok);
-        atomicMax(&s_rrem, (unsigned long long)rem);
-        atomicMax(&s_rrel, (unsigned long long)rel);
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int64_t* g = a.stats;
-        for (int i = 0; i < MOE_STATS_HEADER_WORDS; ++i) g[i] = 0;
-        const int64_t S = (int64_t)a.T * a.k;
-        const int64_t emax = a.E > 0 ? (int64_t)(s_emax >> 32) : 0;
-        g[MOE_ST_STATUS] = *ws32(a.wl.status);
-        g[MOE_ST_TOKENS] = a.T;
-        g[MOE_ST_SLOTS] = S;
-        g[MOE_ST_ROW_BYTES] = a.row_bytes;
-        g[MOE_ST_MAX_EXPERT] = emax;
-        g[MOE_ST_ARGMAX_EXPERT] = a.E - 1 - (int64_t)(s_emax & 0xffffffffull);
-        g[MOE_ST_MIN_EXPERT] = (int64_t)(s_emin >> 32);
-        g[MOE_ST_MAX_RANK_SLOTS] = (int64_t)s_rslots;
-        g[MOE_ST_MAX_RANK_TOKENS] = (int64_t)s_rtok;
-        g[MOE_ST_SUM_MODE0] = (int64_t)s_sum[0];
-        g[MOE_ST_SUM_MODE1] = (int64_t)s_sum[1];
-        g[MOE_ST_SUM_MODE2] = (int64_t)s_sum[2];
-        g[MOE_ST_MAX_SRC_MODE1] = (int64_t)s_smax[0];
-        g[MOE_ST_MAX_SRC_MODE2] = (int64_t)s_smax[1];
-        g[MOE_ST_MAX_RECV_REMOTE] = (int64_t)s_rrem;
-        g[MOE_ST_MAX_RECV_RELAY] = (int64_t)s_rrel;
-        g[MOE_ST_SUM_NAIVE_BYTES] = (int64_t)s_sum[3];
-        g[MOE_ST_SUM_MODE0_BYTES] = (int64_t)s_sum[4];
-        g[MOE_ST_SUM_MODE1_BYTES] = (int64_t)s_sum[5];
-        g[MOE_ST_SUM_MODE2_BYTES] = (int64_t)s_sum[6];
-        // Imbalance ratio: busiest expert over the layer mean T*k/E
-        // ("Balancing and Beyond", section 2); the same for ranks.
-        const double ratio = S > 0 ? (double)emax / ((double)S / (double)a.E) : 0.0;
-        const double rratio = S > 0 ? (double)s_rslots / ((double)S / (double)a.R) : 0.0;
-        g[MOE_ST_IMBALANCE_RATIO] = __double_as_longlong(ratio);
-        g[MOE_ST_RANK_IMBALANCE] = __double_as_longlong(rratio);
-        g[MOE_ST_NUM_HOSTS] = a.H;
-    }
+    write_stats(a, a.out.expert_count, a.out.rank_count);
+}
+
+// Copies the statistics record out of the workspace (one small block; it
+// starts under programmatic dependent launch and waits for the layout).
+__global__ void __launch_bounds__(256) stats_copy_kernel(const int64_t* rec, int64_t* out, int words) {
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int i = threadIdx.x; i < words; i += blockDim.x) out[i] = __ldcg(rec + i);
 }
 
 size_t count_smem_bytes(const LayoutArgs& a) {
-    return sizeof(int32_t) * (2 * (size_t)a.E + kHostSlots + (a.Rs + 1) + 4 * (size_t)a.Rs + 5 * (size_t)a.R);
+    return sizeof(int32_t) * (3 * (size_t)a.E + kHostSlots + (a.Rs + 1) + 4 * (size_t)a.Rs + 5 * (size_t)a.R);
 }
 
 size_t rank_smem_bytes(const LayoutArgs& a) {
-    return sizeof(int32_t) * ((size_t)(kRankWarps + 2) * a.E + (size_t)kLayoutTokensPerBlock * a.k);
+    return sizeof(int32_t) * ((size_t)(kRankWarps + 7) * a.E + 2 * kRankThreads + (2 * (size_t)a.R + 1) +
+                              (size_t)kLayoutTokensPerBlock * a.k);
+}
+
+template <typename K>
+cudaError_t allow_smem(K kernel, size_t bytes) {
+    return ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), bytes);
 }
 
 }  // namespace
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
+    cudaError_t err;
+    if (a.T == 0) {
+        layout_empty_kernel<<<1, 128, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
     const size_t smem_count = count_smem_bytes(a);
     const size_t smem_rank = rank_smem_bytes(a);
-    cudaError_t err;
-    if (smem_count > 48 * 1024) {
-        err = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_count);
-        if (err != cudaSuccess) return err;
-    }
-    if (smem_rank > 48 * 1024) {
-        err = cudaFuncSetAttribute(layout_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_rank);
-        if (err != cudaSuccess) return err;
-    }
-    layout_count_kernel<<<a.wl.blocks, kCountThreads, smem_count, stream>>>(a);
-    err = cudaGetLastError();
-    if (err != cudaSuccess || a.T == 0) return err;
+    auto count = a.k <= 8 ? layout_count_kernel<8> : layout_count_kernel<32>;
+    if ((err = allow_smem(count, smem_count)) != cudaSuccess) return err;
+    if ((err = allow_smem(layout_rank_kernel, smem_rank)) != cudaSuccess) return err;
+    count<<<a.wl.blocks, kCountThreads, smem_count, stream>>>(a);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.wl.blocks);
-    cfg.blockDim = dim3(kRankThreads);
-    cfg.dynamicSmemBytes = smem_rank;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, layout_rank_kernel, a);
+    return launch_pdl(layout_rank_kernel, dim3(a.wl.blocks), dim3(kRankThreads), smem_rank, stream, a);
 }
 
-cudaError_t launch_stats(const StatsArgs& a, cudaStream_t stream) {
-    stats_kernel<<<1, 256, 0, stream>>>(a);
-    return cudaGetLastError();
+
+cudaError_t launch_stats_copy(const uint8_t* ws, const WsLayout& wl, int64_t* out, cudaStream_t stream) {
+    return launch_pdl(stats_copy_kernel, dim3(1), dim3(256), 0, stream,
+                      reinterpret_cast<const int64_t*>(ws + wl.stats), out, (int)wl.stats_words);
 }
 
 }  // namespace moe

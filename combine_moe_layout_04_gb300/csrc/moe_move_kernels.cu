@@ -1,18 +1,25 @@
 // moe_move_kernels.cu -- dispatch-permute and combine-unpermute on sm_103a.
 //
-// Both kernels are HBM-bound row moves ("Poor HybridEP performance on
-// dual-node 16x B300 GPUs": dispatch_with_permute / combine_with_unpermute),
-// so they are written for bytes in flight, not for arithmetic:
-//  * the work unit is one (token, column chunk): a warp moves one chunk of
-//    32 x U 16-byte vectors, so a persistent grid of SMs x resident blocks
-//    walks T x chunks units with a tail of at most one chunk per warp;
-//  * every lane issues all of its loads of a unit before using any of them
-//    (dispatch: U loads of x, then k x U stores; combine: k x U loads of y,
-//    then the fma chain), which keeps 16 x 16 B per lane in flight;
-//  * x and y are read with ld.global.nc.L1::no_allocate (read once);
-//  * the receive row of each slot comes from pos; a row index outside
-//    [0, T*k) is skipped (dispatch) or contributes nothing (combine), so a bad
-//    layout cannot write out of bounds.
+// Both are HBM-bound row moves ("Poor HybridEP performance on dual-node 16x
+// B300 GPUs": dispatch_with_permute / combine_with_unpermute), so they are
+// written for bytes in flight, not for arithmetic.  Two families:
+//
+//  * bulk kernels (the default where they apply): the Blackwell copy engine
+//    (cp.async.bulk, "TMA") moves the rows.  Each warp runs its own pipeline
+//    of shared-memory stages guarded by mbarriers.  Combine gathers the k rows
+//    of one (token, column chunk) unit into a stage with k bulk copies and
+//    reduces it from shared memory; dispatch loads one x chunk and writes it
+//    to its k receive rows with k bulk stores.  Bytes in flight are bounded by
+//    shared memory (about 190 KB per SM), not by registers.  Every barrier
+//    wait has a wall-time limit; a kernel that gives up records a fault bit,
+//    drains its own copies and returns.
+//  * LSU kernels (fallback: k > 8, or buffers a bulk copy cannot address):
+//    one warp per (token, column chunk) unit with 16-byte vector loads and
+//    stores, every load of a unit issued before any is used.
+//
+// Both walk a persistent grid over T x chunks units with a tail of at most one
+// unit per warp.  A receive row index outside [0, T*k) is skipped (dispatch)
+// or contributes nothing (combine), so a bad layout cannot write out of bounds.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -146,13 +153,257 @@ combine_kernel(const MoveArgs m, const uint4* __restrict__ y, const float* __res
     }
 }
 
+// ---- bulk (TMA) kernels --------------------------------------------------
+
+// Device fault bits of the row movers (bounded waits that gave up).
+__device__ unsigned int g_move_faults;
+constexpr unsigned kFaultWaitTimeout = 0x1u;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
+
+// Per-warp pipeline bookkeeping: a stage is "pending" from the copy issue
+// until its barrier phase is waited for; ph counts completed waits, so the
+// phase to wait for has parity ph & 1.
+template <int STAGES>
+__device__ __forceinline__ void drain_stages(uint32_t bar0, const bool (&pending)[STAGES],
+                                             const uint32_t (&ph)[STAGES]) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s)
+        if (pending[s]) mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs);
+}
+
+// Combine: each warp owns STAGES stages of 8 rows x CHUNK bytes; a stage holds
+// the k row pieces of one (token, column chunk) unit.
+template <int WARPS, int STAGES, int CHUNK>
+__global__ void __launch_bounds__(WARPS * 32, 1)
+combine_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ y, const float* __restrict__ w,
+                    uint8_t* __restrict__ out, int row_bytes) {
+    constexpr int KMAX = 8;
+    constexpr int STAGE_BYTES = KMAX * CHUNK;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t stage0 = smem_u32(smem + (size_t)warp * STAGES * STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(&s_bar[warp][0]);
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int S = m.T * m.k;
+    const int nch = m.nchunks;
+    const long long units = (long long)m.T * nch;
+    const long long nw = (long long)gridDim.x * WARPS;
+    const long long gw = (long long)blockIdx.x * WARPS + warp;
+
+    long long su[STAGES];   // unit held by each stage
+    unsigned vm[STAGES];    // rows of that unit that were fetched
+    float wr[STAGES];       // lane j < k: gate weight of row j of that unit
+    bool pending[STAGES];
+    uint32_t ph[STAGES];
+
+    auto fetch_meta = [&](long long u, int& p, float& wv) {
+        p = -1;
+        wv = 0.0f;
+        if (u < units && lane < m.k) {
+            const int t = (int)(u / nch);
+            p = m.pos[(size_t)t * m.k + lane];
+            wv = w[(size_t)t * m.k + lane];
+            if (p < 0 || p >= S) p = -1;
+        }
+    };
+    // Issues the k bulk copies of unit u into stage s (all lanes call it).
+    auto issue = [&](int s, long long u, int p) -> unsigned {
+        const int t = (int)(u / nch);
+        const int c = (int)(u - (long long)t * nch);
+        const int cb = min(CHUNK, row_bytes - c * CHUNK);
+        const unsigned mask = __ballot_sync(0xffffffffu, p >= 0);
+        if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(__popc(mask) * cb));
+        __syncwarp();
+        if (p >= 0)
+            bulk_g2s(stage0 + s * STAGE_BYTES + lane * CHUNK,
+                     y + (size_t)p * row_bytes + (size_t)c * CHUNK, (uint32_t)cb, bar0 + 8 * s);
+        return mask;
+    };
+
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+        su[s] = gw + s * nw;
+        ph[s] = 0;
+        pending[s] = su[s] < units;
+        int p;
+        float wv;
+        fetch_meta(su[s], p, wv);
+        wr[s] = wv;
+        vm[s] = pending[s] ? issue(s, su[s], p) : 0u;
+    }
+    bool failed = false, busy = true;
+    while (busy && !failed) {
+        busy = false;
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            if (!pending[s] || failed) continue;
+            const long long u = su[s];
+            const long long un = u + STAGES * nw;
+            int pn;
+            float wn;
+            fetch_meta(un, pn, wn);  // overlaps the wait below
+            // give up as a warp, so that no lane runs ahead into a shuffle
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs))) {
+                failed = true;
+                continue;
+            }
+            ph[s] += 1;
+            pending[s] = false;
+            const int t = (int)(u / nch);
+            const int c = (int)(u - (long long)t * nch);
+            const int cb = min(CHUNK, row_bytes - c * CHUNK);
+            float wj[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) wj[j] = __shfl_sync(0xffffffffu, wr[s], j);
+            const uint32_t st = stage0 + s * STAGE_BYTES;
+            uint4* orow = reinterpret_cast<uint4*>(out + (size_t)t * row_bytes + (size_t)c * CHUNK);
+            for (int v = lane; v < cb / 16; v += 32) {
+                float acc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j >= m.k) break;
+                    if ((vm[s] >> j) & 1u) fma_bf16x8(acc, wj[j], lds_v4(st + j * CHUNK + v * 16));
+                }
+                st_v4(orow + v, pack_bf16x8(acc));
+            }
+            __syncwarp();
+            fence_proxy_async_smem();
+            su[s] = un;
+            wr[s] = wn;
+            if (un < units) {
+                vm[s] = issue(s, un, pn);
+                pending[s] = true;
+                busy = true;
+            }
+        }
+    }
+    if (failed) {
+        if (lane == 0) atomicOr(&g_move_faults, kFaultWaitTimeout);
+        drain_stages<STAGES>(bar0, pending, ph);
+    }
+}
+
+// Dispatch: each warp owns STAGES stages of CHUNK bytes of x; a stage holds one
+// (token, column chunk) unit, written to its k receive rows by k bulk stores.
+template <int WARPS, int STAGES, int CHUNK, bool EVICT_FIRST = false>
+__global__ void __launch_bounds__(WARPS * 32, 1)
+dispatch_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ x, const float* __restrict__ xs,
+                     uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t stage0 = smem_u32(smem + (size_t)warp * STAGES * CHUNK);
+    const uint32_t bar0 = smem_u32(&s_bar[warp][0]);
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int S = m.T * m.k;
+    const int nch = m.nchunks;
+    const long long units = (long long)m.T * nch;
+    const long long nw = (long long)gridDim.x * WARPS;
+    const long long gw = (long long)blockIdx.x * WARPS + warp;
+
+    long long su[STAGES];
+    bool pending[STAGES];
+    uint32_t ph[STAGES];
+    const uint64_t pol = EVICT_FIRST ? l2_evict_first_policy() : 0ull;
+    // Lane 0 issues the bulk load of unit u into stage s.
+    auto issue = [&](int s, long long u) {
+        if (lane == 0) {
+            const int t = (int)(u / nch);
+            const int c = (int)(u - (long long)t * nch);
+            const int cb = min(CHUNK, row_bytes - c * CHUNK);
+            mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)cb);
+            if (EVICT_FIRST)
+                bulk_g2s_hint(stage0 + s * CHUNK, x + (size_t)t * row_bytes + (size_t)c * CHUNK, (uint32_t)cb,
+                              bar0 + 8 * s, pol);
+            else
+                bulk_g2s(stage0 + s * CHUNK, x + (size_t)t * row_bytes + (size_t)c * CHUNK, (uint32_t)cb,
+                         bar0 + 8 * s);
+        }
+    };
+
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+        su[s] = gw + s * nw;
+        ph[s] = 0;
+        pending[s] = su[s] < units;
+        if (pending[s]) issue(s, su[s]);
+    }
+    bool failed = false, busy = true;
+    while (busy && !failed) {
+        busy = false;
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            if (!pending[s] || failed) continue;
+            const long long u = su[s];
+            const int t = (int)(u / nch);
+            const int c = (int)(u - (long long)t * nch);
+            const int cb = min(CHUNK, row_bytes - c * CHUNK);
+            int p = -1;
+            if (lane < m.k) {
+                p = m.pos[(size_t)t * m.k + lane];
+                if (p < 0 || p >= S) p = -1;
+            }
+            // give up as a warp, so that no lane runs ahead into a shuffle
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs))) {
+                failed = true;
+                continue;
+            }
+            ph[s] += 1;
+            pending[s] = false;
+            fence_proxy_async_smem();
+            if (p >= 0) {
+                if (EVICT_FIRST)
+                    bulk_s2g_hint(recv + (size_t)p * row_bytes + (size_t)c * CHUNK, stage0 + s * CHUNK,
+                                  (uint32_t)cb, pol);
+                else
+                    bulk_s2g(recv + (size_t)p * row_bytes + (size_t)c * CHUNK, stage0 + s * CHUNK, (uint32_t)cb);
+            }
+            bulk_commit();
+            if (groups > 0 && c == 0) {
+                // fp8 scales: h/128 floats per row, moved with the first chunk.
+                for (int j = 0; j < m.k; ++j) {
+                    const int pj = __shfl_sync(0xffffffffu, p, j);
+                    if (pj < 0) continue;
+                    for (int g = lane; g < groups; g += 32)
+                        rs[(size_t)pj * groups + g] = xs[(size_t)t * groups + g];
+                }
+            }
+            // The stage may be refilled once every lane's stores have read it.
+            bulk_wait_read<0>();
+            __syncwarp();
+            su[s] = u + STAGES * nw;
+            if (su[s] < units) {
+                issue(s, su[s]);
+                pending[s] = true;
+                busy = true;
+            }
+        }
+    }
+    bulk_wait_all();
+    if (failed) {
+        if (lane == 0) atomicOr(&g_move_faults, kFaultWaitTimeout);
+        drain_stages<STAGES>(bar0, pending, ph);
+    }
+}
+
 template <typename K>
 int resident_blocks(K kernel) {
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kMoveThreads, 0);
-    return max(1, sms) * max(1, per_sm);
+    return device_sm_count() * blocks_per_sm(reinterpret_cast<const void*>(kernel), kMoveThreads, 0);
 }
 
 template <typename K>
@@ -162,10 +413,52 @@ int grid_for(K kernel, long long units) {
     return (int)max(1LL, min(need, cap));
 }
 
-}  // namespace
+// Default shapes of the bulk pipelines, chosen by a sweep on GB300 at the
+// prefill-fp8 shape: warps per CTA, stages per warp, chunk bytes, CTAs per SM.
+constexpr int kCombWarps = 8, kCombStages = 2, kCombChunk = 512, kCombCtasPerSm = 3;
+constexpr int kDispWarps = 4, kDispStages = 4, kDispChunk = 7168, kDispCtasPerSm = 1;
 
-cudaError_t launch_dispatch(const MoveArgs& m0, const void* x, const float* xs, void* recv,
-                            float* rs, int groups, cudaStream_t stream) {
+template <int WARPS, int STAGES, int CHUNK, int PER_SM>
+cudaError_t launch_combine_bulk(MoveArgs m, const void* y, const float* w, void* out, cudaStream_t stream) {
+    const int row_bytes = m.nvec * 16;
+    m.nchunks = (row_bytes + CHUNK - 1) / CHUNK;
+    const long long units = (long long)m.T * m.nchunks;
+    if (units == 0) return cudaSuccess;
+    auto kern = combine_bulk_kernel<WARPS, STAGES, CHUNK>;
+    const size_t smem = (size_t)WARPS * STAGES * 8 * CHUNK;
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
+    const int sms = device_sm_count();
+    const long long need = (units + WARPS - 1) / WARPS;
+    const long long cap = (long long)sms * PER_SM;
+    const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
+    kern<<<grid, WARPS * 32, smem, stream>>>(m, static_cast<const uint8_t*>(y), w, static_cast<uint8_t*>(out),
+                                             row_bytes);
+    return cudaGetLastError();
+}
+
+template <int WARPS, int STAGES, int CHUNK, int PER_SM>
+cudaError_t launch_dispatch_bulk(MoveArgs m, const void* x, const float* xs, void* recv, float* rs,
+                                 int groups, cudaStream_t stream) {
+    const int row_bytes = m.nvec * 16;
+    m.nchunks = (row_bytes + CHUNK - 1) / CHUNK;
+    const long long units = (long long)m.T * m.nchunks;
+    if (units == 0) return cudaSuccess;
+    auto kern = dispatch_bulk_kernel<WARPS, STAGES, CHUNK>;
+    const size_t smem = (size_t)WARPS * STAGES * CHUNK;
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
+    const int sms = device_sm_count();
+    const long long need = (units + WARPS - 1) / WARPS;
+    const long long cap = (long long)sms * PER_SM;
+    const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
+    kern<<<grid, WARPS * 32, smem, stream>>>(m, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(recv), rs,
+                                             row_bytes, groups);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_lsu(const MoveArgs& m0, const void* x, const float* xs, void* recv,
+                                float* rs, int groups, cudaStream_t stream) {
     constexpr int U = 4;
     MoveArgs m = m0;
     m.chunk_vecs = 32 * U;
@@ -173,30 +466,53 @@ cudaError_t launch_dispatch(const MoveArgs& m0, const void* x, const float* xs, 
     const long long units = (long long)m.T * m.nchunks;
     if (units == 0) return cudaSuccess;
     auto kern = dispatch_kernel<U>;
-    kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(
-        m, static_cast<const uint4*>(x), xs, static_cast<uint4*>(recv), rs, groups);
+    kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(m, static_cast<const uint4*>(x), xs,
+                                                              static_cast<uint4*>(recv), rs, groups);
     return cudaGetLastError();
 }
 
 template <int KB, int U>
-static cudaError_t launch_combine_t(MoveArgs m, const void* y, const float* w, void* out,
-                                    cudaStream_t stream) {
+cudaError_t launch_combine_t(MoveArgs m, const void* y, const float* w, void* out, cudaStream_t stream) {
     m.chunk_vecs = 32 * U;
     m.nchunks = (m.nvec + m.chunk_vecs - 1) / m.chunk_vecs;
     const long long units = (long long)m.T * m.nchunks;
     if (units == 0) return cudaSuccess;
     auto kern = combine_kernel<KB, U>;
-    kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(
-        m, static_cast<const uint4*>(y), w, static_cast<uint4*>(out));
+    kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(m, static_cast<const uint4*>(y), w,
+                                                              static_cast<uint4*>(out));
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, void* out,
-                           cudaStream_t stream) {
+cudaError_t launch_combine_lsu(const MoveArgs& m, const void* y, const float* w, void* out,
+                               cudaStream_t stream) {
     if (m.k >= 8) return launch_combine_t<8, 1>(m, y, w, out, stream);
     if (m.k >= 4) return launch_combine_t<4, 2>(m, y, w, out, stream);
     if (m.k >= 2) return launch_combine_t<2, 4>(m, y, w, out, stream);
     return launch_combine_t<1, 4>(m, y, w, out, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const MoveArgs& m, const void* x, const float* xs, void* recv,
+                            float* rs, int groups, cudaStream_t stream) {
+    return launch_dispatch_bulk<kDispWarps, kDispStages, kDispChunk, kDispCtasPerSm>(m, x, xs, recv, rs, groups, stream);
+}
+
+cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, void* out,
+                           cudaStream_t stream) {
+    if (m.k <= 8) return launch_combine_bulk<kCombWarps, kCombStages, kCombChunk, kCombCtasPerSm>(m, y, w, out, stream);
+    return launch_combine_lsu(m, y, w, out, stream);
+}
+
+cudaError_t read_move_faults(uint32_t* bits, cudaStream_t stream) {
+    unsigned v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_move_faults, sizeof(v), 0, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_move_faults, &zero, sizeof(zero), 0,
+                                                      cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) *bits = v;
+    return e;
 }
 
 }  // namespace moe

@@ -235,6 +235,14 @@ int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream
 int moe_layout_noalloc(const moe_problem* problem, const int32_t* ids,
                        const moe_layout_t* layout, moe_stream_t stream);
 
+/* Device faults of the row movers since the last call: bit
+ * MOE_FAULT_WAIT_TIMEOUT is set when a bulk-copy pipeline of moe_dispatch or
+ * moe_combine waited more than one second for its own copies, gave up, drained
+ * them and returned (its output is then incomplete).  Waits for the stream,
+ * copies the bits to *bits and clears them. */
+#define MOE_FAULT_WAIT_TIMEOUT 0x1u
+int moe_move_faults(uint32_t* bits, moe_stream_t stream);
+
 /* A short English description of a moe_status_code. */
 const char* moe_status_string(int code);
 
