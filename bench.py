@@ -2,8 +2,9 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-A step is one pass of the whole hot path over one batch: moe_layout,
-moe_stats, moe_dispatch, moe_combine (five kernels), inputs resident in HBM.
+A step is one pass of the whole hot path over one batch: moe_layout (which
+also writes the statistics record), moe_dispatch and moe_combine, inputs
+resident in HBM.
 The headline value is the effective HBM bandwidth of dispatch + combine: their
 algorithmic bytes (read each token row once and write k copies; read k rows
 and write one) divided by the whole step's time, layout and stats included.
@@ -32,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "dispatch+combine µs and effective HBM GB/s (fraction of GB300 peak) per layer"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 5  # count, rank, stats copy, dispatch, combine
+KERNELS_PER_STEP = 3  # layout (one cooperative kernel), dispatch, combine
 
 
 def algorithmic_bytes(w, tokens=None):
@@ -270,9 +271,9 @@ def run_ours(args, w):
     gates = mw.gen_gates(w)
     prob = moe.Problem(w.T, w.h, w.k, w.E, w.R, w.P, w.R_src,
                        moe.MOE_DTYPE_FP8_E4M3 if fp8 else moe.MOE_DTYPE_BF16)
-    lay = moe.Layout(prob, dev)
+    lay = moe.Layout(prob, dev, with_stats=True)  # the layout call also writes the statistics
     ws = moe.alloc_workspace(prob, dev)
-    stats = torch.empty(moe.moe_stats_words(prob), dtype=torch.int64, device=dev)
+    stats = lay.stats
     ids_d = torch.from_numpy(ids).to(dev)
     gates_d = torch.from_numpy(gates).to(dev)
     if fp8:
@@ -292,10 +293,9 @@ def run_ours(args, w):
 
     def step(ev=None):
         # Events bracket the two row movers: before dispatch, between dispatch
-        # and combine, after combine.  Layout and statistics take the rest of
-        # the step.
+        # and combine, after combine.  Layout and statistics (written by the
+        # layout call into lay.stats) take the rest of the step.
         moe.moe_layout(prob, ids_d, ws, lay, stream)
-        moe.moe_stats(prob, lay, ws, stats, stream)
         if ev is not None:
             ev[0].record(stream)
         moe.moe_dispatch(prob, lay, x_d, xs_d, recv, recv_s, stream)

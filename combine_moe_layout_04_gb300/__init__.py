@@ -21,10 +21,12 @@ from typing import Optional
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_layout.so")
 
-MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_BAD_IDS, MOE_ERR_ALIGN, MOE_ERR_CAPACITY = 0, 1, 2, 3, 4, 5
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_BAD_IDS, MOE_ERR_ALIGN, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT = \
+    0, 1, 2, 3, 4, 5, 6
 MOE_NOALLOC_SCRATCH_BYTES = 2 << 20
 MOE_DTYPE_BF16, MOE_DTYPE_FP8_E4M3 = 0, 1
 MOE_STATUS_ID_RANGE, MOE_STATUS_ID_REPEAT, MOE_STATUS_PLACEMENT, MOE_STATUS_SRC_OFFSET = 1, 2, 4, 8
+MOE_STATUS_TIMEOUT = 16
 MOE_FP8_GROUP = 128
 MOE_STATS_HEADER_WORDS = 32
 MOE_FAULT_WAIT_TIMEOUT = 1
@@ -67,7 +69,7 @@ _LAYOUT_FIELDS = ("expert_count", "expert_offset", "rank_count", "rank_offset", 
 
 
 class _LayoutC(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in _LAYOUT_FIELDS]
+    _fields_ = [(n, ctypes.c_void_p) for n in _LAYOUT_FIELDS] + [("stats", ctypes.c_void_p)]
 
 
 _lib = None
@@ -153,7 +155,7 @@ class Problem:
 class Layout:
     """Caller-owned device arrays of a layout (moe_layout_t)."""
 
-    def __init__(self, problem: Problem, device="cuda"):
+    def __init__(self, problem: Problem, device="cuda", with_stats: bool = False):
         import torch
         p = problem
         i32 = dict(dtype=torch.int32, device=device)
@@ -166,9 +168,14 @@ class Layout:
         self.host_mask = torch.empty((p.num_tokens, p.num_hosts), dtype=torch.uint8, device=device)
         self.pos = torch.empty((p.num_tokens, p.topk), **i32)
         self.recv_src = torch.empty(p.num_tokens * p.topk, **i32)
+        # Optional: the statistics record, written by moe_layout itself.
+        self.stats = (torch.empty(moe_stats_words(p), dtype=torch.int64, device=device)
+                      if with_stats else None)
 
     def c(self) -> _LayoutC:
-        return _LayoutC(*[getattr(self, n).data_ptr() for n in _LAYOUT_FIELDS])
+        stats = getattr(self, "stats", None)
+        return _LayoutC(*[getattr(self, n).data_ptr() for n in _LAYOUT_FIELDS],
+                        None if stats is None else stats.data_ptr())
 
     def to_host(self) -> dict:
         return {n: getattr(self, n).cpu().numpy() for n in _LAYOUT_FIELDS}

@@ -81,7 +81,7 @@ int moe_layout(const moe_problem* problem, const int32_t* ids, void* workspace,
     if (rc != MOE_OK) return rc;
     if (!layout_complete(layout, d.T) || workspace == nullptr || (d.T > 0 && ids == nullptr))
         return MOE_ERR_INVALID;
-    if (!aligned(workspace, 256) || !aligned(ids, 4)) return MOE_ERR_ALIGN;
+    if (!aligned(workspace, 256) || !aligned(ids, 4) || !aligned(layout->stats, 8)) return MOE_ERR_ALIGN;
     moe::LayoutArgs a{};
     a.ids = ids;
     a.expert_to_rank = problem->expert_to_rank;
@@ -159,6 +159,7 @@ int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     *status_bits = bits;
+    if (bits & MOE_STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
     if (bits & (MOE_STATUS_ID_RANGE | MOE_STATUS_ID_REPEAT)) return MOE_ERR_BAD_IDS;
     if (bits & (MOE_STATUS_PLACEMENT | MOE_STATUS_SRC_OFFSET)) return MOE_ERR_INVALID;
     return MOE_OK;
@@ -177,6 +178,7 @@ const char* moe_status_string(int code) {
         case MOE_ERR_BAD_IDS: return "expert id out of range or repeated within a token";
         case MOE_ERR_ALIGN: return "misaligned buffer";
         case MOE_ERR_CAPACITY: return "problem too large for the fixed layout scratch";
+        case MOE_ERR_TIMEOUT: return "a bounded device wait gave up";
         default: return "unknown status";
     }
 }

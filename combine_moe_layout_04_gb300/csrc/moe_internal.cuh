@@ -31,6 +31,7 @@ constexpr int kLayoutGroup = 16;
 // every layout; the per-block table follows.
 struct WsLayout {
     size_t status;                                  // u32 device status bits
+    size_t barrier;                                 // u32 grid-barrier arrivals
     size_t hcount;                                  // int32 [H]
     size_t src_tokens, src_mode0, src_mode1, src_mode2;            // int32 [R_src]
     size_t dst_tokens, dst_self, dst_local, dst_remote, dst_relay;  // int32 [R]
@@ -51,6 +52,7 @@ inline WsLayout make_ws_layout(int T, int E, int R, int H, int Rs) {
     w.blocks = T > 0 ? (T + kLayoutTokensPerBlock - 1) / kLayoutTokensPerBlock : 1;
     w.groups = (w.blocks + kLayoutGroup - 1) / kLayoutGroup;
     w.status = take(4);
+    w.barrier = take(4);
     w.hcount = take(4 * (size_t)H);
     // The four per-source and the five per-destination arrays are contiguous.
     w.src_tokens = take(4 * 4 * (size_t)Rs);
@@ -99,6 +101,12 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;
     asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // Streaming 16-byte load through the non-coherent path, no L1 allocation.

@@ -3,12 +3,12 @@
 // The layout is a stable counting sort of the T*k slots by the key
 // (rank(e), e), plus the per-(token, host) de-duplication mask of Mode 2
 // ("Balancing and Beyond", section 3.2: one network copy per token and remote
-// host, relayed through the same-index GPU).  Two kernels:
+// host, relayed through the same-index GPU).  Two phases:
 //
 //  count  one thread per token, 128 tokens per block.  A token's k ids stay in
 //         registers.  Every counter is aggregated across the warp before it
-//         touches shared memory: __match_any_sync groups equal experts and
-//         equal (category, rank) keys, ballots count hosts, shuffles reduce
+//         touches shared memory: __match_any_sync groups equal expert ids,
+//         ballots count the tokens per rank and per host, shuffles reduce
 //         the per-source-rank counts.  Each block publishes its expert
 //         histogram to a [B][E] table and adds it to the totals of its group
 //         of 16 blocks (16 atomics per counter instead of B).
@@ -21,11 +21,16 @@
 //         expert totals (the sum of the group rows) and the expert and rank
 //         offsets itself (cheap: O(E + R)); block 0 writes them out and also
 //         writes the statistics record into the workspace, so moe_stats is a
-//         plain copy.  The kernel starts early under
-//         programmatic dependent launch and ranks its slots (ids only) before
-//         it waits for the count kernel.
+//         plain copy.
 //
-// No kernel here spins on a flag, so none can hang.
+// Where the whole grid fits on the GPU at once, both phases run in one
+// cooperative kernel: each block counts, ranks its own slots (ids only),
+// publishes its counts and meets the others at one grid barrier before the
+// rest of the rank phase.  The barrier's counter is cleared with the other
+// accumulators before the launch, and its wait gives up after one second
+// (status bit MOE_STATUS_TIMEOUT) instead of spinning forever.  Otherwise the
+// phases run as two kernels, the second launched under programmatic dependent
+// launch so that its id-only ranking overlaps the first.
 
 #include <cuda_runtime.h>
 
@@ -99,7 +104,7 @@ __device__ __forceinline__ int src_rank_of(const LayoutArgs& a, const int32_t* s
 
 __device__ __forceinline__ int clamp_id(int e, int E) { return (e < 0 || e >= E) ? 0 : e; }
 
-// One atomic per group of lanes holding the same non-negative key.
+// One atomic per group of lanes holding the same non-negative key; -1 skips.
 __device__ __forceinline__ void warp_count(int32_t* counters, int key) {
     const unsigned same = __match_any_sync(kFull, key);
     if (key >= 0 && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&counters[key], __popc(same));
@@ -194,13 +199,15 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
         if (lane == 0) s_red[i][warp] = w;
     }
     __syncthreads();
+    __shared__ unsigned long long s_fin[R_COUNT];
+    if (tid < R_COUNT) {
+        unsigned long long x = 0ull;
+        for (int w = 0; w < nwarps; ++w) x = tid < RSUM_TOK ? max(x, s_red[tid][w]) : x + s_red[tid][w];
+        s_fin[tid] = x;
+    }
+    __syncthreads();
     if (tid == 0) {
-        unsigned long long r[R_COUNT];
-        for (int i = 0; i < R_COUNT; ++i) {
-            r[i] = 0ull;
-            for (int w = 0; w < nwarps; ++w)
-                r[i] = i < RSUM_TOK ? max(r[i], s_red[i][w]) : r[i] + s_red[i][w];
-        }
+        const unsigned long long* r = s_fin;
         for (int i = 0; i < MOE_STATS_HEADER_WORDS; ++i) rec[i] = 0;
         const int64_t S = (int64_t)a.T * a.k;
         const int64_t emax = (int64_t)(r[RMAX_EXPERT] >> 32);
@@ -233,57 +240,84 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
         rec[MOE_ST_RANK_IMBALANCE] = __double_as_longlong(rratio);
         rec[MOE_ST_NUM_HOSTS] = a.H;
     }
+    if (a.out.stats != nullptr) {
+        // The caller asked for the record with the layout as well.
+        __syncthreads();
+        for (size_t i = tid; i < a.wl.stats_words; i += blockDim.x) a.out.stats[i] = rec[i];
+    }
 }
 
-template <int KMAX>
-__global__ void __launch_bounds__(kCountThreads)
-layout_count_kernel(const LayoutArgs a) {
-    extern __shared__ int32_t smem[];
-    int32_t* s_rank = smem;                  // [E] rank of each expert
-    int32_t* s_host = s_rank + a.E;          // [E] host of each expert
-    int32_t* s_hist = s_host + a.E;          // [E] this block's expert counts
-    int32_t* s_hc = s_hist + a.E;            // [64] tokens per host
-    int32_t* s_soff = s_hc + kHostSlots;     // [Rs+1] source offsets
-    int32_t* s_src = s_soff + (a.Rs + 1);    // [4][Rs] tokens, mode0, mode1, mode2
-    int32_t* s_dst = s_src + 4 * a.Rs;       // [5][R] tokens, self, local, remote, relay
+// ---- count phase -----------------------------------------------------------
+
+struct CountSmem {
+    const int32_t* eid;  // the block's ids staged in shared memory, or NULL (read global)
+    int32_t* rank;   // [E] rank of each expert
+    int32_t* host;   // [E] host of each expert
+    int32_t* hist;   // [E] this block's expert counts
+    int32_t* hc;     // [64] tokens per host
+    int32_t* soff;   // [Rs+1] source offsets
+    int32_t* src;    // [4][Rs] tokens, mode0, mode1, mode2
+    int32_t* dst;    // [5][R] tokens, self, local, remote, relay
+};
+
+__host__ __device__ inline size_t count_smem_words(int E, int R, int Rs) {
+    return 3 * (size_t)E + kHostSlots + (Rs + 1) + 4 * (size_t)Rs + 5 * (size_t)R;
+}
+
+__device__ inline CountSmem carve_count(const LayoutArgs& a, int32_t* base) {
+    CountSmem m;
+    m.eid = nullptr;
+    m.rank = base;
+    m.host = m.rank + a.E;
+    m.hist = m.host + a.E;
+    m.hc = m.hist + a.E;
+    m.soff = m.hc + kHostSlots;
+    m.src = m.soff + (a.Rs + 1);
+    m.dst = m.src + 4 * a.Rs;
+    return m;
+}
+
+// Counts the block's 128 tokens (threads 0..127 hold one token each; any
+// further threads take part in the collectives with no token) and publishes
+// the block's expert histogram and counters.  All threads of the block call
+// it.  With HIST the expert histogram is counted here; without, sm.hist
+// already holds it (the rank prologue counted the same slots).
+template <int KMAX, bool HIST>
+__device__ void count_phase(const LayoutArgs& a, const CountSmem& sm, int b) {
     __shared__ uint32_t s_status;
-
-    // The rank kernel's prologue only reads ids: let it start now.
-    pdl_launch_dependents();
-
+    __shared__ int s_rs0;
     const int tid = threadIdx.x, lane = tid & 31;
-    const int b = blockIdx.x;
     if (tid == 0) s_status = 0;
     uint32_t st = 0;
     for (int e = tid; e < a.E; e += blockDim.x) {
         const int r = rank_of_expert(a, e, &st);
-        s_rank[e] = r;
-        s_host[e] = r / a.P;
-        s_hist[e] = 0;
+        sm.rank[e] = r;
+        sm.host[e] = r / a.P;
+        if (HIST) sm.hist[e] = 0;
     }
-    for (int i = tid; i < kHostSlots; i += blockDim.x) s_hc[i] = 0;
-    for (int i = tid; i < 4 * a.Rs; i += blockDim.x) s_src[i] = 0;
-    for (int i = tid; i < 5 * a.R; i += blockDim.x) s_dst[i] = 0;
+    for (int i = tid; i < kHostSlots; i += blockDim.x) sm.hc[i] = 0;
+    for (int i = tid; i < 4 * a.Rs; i += blockDim.x) sm.src[i] = 0;
+    for (int i = tid; i < 5 * a.R; i += blockDim.x) sm.dst[i] = 0;
     if (a.src_offsets) {
-        for (int i = tid; i <= a.Rs; i += blockDim.x) s_soff[i] = a.src_offsets[i];
+        for (int i = tid; i <= a.Rs; i += blockDim.x) sm.soff[i] = a.src_offsets[i];
     }
     __syncthreads();
     if (a.src_offsets && b == 0) {
         for (int i = tid; i < a.Rs; i += blockDim.x)
-            if (s_soff[i + 1] < s_soff[i]) st |= MOE_STATUS_SRC_OFFSET;
-        if (tid == 0 && (s_soff[0] != 0 || s_soff[a.Rs] != a.T)) st |= MOE_STATUS_SRC_OFFSET;
+            if (sm.soff[i + 1] < sm.soff[i]) st |= MOE_STATUS_SRC_OFFSET;
+        if (tid == 0 && (sm.soff[0] != 0 || sm.soff[a.Rs] != a.T)) st |= MOE_STATUS_SRC_OFFSET;
     }
 
     const int t = b * kLayoutTokensPerBlock + tid;
-    const bool valid = t < a.T;
-    const int rs = valid ? min(max(src_rank_of(a, s_soff, t), 0), a.Rs - 1) : 0;
+    const bool valid = tid < kLayoutTokensPerBlock && t < a.T;
+    const int rs = valid ? min(max(src_rank_of(a, sm.soff, t), 0), a.Rs - 1) : 0;
     const int own = rs / a.P;
-    __shared__ int s_rs0;
-    if (tid == 0) s_rs0 = rs;  // thread 0 always holds a token
-    __syncthreads();
+    // Token b*128 always exists: its source rank is the block's first.
+    const int rs_first = min(max(src_rank_of(a, sm.soff, b * kLayoutTokensPerBlock), 0), a.Rs - 1);
+    if (tid == 0) s_rs0 = rs_first;
     // Usual case: one source rank for the whole block (every token of a rank
     // is contiguous and a rank holds at least 128 tokens in most layouts).
-    const bool block_one_src = __syncthreads_and(!valid || rs == s_rs0);
+    const bool block_one_src = __syncthreads_and(!valid || rs == rs_first);
     const bool small_r = a.R <= 64;  // a token's ranks fit a 64-bit mask
 
     // The token's ids, validated, then clamped into [0, E).
@@ -292,7 +326,8 @@ layout_count_kernel(const LayoutArgs a) {
     for (int j = 0; j < KMAX; ++j) {
         ev[j] = -1;
         rv[j] = -1;
-        if (j < a.k && valid) ev[j] = a.ids[(size_t)t * a.k + j];
+        if (j < a.k && valid)
+            ev[j] = sm.eid ? sm.eid[tid * a.k + j] : a.ids[(size_t)t * a.k + j];
     }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
@@ -313,10 +348,10 @@ layout_count_kernel(const LayoutArgs a) {
     for (int j = 0; j < KMAX; ++j) {
         if (j >= a.k) break;  // a.k is the same for the whole warp
         const int e = ev[j];  // -1 for tokens past T
-        warp_count(s_hist, e);
+        if (HIST) warp_count(sm.hist, e);
         if (e >= 0) {
-            const int r = s_rank[e];
-            const int hh = s_host[e];
+            const int r = sm.rank[e];
+            const int hh = sm.host[e];
             rv[j] = r;
             hmask |= 1ull << hh;
             mode0 += (r != rs);
@@ -327,25 +362,26 @@ layout_count_kernel(const LayoutArgs a) {
                 bool first = true;  // first slot of this token on rank r
 #pragma unroll
                 for (int i = 0; i < j; ++i) first = first && (rv[i] != r);
-                if (first) atomicAdd(&s_dst[r], 1);
+                if (first) atomicAdd(&sm.dst[r], 1);
             }
             if (!block_one_src) {
                 const int cat = (r == rs) ? 1 : (hh == own ? 2 : 3);  // self, local, remote
-                atomicAdd(&s_dst[cat * a.R + r], 1);
+                atomicAdd(&sm.dst[cat * a.R + r], 1);
             }
         }
     }
     if (small_r) {
-        // Tokens per rank: one ballot per rank that some lane reaches.
-        unsigned long long any = rmask;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) any |= __shfl_xor_sync(kFull, any, off);
-        while (any) {
-            const int r = __ffsll((long long)any) - 1;
-            any &= any - 1;
-            const unsigned m = __ballot_sync(kFull, (rmask >> r) & 1ull);
-            if (lane == 0) atomicAdd(&s_dst[r], __popc(m));
+        // Tokens per rank: one ballot per rank; lane r (and r - 32) keeps the
+        // count of rank r and adds it with a single atomic.
+        int mine_lo = 0, mine_hi = 0;
+#pragma unroll 8
+        for (int r = 0; r < a.R; ++r) {
+            const int c = __popc(__ballot_sync(kFull, (rmask >> r) & 1ull));
+            if (r == lane) mine_lo = c;
+            if (r == lane + 32) mine_hi = c;
         }
+        if (lane < a.R && mine_lo) atomicAdd(&sm.dst[lane], mine_lo);
+        if (lane + 32 < a.R && mine_hi) atomicAdd(&sm.dst[lane + 32], mine_hi);
     }
     if (valid) {
         uint8_t* mrow = a.out.host_mask + (size_t)t * a.H;
@@ -353,36 +389,36 @@ layout_count_kernel(const LayoutArgs a) {
     }
     for (int hh = 0; hh < a.H; ++hh) {
         const unsigned m = __ballot_sync(kFull, valid && ((hmask >> hh) & 1ull));
-        if (lane == 0 && m) atomicAdd(&s_hc[hh], __popc(m));
+        if (lane == 0 && m) atomicAdd(&sm.hc[hh], __popc(m));
     }
     const int mode2 = valid ? __popcll(hmask & ~(1ull << own)) : 0;
     const int rs0 = __shfl_sync(kFull, rs, 0);
     if (__all_sync(kFull, !valid || rs == rs0)) {
-        // The warp's tokens share one source rank.
+        // The warp's tokens share one source rank (or it has none).
         const int n_tok = warp_sum(valid ? 1 : 0);
         const int n0 = warp_sum(mode0), n1 = warp_sum(mode1), n2 = warp_sum(mode2);
         if (lane == 0 && n_tok > 0) {
-            atomicAdd(&s_src[0 * a.Rs + rs0], n_tok);
-            atomicAdd(&s_src[1 * a.Rs + rs0], n0);
-            atomicAdd(&s_src[2 * a.Rs + rs0], n1);
-            atomicAdd(&s_src[3 * a.Rs + rs0], n2);
+            atomicAdd(&sm.src[0 * a.Rs + rs0], n_tok);
+            atomicAdd(&sm.src[1 * a.Rs + rs0], n0);
+            atomicAdd(&sm.src[2 * a.Rs + rs0], n1);
+            atomicAdd(&sm.src[3 * a.Rs + rs0], n2);
         }
         const int own0 = rs0 / a.P;
         for (int hh = 0; hh < a.H; ++hh) {
             if (hh == own0) continue;
             const unsigned m = __ballot_sync(kFull, valid && ((hmask >> hh) & 1ull));
-            if (lane == 0 && m) atomicAdd(&s_dst[4 * a.R + hh * a.P + rs0 % a.P], __popc(m));
+            if (lane == 0 && m) atomicAdd(&sm.dst[4 * a.R + hh * a.P + rs0 % a.P], __popc(m));
         }
     } else if (valid) {
-        atomicAdd(&s_src[0 * a.Rs + rs], 1);
-        atomicAdd(&s_src[1 * a.Rs + rs], mode0);
-        atomicAdd(&s_src[2 * a.Rs + rs], mode1);
-        atomicAdd(&s_src[3 * a.Rs + rs], mode2);
+        atomicAdd(&sm.src[0 * a.Rs + rs], 1);
+        atomicAdd(&sm.src[1 * a.Rs + rs], mode0);
+        atomicAdd(&sm.src[2 * a.Rs + rs], mode1);
+        atomicAdd(&sm.src[3 * a.Rs + rs], mode2);
         unsigned long long bits = hmask & ~(1ull << own);
         while (bits) {
             const int hh = __ffsll((long long)bits) - 1;
             bits &= bits - 1;
-            atomicAdd(&s_dst[4 * a.R + hh * a.P + rs % a.P], 1);
+            atomicAdd(&sm.dst[4 * a.R + hh * a.P + rs % a.P], 1);
         }
     }
     if (st) atomicOr(&s_status, st);
@@ -391,11 +427,11 @@ layout_count_kernel(const LayoutArgs a) {
         // Slots by (category, destination rank) follow from the expert counts.
         const int own_b = s_rs0 / a.P;
         for (int e = tid; e < a.E; e += blockDim.x) {
-            const int c = s_hist[e];
+            const int c = sm.hist[e];
             if (c == 0) continue;
-            const int r = s_rank[e];
-            const int cat = (r == s_rs0) ? 1 : (s_host[e] == own_b ? 2 : 3);
-            atomicAdd(&s_dst[cat * a.R + r], c);
+            const int r = sm.rank[e];
+            const int cat = (r == s_rs0) ? 1 : (sm.host[e] == own_b ? 2 : 3);
+            atomicAdd(&sm.dst[cat * a.R + r], c);
         }
         __syncthreads();
     }
@@ -404,58 +440,90 @@ layout_count_kernel(const LayoutArgs a) {
     int32_t* g_agg = reinterpret_cast<int32_t*>(a.ws + a.wl.agg) + (size_t)b * a.E;
     int32_t* g_group = reinterpret_cast<int32_t*>(a.ws + a.wl.group) + (size_t)(b / kLayoutGroup) * a.E;
     for (int e = tid; e < a.E; e += blockDim.x) {
-        const int v = s_hist[e];
+        const int v = sm.hist[e];
         g_agg[e] = v;
         if (v) atomicAdd(&g_group[e], v);
     }
     int32_t* g_hcount = reinterpret_cast<int32_t*>(a.ws + a.wl.hcount);
     for (int hh = tid; hh < a.H; hh += blockDim.x)
-        if (s_hc[hh]) atomicAdd(&g_hcount[hh], s_hc[hh]);
+        if (sm.hc[hh]) atomicAdd(&g_hcount[hh], sm.hc[hh]);
     int32_t* g_src = reinterpret_cast<int32_t*>(a.ws + a.wl.src_tokens);  // 4 blocks of R_src
     for (int i = tid; i < 4 * a.Rs; i += blockDim.x)
-        if (s_src[i]) atomicAdd(&g_src[i], s_src[i]);
+        if (sm.src[i]) atomicAdd(&g_src[i], sm.src[i]);
     int32_t* g_dst = reinterpret_cast<int32_t*>(a.ws + a.wl.dst_tokens);  // 5 blocks of R
     for (int i = tid; i < 5 * a.R; i += blockDim.x)
-        if (s_dst[i]) atomicAdd(&g_dst[i], s_dst[i]);
+        if (sm.dst[i]) atomicAdd(&g_dst[i], sm.dst[i]);
     if (tid == 0 && s_status) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), s_status);
 }
 
-__global__ void __launch_bounds__(kRankThreads)
-layout_rank_kernel(const LayoutArgs a) {
-    extern __shared__ int32_t smem[];
-    int32_t* s_whist = smem;                            // [8][E] per-warp counts -> warp prefixes
-    int32_t* s_agg = s_whist + kRankWarps * a.E;        // [E] this block's counts
-    int32_t* s_tot = s_agg + a.E;                       // [E] totals over all blocks
-    int32_t* s_rank = s_tot + a.E;                      // [E] rank of each expert
-    int32_t* s_order = s_rank + a.E;                    // [E] experts in (rank, e) order
-    int32_t* s_scan = s_order + a.E;                    // [E] receive offsets, in that order
-    int32_t* s_base = s_scan + a.E;                     // [E] first receive row of the block's slots
-    int32_t* s_part = s_base + a.E;                     // [2][256] partial totals and prefixes
-    int32_t* s_rstart = s_part + 2 * kRankThreads;      // [R+1] first position of a rank in s_order
-    int32_t* s_rfill = s_rstart + (a.R + 1);            // [R]
-    int32_t* s_lrank = s_rfill + a.R;                   // [T_B * k] rank inside the warp's run
-    __shared__ int32_t s_warp[32];
+// ---- rank phase ------------------------------------------------------------
 
-    pdl_launch_dependents();  // the next kernel waits for this one's results
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.x;
+struct RankSmem {
+    int32_t* whist;   // [8][E] per-warp counts -> warp prefixes
+    int32_t* tot;     // [E] totals over all blocks
+    int32_t* rank;    // [E] rank of each expert
+    int32_t* order;   // [E] experts in (rank, e) order
+    int32_t* scan;    // [E] receive offsets, in that order
+    int32_t* base;    // [E] first receive row of the block's slots
+    int32_t* part;    // [2][256] partial totals and prefixes
+    int32_t* rstart;  // [R+1] first position of a rank in order
+    int32_t* rfill;   // [R]
+    int32_t* lrank;   // [T_B * k] rank inside the warp's run
+    int32_t* eid;     // [T_B * k] the block's ids, as read
+};
+
+__host__ __device__ inline size_t rank_smem_words(int E, int R, int k) {
+    return (size_t)(kRankWarps + 5) * E + 2 * kRankThreads + (2 * (size_t)R + 1) +
+           2 * (size_t)kLayoutTokensPerBlock * k;
+}
+
+__device__ inline RankSmem carve_rank(const LayoutArgs& a, int32_t* base) {
+    RankSmem m;
+    m.whist = base;
+    m.tot = m.whist + kRankWarps * a.E;
+    m.rank = m.tot + a.E;
+    m.order = m.rank + a.E;
+    m.scan = m.order + a.E;
+    m.base = m.scan + a.E;
+    m.part = m.base + a.E;
+    m.rstart = m.part + 2 * kRankThreads;
+    m.rfill = m.rstart + (a.R + 1);
+    m.lrank = m.rfill + a.R;
+    m.eid = m.lrank + kLayoutTokensPerBlock * a.k;
+    return m;
+}
+
+struct SlotRange {
+    int s0, s1, nslots, spw;  // block's slots [s0, s1), slots per warp run
+};
+
+__device__ inline SlotRange slot_range(const LayoutArgs& a, int b) {
+    SlotRange r;
     const int S = a.T * a.k;
-    const int s0 = b * kLayoutTokensPerBlock * a.k;
-    const int s1 = min(S, s0 + kLayoutTokensPerBlock * a.k);
-    const int nslots = s1 - s0;
-    const int spw = (nslots + kRankWarps * 32 - 1) / (kRankWarps * 32) * 32;
+    r.s0 = min(S, b * kLayoutTokensPerBlock * a.k);
+    r.s1 = min(S, r.s0 + kLayoutTokensPerBlock * a.k);
+    r.nslots = r.s1 - r.s0;
+    r.spw = (r.nslots + kRankWarps * 32 - 1) / (kRankWarps * 32) * 32;
+    return r;
+}
 
-    for (int i = tid; i < kRankWarps * a.E; i += blockDim.x) s_whist[i] = 0;
+// Stable rank of each of the block's slots among the same expert's slots of
+// its warp's run (ids only), then exclusive per-warp prefixes per expert.
+// Needs exactly kRankThreads threads.
+__device__ void rank_prologue(const LayoutArgs& a, const RankSmem& sm, int b) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const SlotRange sr = slot_range(a, b);
+    // Stage the block's ids: independent loads, one round trip.
+    for (int i = tid; i < sr.nslots; i += blockDim.x) sm.eid[i] = a.ids[sr.s0 + i];
+    for (int i = tid; i < kRankWarps * a.E; i += blockDim.x) sm.whist[i] = 0;
     __syncthreads();
-
-    // Stable rank of each slot among the same expert's slots of this warp's run.
-    int32_t* my_hist = s_whist + warp * a.E;
-    const int w_lo = s0 + warp * spw;
-    const int w_hi = min(s1, w_lo + spw);
-    for (int base = w_lo; base < w_lo + spw; base += 32) {
+    int32_t* my_hist = sm.whist + warp * a.E;
+    const int w_lo = sr.s0 + warp * sr.spw;
+    const int w_hi = min(sr.s1, w_lo + sr.spw);
+    for (int base = w_lo; base < w_lo + sr.spw; base += 32) {
         const int s = base + lane;
         const bool valid = s < w_hi;
-        const int e = valid ? clamp_id(a.ids[s], a.E) : -1;
+        const int e = valid ? clamp_id(sm.eid[s - sr.s0], a.E) : -1;
         const unsigned same = __match_any_sync(kFull, e);
         const int leader = __ffs(same) - 1;
         int before = 0;
@@ -464,30 +532,41 @@ layout_rank_kernel(const LayoutArgs a) {
             my_hist[e] = before + __popc(same);
         }
         before = __shfl_sync(kFull, before, leader);
-        if (valid) s_lrank[s - s0] = before + __popc(same & lanemask_lt());
+        if (valid) sm.lrank[s - sr.s0] = before + __popc(same & lanemask_lt());
         __syncwarp();
     }
-    uint32_t st_unused = 0;
-    for (int e = tid; e < a.E; e += blockDim.x) s_rank[e] = rank_of_expert(a, e, &st_unused);
     __syncthreads();
     for (int e = tid; e < a.E; e += blockDim.x) {
         int run = 0;
 #pragma unroll
         for (int w = 0; w < kRankWarps; ++w) {
-            const int c = s_whist[w * a.E + e];
-            s_whist[w * a.E + e] = run;
+            const int c = sm.whist[w * a.E + e];
+            sm.whist[w * a.E + e] = run;
             run += c;
         }
-        s_agg[e] = run;
+        sm.tot[e] = run;  // this block's expert histogram (until rank_finish)
     }
+    __syncthreads();
+}
 
-    // From here on the count kernel's tables are needed.  One pass of loads
-    // gives each expert's total (all group rows) and this block's prefix (the
-    // group rows before its group, then the blocks of its own group before it).
-    pdl_wait();
+// The rest of the rank phase, once every block's counts are published:
+// totals, offsets, this block's prefix, outputs, statistics (block 0) and
+// the positions of the block's slots.
+__device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b) {
+    __shared__ int32_t s_warp[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int S = a.T * a.k;
+    const SlotRange sr = slot_range(a, b);
     const int32_t* g_group = reinterpret_cast<const int32_t*>(a.ws + a.wl.group);
     const int32_t* g_agg = reinterpret_cast<const int32_t*>(a.ws + a.wl.agg);
+    if (a.expert_to_rank != nullptr) {
+        uint32_t st_unused = 0;
+        for (int e = tid; e < a.E; e += blockDim.x) sm.rank[e] = rank_of_expert(a, e, &st_unused);
+    }
     {
+        // One pass of loads gives each expert's total (all group rows) and
+        // this block's prefix (the group rows before its group, then the
+        // blocks of its own group before it).
         const int sb = b / kLayoutGroup;
         const int tail0 = sb * kLayoutGroup;
         const int G = a.wl.groups;
@@ -498,31 +577,31 @@ layout_rank_kernel(const LayoutArgs a) {
             const bool active = slot < a.E && part < parts;
             int tot = 0, pre = 0;
             if (active) {
-#pragma unroll 4
+#pragma unroll 8
                 for (int g = part; g < G; g += parts) {
                     const int v = __ldcg(g_group + (size_t)g * a.E + slot);
                     tot += v;
                     pre += g < sb ? v : 0;
                 }
-#pragma unroll 4
+#pragma unroll 8
                 for (int p = tail0 + part; p < b; p += parts) pre += __ldcg(g_agg + (size_t)p * a.E + slot);
             }
-            s_part[tid] = active ? tot : 0;
-            s_part[kRankThreads + tid] = active ? pre : 0;
+            sm.part[tid] = active ? tot : 0;
+            sm.part[kRankThreads + tid] = active ? pre : 0;
             __syncthreads();
             if (parts > 1) {
                 if (tid < a.E) {
                     int sum_t = 0, sum_p = 0;
                     for (int q = 0; q < parts; ++q) {
-                        sum_t += s_part[q * a.E + tid];
-                        sum_p += s_part[kRankThreads + q * a.E + tid];
+                        sum_t += sm.part[q * a.E + tid];
+                        sum_p += sm.part[kRankThreads + q * a.E + tid];
                     }
-                    s_tot[tid] = sum_t;
-                    s_base[tid] = sum_p;
+                    sm.tot[tid] = sum_t;
+                    sm.base[tid] = sum_p;
                 }
             } else if (slot < a.E) {
-                s_tot[slot] = s_part[tid];
-                s_base[slot] = s_part[kRankThreads + tid];
+                sm.tot[slot] = sm.part[tid];
+                sm.base[slot] = sm.part[kRankThreads + tid];
             }
             __syncthreads();
         }
@@ -532,54 +611,54 @@ layout_rank_kernel(const LayoutArgs a) {
     // contiguous placement).
     if (a.expert_to_rank == nullptr) {
         const int per = a.E / a.R;
-        for (int i = tid; i < a.E; i += blockDim.x) s_order[i] = i;
-        for (int r = tid; r <= a.R; r += blockDim.x) s_rstart[r] = r * per;
+        for (int i = tid; i < a.E; i += blockDim.x) sm.order[i] = i;
+        for (int r = tid; r <= a.R; r += blockDim.x) sm.rstart[r] = r * per;
     } else {
-        for (int r = tid; r < a.R; r += blockDim.x) { s_rstart[r] = 0; s_rfill[r] = 0; }
+        for (int r = tid; r < a.R; r += blockDim.x) { sm.rstart[r] = 0; sm.rfill[r] = 0; }
         __syncthreads();
-        for (int e = tid; e < a.E; e += blockDim.x) atomicAdd(&s_rstart[s_rank[e]], 1);
+        for (int e = tid; e < a.E; e += blockDim.x) atomicAdd(&sm.rstart[sm.rank[e]], 1);
         __syncthreads();
-        block_exclusive_scan(s_rstart, a.R, s_warp);
-        if (tid == 0) s_rstart[a.R] = a.E;
+        block_exclusive_scan(sm.rstart, a.R, s_warp);
+        if (tid == 0) sm.rstart[a.R] = a.E;
         __syncthreads();
         if (warp == 0) {
             for (int c = 0; c < a.E; c += 32) {
                 const int e = c + lane;
-                const int r = e < a.E ? s_rank[e] : -1;
+                const int r = e < a.E ? sm.rank[e] : -1;
                 const unsigned same = __match_any_sync(kFull, r);
                 const int leader = __ffs(same) - 1;
                 int before = 0;
                 if (r >= 0 && lane == leader) {
-                    before = s_rfill[r];
-                    s_rfill[r] = before + __popc(same);
+                    before = sm.rfill[r];
+                    sm.rfill[r] = before + __popc(same);
                 }
                 before = __shfl_sync(kFull, before, leader);
-                if (r >= 0) s_order[s_rstart[r] + before + __popc(same & lanemask_lt())] = e;
+                if (r >= 0) sm.order[sm.rstart[r] + before + __popc(same & lanemask_lt())] = e;
                 __syncwarp();
             }
         }
     }
     __syncthreads();
-    for (int i = tid; i < a.E; i += blockDim.x) s_scan[i] = s_tot[s_order[i]];
+    for (int i = tid; i < a.E; i += blockDim.x) sm.scan[i] = sm.tot[sm.order[i]];
     __syncthreads();
-    const int total = block_exclusive_scan(s_scan, a.E, s_warp);
-
-    for (int i = tid; i < a.E; i += blockDim.x) s_base[s_order[i]] += s_scan[i];
+    const int total = block_exclusive_scan(sm.scan, a.E, s_warp);
+    for (int i = tid; i < a.E; i += blockDim.x) sm.base[sm.order[i]] += sm.scan[i];
     __syncthreads();
 
-    if (b == 0) {
+    if (b == a.wl.blocks) {
+        // The extra block: counts, offsets and statistics (the slot blocks
+        // write positions meanwhile).
         for (int i = tid; i < a.E; i += blockDim.x) {
-            const int e = s_order[i];
-            a.out.expert_count[e] = s_tot[e];
-            a.out.expert_offset[e] = s_scan[i];
+            const int e = sm.order[i];
+            a.out.expert_count[e] = sm.tot[e];
+            a.out.expert_offset[e] = sm.scan[i];
         }
-        int32_t* s_rcount = s_rfill;  // free again: rank counts for the statistics
         for (int r = tid; r < a.R; r += blockDim.x) {
-            const int lo = s_rstart[r] < a.E ? s_scan[s_rstart[r]] : total;
-            const int hi = s_rstart[r + 1] < a.E ? s_scan[s_rstart[r + 1]] : total;
+            const int lo = sm.rstart[r] < a.E ? sm.scan[sm.rstart[r]] : total;
+            const int hi = sm.rstart[r + 1] < a.E ? sm.scan[sm.rstart[r + 1]] : total;
             a.out.rank_offset[r] = lo;
             a.out.rank_count[r] = hi - lo;
-            s_rcount[r] = hi - lo;
+            sm.rfill[r] = hi - lo;  // free again: rank counts for the statistics
         }
         if (tid == 0) {
             a.out.expert_offset[a.E] = total;
@@ -595,17 +674,80 @@ layout_rank_kernel(const LayoutArgs a) {
             a.out.host_offset[a.H] = run;
         }
         __syncthreads();
-        write_stats(a, s_tot, s_rfill);
+        write_stats(a, sm.tot, sm.rfill);
+        return;
     }
 
-    for (int i = tid; i < nslots; i += blockDim.x) {
-        const int s = s0 + i;
-        const int e = clamp_id(a.ids[s], a.E);
-        const int w = i / spw;
-        const int p = s_base[e] + s_whist[w * a.E + e] + s_lrank[i];
+    for (int i = tid; i < sr.nslots; i += blockDim.x) {
+        const int s = sr.s0 + i;
+        const int e = clamp_id(sm.eid[i], a.E);
+        const int w = i / sr.spw;
+        const int p = sm.base[e] + sm.whist[w * a.E + e] + sm.lrank[i];
         a.out.pos[s] = p;
         if (p >= 0 && p < S) a.out.recv_src[p] = s;
     }
+}
+
+// ---- kernels ---------------------------------------------------------------
+
+template <int KMAX>
+__global__ void __launch_bounds__(kCountThreads) layout_count_kernel(const LayoutArgs a) {
+    extern __shared__ int32_t smem[];
+    pdl_launch_dependents();  // the rank kernel's prologue only reads ids
+    count_phase<KMAX, true>(a, carve_count(a, smem), blockIdx.x);
+}
+
+__global__ void __launch_bounds__(kRankThreads) layout_rank_kernel(const LayoutArgs a) {
+    extern __shared__ int32_t smem[];
+    pdl_launch_dependents();  // the next kernel waits for this one's results
+    const RankSmem sm = carve_rank(a, smem);
+    if (blockIdx.x < a.wl.blocks) rank_prologue(a, sm, blockIdx.x);
+    pdl_wait();  // from here on the count kernel's tables are needed
+    rank_finish(a, sm, blockIdx.x);
+}
+
+// Arrival at a grid-wide barrier whose counter starts at zero; every block of
+// a cooperative launch calls it once.  Gives up after limit_ns (returns false).
+__device__ bool grid_barrier(uint32_t* counter, uint64_t limit_ns) {
+    __shared__ int s_ok;
+    __threadfence();  // every thread's published counts before the arrival
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        atomicAdd(counter, 1u);
+        bool ok = true;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(counter) < gridDim.x) {
+            __nanosleep(32);
+            if (globaltimer_ns() - t0 > limit_ns) {
+                ok = false;
+                break;
+            }
+        }
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kRankThreads) layout_fused_kernel(const LayoutArgs a) {
+    extern __shared__ int32_t smem[];
+    const int b = blockIdx.x;
+    const RankSmem rsm = carve_rank(a, smem);
+    CountSmem csm = carve_count(a, smem + rank_smem_words(a.E, a.R, a.k));
+    if (b < a.wl.blocks) {
+        // The slot ranking also counts the block's experts: the count phase
+        // takes that histogram instead of counting again.
+        rank_prologue(a, rsm, b);
+        csm.hist = rsm.tot;
+        csm.eid = rsm.eid;
+        count_phase<KMAX, false>(a, csm, b);
+    }
+    if (!grid_barrier(reinterpret_cast<uint32_t*>(a.ws + a.wl.barrier), 1000000000ull)) {
+        if (threadIdx.x == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), MOE_STATUS_TIMEOUT);
+        return;
+    }
+    rank_finish(a, rsm, b);
 }
 
 // Layout with no tokens: counts and offsets are all zero.
@@ -634,39 +776,53 @@ __global__ void __launch_bounds__(256) stats_copy_kernel(const int64_t* rec, int
     for (int i = threadIdx.x; i < words; i += blockDim.x) out[i] = __ldcg(rec + i);
 }
 
-size_t count_smem_bytes(const LayoutArgs& a) {
-    return sizeof(int32_t) * (3 * (size_t)a.E + kHostSlots + (a.Rs + 1) + 4 * (size_t)a.Rs + 5 * (size_t)a.R);
-}
-
-size_t rank_smem_bytes(const LayoutArgs& a) {
-    return sizeof(int32_t) * ((size_t)(kRankWarps + 7) * a.E + 2 * kRankThreads + (2 * (size_t)a.R + 1) +
-                              (size_t)kLayoutTokensPerBlock * a.k);
-}
-
 template <typename K>
 cudaError_t allow_smem(K kernel, size_t bytes) {
     return ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), bytes);
 }
 
-}  // namespace
-
-cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
+template <int KMAX>
+cudaError_t launch_layout_k(const LayoutArgs& a, cudaStream_t stream) {
     cudaError_t err;
-    if (a.T == 0) {
-        layout_empty_kernel<<<1, 128, 0, stream>>>(a);
-        return cudaGetLastError();
+    const size_t smem_count = sizeof(int32_t) * count_smem_words(a.E, a.R, a.Rs);
+    const size_t smem_rank = sizeof(int32_t) * rank_smem_words(a.E, a.R, a.k);
+    // One cooperative kernel when every block of the grid can be resident.
+    auto fused = layout_fused_kernel<KMAX>;
+    const size_t smem_fused = smem_rank + smem_count;
+    if ((err = allow_smem(fused, smem_fused)) != cudaSuccess) return err;
+    const int per_sm = blocks_per_sm(reinterpret_cast<const void*>(fused), kRankThreads, smem_fused);
+    // Grids have one block more than slot blocks: it writes counts, offsets
+    // and statistics while the others write positions.
+    if (a.wl.blocks + 1 <= per_sm * device_sm_count()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.wl.blocks + 1);
+        cfg.blockDim = dim3(kRankThreads);
+        cfg.dynamicSmemBytes = smem_fused;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, fused, a);
     }
-    const size_t smem_count = count_smem_bytes(a);
-    const size_t smem_rank = rank_smem_bytes(a);
-    auto count = a.k <= 8 ? layout_count_kernel<8> : layout_count_kernel<32>;
+    auto count = layout_count_kernel<KMAX>;
     if ((err = allow_smem(count, smem_count)) != cudaSuccess) return err;
     if ((err = allow_smem(layout_rank_kernel, smem_rank)) != cudaSuccess) return err;
     count<<<a.wl.blocks, kCountThreads, smem_count, stream>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-
-    return launch_pdl(layout_rank_kernel, dim3(a.wl.blocks), dim3(kRankThreads), smem_rank, stream, a);
+    return launch_pdl(layout_rank_kernel, dim3(a.wl.blocks + 1), dim3(kRankThreads), smem_rank, stream, a);
 }
 
+}  // namespace
+
+cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
+    if (a.T == 0) {
+        layout_empty_kernel<<<1, 128, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
+    return a.k <= 8 ? launch_layout_k<8>(a, stream) : launch_layout_k<32>(a, stream);
+}
 
 cudaError_t launch_stats_copy(const uint8_t* ws, const WsLayout& wl, int64_t* out, cudaStream_t stream) {
     return launch_pdl(stats_copy_kernel, dim3(1), dim3(256), 0, stream,

@@ -51,8 +51,10 @@ typedef enum {
     MOE_ERR_CUDA = 2,      /* a CUDA launch or copy failed */
     MOE_ERR_BAD_IDS = 3,   /* an expert id out of [0, E) or repeated in a row */
     MOE_ERR_ALIGN = 4,     /* a row buffer is not 16-byte aligned */
-    MOE_ERR_CAPACITY = 5   /* the problem needs more scratch than
+    MOE_ERR_CAPACITY = 5,  /* the problem needs more scratch than
                               moe_layout_noalloc's fixed buffer holds */
+    MOE_ERR_TIMEOUT = 6    /* a bounded device wait gave up (see
+                              MOE_STATUS_TIMEOUT); outputs are incomplete */
 } moe_status_code;
 
 typedef enum {
@@ -65,6 +67,8 @@ typedef enum {
 #define MOE_STATUS_ID_REPEAT  0x2u   /* the same id twice in one token */
 #define MOE_STATUS_PLACEMENT  0x4u   /* expert_to_rank[e] outside [0, R) */
 #define MOE_STATUS_SRC_OFFSET 0x8u   /* src_rank_offsets not ascending 0..T */
+#define MOE_STATUS_TIMEOUT    0x10u  /* the layout's grid barrier waited more
+                                        than one second and gave up */
 
 /* Limits checked on the host. */
 #define MOE_MAX_TOPK     32
@@ -110,6 +114,9 @@ typedef struct moe_layout_t {
     uint8_t* host_mask;      /* [T, H] u8: 1 iff some slot of t goes to host H */
     int32_t* pos;            /* [T, k] receive row of slot (t, j) */
     int32_t* recv_src;       /* [T*k]  t*k + j of the slot held by each row */
+    int64_t* stats;          /* optional [moe_stats_words()] int64: when not
+                                NULL, moe_layout also writes the statistics
+                                record here (what moe_stats would copy out) */
 } moe_layout_t;
 
 /* Bytes of workspace needed for a problem ("Balancing and Beyond" section

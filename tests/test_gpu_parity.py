@@ -261,3 +261,30 @@ def test_round_trip_identity_experts(dev):
     # equal as values: an input of -0.0 sums to +0.0 from the +0.0 start of the
     # fma chain, while k * (-0.0) is -0.0
     assert torch.equal(case.out.float(), want.float())
+
+
+def test_layout_two_kernel_path_large_batch(dev, oracle_mod):
+    """T = 200000 tokens (1563 blocks) is more than one cooperative grid can
+    hold, so the layout runs as two kernels; results must not change."""
+    w = mw.Workload("big", T=200000, h=8, k=2, E=16, R=4, P=2, R_src=4, routing="zipf", zipf_s=0.8)
+    case = Case(w, dev, y_on_device=False)
+    rc, bits = case.run(dispatch=False, combine=False)
+    assert rc == 0 and bits == 0
+    prob, ref = _check_layout(oracle_mod, case)
+    _check_stats(oracle_mod, case, prob)
+
+
+def test_stats_delivered_with_the_layout(dev):
+    """moe_layout can write the statistics record itself (layout.stats); it
+    equals what moe_stats copies out of the workspace."""
+    import torch
+    import combine_moe_layout_04_gb300 as moe
+    w = mw.scaled(mw.WORKLOADS["decode-EP32-r8"], T=1024, R_src=8)
+    case = Case(w, dev, y_on_device=False)
+    lay = moe.Layout(case.prob, dev, with_stats=True)
+    lay.stats.fill_(-1)
+    moe.moe_layout(case.prob, case.ids_d, case.ws, lay)
+    moe.moe_stats(case.prob, lay, case.ws, case.stats)
+    torch.cuda.synchronize()
+    assert torch.equal(lay.stats, case.stats)
+    assert moe.moe_move_faults() == 0
