@@ -43,7 +43,7 @@ STATS_SRC = ("src_tokens", "src_copies", "src_mode0", "src_mode1", "src_mode2",
 STATS_DST = ("recv_slots", "recv_tokens", "recv_self", "recv_local", "recv_remote", "recv_relay")
 EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
             "moe_combine", "moe_status", "moe_status_string", "moe_layout_noalloc",
-            "moe_move_faults")
+            "moe_move_faults", "moe_selftest_bounded_waits")
 
 
 class MoeLibraryMissing(RuntimeError):
@@ -103,6 +103,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_layout_noalloc.restype = i
     lib.moe_move_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
     lib.moe_move_faults.restype = i
+    lib.moe_selftest_bounded_waits.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.moe_selftest_bounded_waits.restype = i
     lib.moe_status_string.argtypes = [i]
     lib.moe_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -247,6 +249,14 @@ def moe_move_faults(stream=None) -> int:
     """Synchronises the stream; returns and clears the row movers' fault bits."""
     bits = ctypes.c_uint32(0)
     _check(load_library().moe_move_faults(ctypes.byref(bits), _stream(stream)), "moe_move_faults")
+    return bits.value
+
+
+def moe_selftest_bounded_waits(stream=None) -> int:
+    """Runs the bounded-wait self-test; returns its bits (0xF = all good)."""
+    bits = ctypes.c_uint32(0)
+    _check(load_library().moe_selftest_bounded_waits(ctypes.byref(bits), _stream(stream)),
+           "moe_selftest_bounded_waits")
     return bits.value
 
 

@@ -170,6 +170,11 @@ int moe_move_faults(uint32_t* bits, moe_stream_t stream) {
     return cuda_status(moe::read_move_faults(bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_selftest_bounded_waits(uint32_t* bits, moe_stream_t stream) {
+    if (bits == nullptr) return MOE_ERR_INVALID;
+    return cuda_status(moe::run_wait_selftest(bits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* moe_status_string(int code) {
     switch (code) {
         case MOE_OK: return "ok";

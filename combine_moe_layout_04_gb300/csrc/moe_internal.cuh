@@ -173,6 +173,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Arrival at a grid-wide barrier whose counter starts at zero; every block of
+// a cooperative launch calls it once.  Gives up after limit_ns (returns false)
+// instead of spinning forever.
+__device__ __forceinline__ bool grid_barrier(uint32_t* counter, uint64_t limit_ns) {
+    __shared__ int s_ok;
+    __threadfence();  // every thread's published results before the arrival
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        atomicAdd(counter, 1u);
+        bool ok = true;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(counter) < gridDim.x) {
+            __nanosleep(32);
+            if (globaltimer_ns() - t0 > limit_ns) {
+                ok = false;
+                break;
+            }
+        }
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
 // Global -> shared bulk copy completing on a barrier (bytes: multiple of 16,
 // both addresses 16-byte aligned).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t bar) {
@@ -305,5 +329,6 @@ cudaError_t launch_dispatch(const MoveArgs& m, const void* x, const float* xs, v
 cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, void* out,
                            cudaStream_t s);
 cudaError_t read_move_faults(uint32_t* bits, cudaStream_t s);
+cudaError_t run_wait_selftest(uint32_t* bits, cudaStream_t s);
 
 }  // namespace moe

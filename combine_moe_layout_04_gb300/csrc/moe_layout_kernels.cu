@@ -706,29 +706,6 @@ __global__ void __launch_bounds__(kRankThreads) layout_rank_kernel(const LayoutA
     rank_finish(a, sm, blockIdx.x);
 }
 
-// Arrival at a grid-wide barrier whose counter starts at zero; every block of
-// a cooperative launch calls it once.  Gives up after limit_ns (returns false).
-__device__ bool grid_barrier(uint32_t* counter, uint64_t limit_ns) {
-    __shared__ int s_ok;
-    __threadfence();  // every thread's published counts before the arrival
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        atomicAdd(counter, 1u);
-        bool ok = true;
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(counter) < gridDim.x) {
-            __nanosleep(32);
-            if (globaltimer_ns() - t0 > limit_ns) {
-                ok = false;
-                break;
-            }
-        }
-        s_ok = ok;
-    }
-    __syncthreads();
-    return s_ok != 0;
-}
-
 template <int KMAX>
 __global__ void __launch_bounds__(kRankThreads) layout_fused_kernel(const LayoutArgs a) {
     extern __shared__ int32_t smem[];

@@ -250,6 +250,15 @@ int moe_layout_noalloc(const moe_problem* problem, const int32_t* ids,
 #define MOE_FAULT_WAIT_TIMEOUT 0x1u
 int moe_move_faults(uint32_t* bits, moe_stream_t stream);
 
+/* Self-test of the library's bounded device waits (the bulk-copy barrier
+ * waits of moe_dispatch / moe_combine and the grid barrier of moe_layout):
+ * runs them, with a 10 ms limit, on barriers that can never complete and on
+ * barriers that do, without faulting or hanging the GPU.  Allocates nothing;
+ * waits for the stream.  *bits receives 0xF when every wait behaved: bit 0 an
+ * mbarrier wait gave up, bit 1 an mbarrier wait succeeded, bit 2 a grid
+ * barrier wait gave up, bit 3 a grid barrier wait succeeded. */
+int moe_selftest_bounded_waits(uint32_t* bits, moe_stream_t stream);
+
 /* A short English description of a moe_status_code. */
 const char* moe_status_string(int code);
 
