@@ -19,6 +19,11 @@ arrays through ctypes.  Each wrapper names the passage it follows:
               dispatch_with_permute).
 * combine  -- gate-weighted sum of the k expert outputs in ascending slot order,
               fp32 fma, bf16 round-to-nearest-even (combine_with_unpermute).
+* quantize_dispatch -- bf16 -> fp8 e4m3 with an fp32 scale per 128 columns,
+              done inside dispatch ("Balancing and Beyond", section 3.1, where
+              the dispatch kernel converts to FP8 on its way and overlaps the
+              token-count reduction with it); e4m3 from the OCP 8-bit float
+              format.
 """
 from __future__ import annotations
 
@@ -87,6 +92,12 @@ def _load():
         lib.oracle_dispatch.restype = None
         lib.oracle_combine.argtypes = [ctypes.POINTER(Problem)] + [p] * 4
         lib.oracle_combine.restype = None
+        lib.oracle_quantize_dispatch.argtypes = [ctypes.POINTER(Problem)] + [p] * 4
+        lib.oracle_quantize_dispatch.restype = None
+        lib.oracle_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_e4m3_sat.restype = ctypes.c_uint8
+        lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_f32.restype = ctypes.c_float
         lib.oracle_f32_to_bf16_rne.argtypes = [ctypes.c_float]
         lib.oracle_f32_to_bf16_rne.restype = ctypes.c_uint16
         lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
@@ -185,6 +196,31 @@ def combine(prob: Problem, pos: np.ndarray, y: np.ndarray, w: np.ndarray) -> np.
     out = np.zeros((prob.T, prob.h), np.uint16)
     lib.oracle_combine(ctypes.byref(prob), _ptr(pos), _ptr(y), _ptr(w), _ptr(out))
     return out
+
+
+def quantize_dispatch(prob: Problem, pos: np.ndarray, x_bf16: np.ndarray):
+    """Per-group amax/448 scales and e4m3 codes of bf16 x, dispatched to
+    every receive row (quantise-in-dispatch).  Returns (codes, scales)."""
+    lib = _load()
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    S = prob.T * prob.k
+    codes = np.zeros((S, prob.h), np.uint8)
+    scales = np.zeros((S, prob.h // prob.scale_group), np.float32)
+    lib.oracle_quantize_dispatch(ctypes.byref(prob), _ptr(pos), _ptr(x), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def f32_to_e4m3(values) -> np.ndarray:
+    lib = _load()
+    v = np.asarray(values, np.float32).ravel()
+    return np.array([lib.oracle_f32_to_e4m3_sat(float(f)) for f in v], np.uint8)
+
+
+def e4m3_to_f32(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, np.uint8).ravel()
+    return np.array([lib.oracle_e4m3_to_f32(int(u)) for u in c], np.float32)
 
 
 def f32_to_bf16(values) -> np.ndarray:

@@ -298,6 +298,62 @@ void oracle_dispatch(const oracle_problem* p, const int32_t* pos,
         }
 }
 
+float oracle_e4m3_to_f32(uint8_t c) {
+    const int sign = (c >> 7) & 1;
+    const int exp = (c >> 3) & 0xF;
+    const int man = c & 0x7;
+    if (exp == 0xF && man == 0x7) return std::nanf("");
+    float mag;
+    if (exp == 0) mag = std::ldexp((float)man / 8.0f, 1 - 7);           // subnormal: 0.m x 2^-6
+    else mag = std::ldexp(1.0f + (float)man / 8.0f, exp - 7);            // normal: 1.m x 2^(e-7)
+    return sign ? -mag : mag;
+}
+
+uint8_t oracle_f32_to_e4m3_sat(float f) {
+    if (std::isnan(f)) return 0x7F;
+    const uint8_t sign = std::signbit(f) ? 0x80 : 0x00;
+    const double a = std::fabs((double)f);
+    // Every non-negative finite code in ascending order of value: codes 0x00
+    // .. 0x7E (0x7F is NaN).  Pick the nearest; on an exact tie the even code
+    // (lowest mantissa bit 0); beyond the largest (448) saturate.
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    double best_d = a;  // distance to code 0 (value 0)
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double v = (double)oracle_e4m3_to_f32((uint8_t)c);
+        const double d = std::fabs(v - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void oracle_quantize_dispatch(const oracle_problem* p, const int32_t* pos, const uint16_t* x_bf16,
+                              uint8_t* recv_codes, float* recv_scales) {
+    const size_t h = (size_t)p->h, g = (size_t)p->scale_group, G = h / g;
+    std::vector<uint8_t> codes(h);
+    std::vector<float> scales(G);
+    for (int t = 0; t < p->T; ++t) {
+        const uint16_t* row = x_bf16 + (size_t)t * h;
+        for (size_t grp = 0; grp < G; ++grp) {
+            float amax = 0.0f;
+            for (size_t c = grp * g; c < (grp + 1) * g; ++c)
+                amax = std::max(amax, std::fabs(oracle_bf16_to_f32(row[c])));
+            const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[grp] = scale;
+            for (size_t c = grp * g; c < (grp + 1) * g; ++c)
+                codes[c] = oracle_f32_to_e4m3_sat(oracle_bf16_to_f32(row[c]) / scale);
+        }
+        for (int j = 0; j < p->k; ++j) {
+            const size_t dst = (size_t)pos[(size_t)t * p->k + j];
+            std::memcpy(recv_codes + dst * h, codes.data(), h);
+            std::memcpy(recv_scales + dst * G, scales.data(), G * sizeof(float));
+        }
+    }
+}
+
 void oracle_combine(const oracle_problem* p, const int32_t* pos,
                     const uint16_t* y, const float* w, uint16_t* out) {
     const size_t h = (size_t)p->h;

@@ -104,6 +104,21 @@ void oracle_dispatch(const oracle_problem* p, const int32_t* pos,
 void oracle_combine(const oracle_problem* p, const int32_t* pos,
                     const uint16_t* y, const float* w, uint16_t* out);
 
+/* Quantise-in-dispatch: for every token row of bf16 x and every group of
+ * scale_group columns, scale = amax / 448 (fp32 division; 1 when the group is
+ * all zeros) and codes = e4m3(x / scale) (fp32 division, round to nearest
+ * even, saturating at +-448); the codes and scales of token t are written to
+ * every receive row pos[t*k+j], like oracle_dispatch. */
+void oracle_quantize_dispatch(const oracle_problem* p, const int32_t* pos, const uint16_t* x_bf16,
+                              uint8_t* recv_codes, float* recv_scales);
+
+/* FP8 E4M3 (OCP 8-bit floating point, E4M3: bias 7, 3 mantissa bits, no
+ * infinities, S.1111.111 is NaN, largest finite 448) written from the format
+ * definition: round to nearest even, saturating to +-448 for finite inputs
+ * beyond it; NaN maps to 0x7F. */
+uint8_t oracle_f32_to_e4m3_sat(float f);
+float oracle_e4m3_to_f32(uint8_t c);
+
 /* bf16 helpers written from the bfloat16 format (the upper 16 bits of an
  * IEEE-754 binary32) and IEEE round-to-nearest-even; exported so the tests
  * can pin them against a library conversion. */

@@ -333,3 +333,76 @@ def test_combine_sums_in_ascending_slot_order(oracle_mod):
     assert np.all(out == 0)
     out_rev = oracle_mod.combine(prob, np.array([[0, 2, 1]], np.int32), y, np.ones((1, 3), np.float32))
     assert np.all(mw.bf16_bits_to_f32(out_rev) == 1.0)
+
+
+# ------------------------------------------------------- fp8 e4m3 quantisation
+
+def _torch_e4m3_values():
+    import torch
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).float().numpy()
+
+
+def test_e4m3_decode_matches_library(oracle_mod):
+    """All 256 e4m3 codes decode as the library's float8_e4m3fn does (0x7F and
+    0xFF are NaN; 0x7E is 448)."""
+    want = _torch_e4m3_values()
+    got = oracle_mod.e4m3_to_f32(np.arange(256))
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and set(np.nonzero(nan)[0]) == {0x7F, 0xFF}
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0
+
+
+def test_e4m3_encode_round_trip_ties_and_saturation(oracle_mod):
+    vals = _torch_e4m3_values()
+    finite = [c for c in range(256) if not np.isnan(vals[c])]
+    enc = oracle_mod.f32_to_e4m3(vals[finite])
+    # -0.0 encodes to 0x80, +0.0 to 0x00: every finite code round-trips
+    assert np.array_equal(enc, np.array(finite, np.uint8))
+    # ties between neighbours go to the even code; compare with the library
+    import torch
+    pos = np.sort(vals[[c for c in range(0x7F) if not np.isnan(vals[c])]])
+    mids = ((pos[1:].astype(np.float64) + pos[:-1]) / 2).astype(np.float32)
+    got = oracle_mod.f32_to_e4m3(np.concatenate([mids, -mids]))
+    want = torch.from_numpy(np.concatenate([mids, -mids])).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want)
+    assert np.all(got[: len(mids)] % 2 == 0)
+    # beyond the largest finite value: saturate to +-448
+    big = np.array([448.0001, 464.0, 480.0, 1e6, 3.4e38], np.float32)
+    assert np.all(oracle_mod.f32_to_e4m3(big) == 0x7E)
+    assert np.all(oracle_mod.f32_to_e4m3(-big) == 0xFE)
+
+
+def test_e4m3_encode_matches_library_rne(oracle_mod):
+    import torch
+    rng = np.random.default_rng(2)
+    v = np.concatenate([rng.uniform(-448, 448, 3000), rng.standard_normal(3000) * 2.0 ** -7,
+                        rng.standard_normal(2000)]).astype(np.float32)
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle_mod.f32_to_e4m3(v), want)
+
+
+def test_quantize_dispatch_bounds_and_rows(oracle_mod):
+    """Per 128-column group: the element of largest magnitude maps to +-448;
+    every element dequantises within half an e4m3 ulp (relative 2^-4, or
+    2^-10 x scale in the subnormal range); each receive row holds its token's
+    quantised row."""
+    w = mw.Workload("q", T=48, h=512, k=4, E=16, R=4, P=2, R_src=1)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, elem_bytes=1)
+    lay = oracle_mod.layout(prob, ids)
+    x = mw.gen_x_bf16(w)
+    codes, scales = oracle_mod.quantize_dispatch(prob, lay["pos"], x)
+    src = lay["recv_src"] // w.k
+    xf = mw.bf16_bits_to_f32(x).reshape(w.T, -1, 128)
+    amax = np.abs(xf).max(axis=2)
+    assert np.array_equal(scales[lay["pos"][:, 0]], (amax / np.float32(448.0)).astype(np.float32))
+    dq = oracle_mod.e4m3_to_f32(codes[lay["pos"][:, 0]]).reshape(w.T, -1, 128)
+    scale = scales[lay["pos"][:, 0]][:, :, None]
+    err = np.abs(dq.astype(np.float64) * scale - xf)
+    assert np.all(err <= np.maximum(2.0 ** -4 * np.abs(xf), 2.0 ** -10 * scale) * (1 + 1e-6))
+    top = np.abs(xf).argmax(axis=2)
+    assert np.all(np.abs(np.take_along_axis(dq, top[:, :, None], axis=2)) == 448.0)
+    assert np.array_equal(codes, codes[lay["pos"][:, 0]][src])
+    assert np.array_equal(scales, scales[lay["pos"][:, 0]][src])
