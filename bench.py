@@ -41,7 +41,8 @@ def algorithmic_bytes(w, tokens=None):
     combine reads k bf16 rows and writes one."""
     T = w.T if tokens is None else tokens
     rho = w.h + 4 * (w.h // w.scale_group) if w.dtype == "fp8" else 2 * w.h
-    dispatch = T * rho * (1 + w.k)
+    # quantise-in-dispatch reads bf16 rows and writes k fp8 rows + scales
+    dispatch = T * (2 * w.h + w.k * rho) if w.quantize else T * rho * (1 + w.k)
     combine = T * w.k * 2 * w.h + T * 2 * w.h
     return dispatch, combine
 
@@ -172,7 +173,9 @@ def oracle_pass(w, tokens, ids, gates, xin, y):
     prob, keep = oracle.make_problem(tokens, w.h, w.k, w.E, w.R, w.P, 1, eb, w.scale_group)
     lay = oracle.layout(prob, ids[:tokens])
     oracle.stats(prob, ids[:tokens])
-    if w.dtype == "fp8":
+    if w.quantize:
+        oracle.quantize_dispatch(prob, lay["pos"], xin[:tokens])
+    elif w.dtype == "fp8":
         oracle.dispatch(prob, lay["pos"], xin[0][:tokens], xin[1][:tokens])
     else:
         oracle.dispatch(prob, lay["pos"], xin[:tokens])
@@ -183,7 +186,7 @@ def oracle_inputs(w, tokens):
     import moe_workloads as mw
     ids = mw.gen_ids(w)
     gates = mw.gen_gates(w)
-    xin = mw.gen_x_fp8(w, rows=tokens) if w.dtype == "fp8" else mw.gen_x_bf16(w, rows=tokens)
+    xin = mw.gen_x_fp8(w, rows=tokens) if (w.dtype == "fp8" and not w.quantize) else mw.gen_x_bf16(w, rows=tokens)
     y = mw.gen_y_host(w, rows=tokens * w.k)
     return ids, gates, xin, y
 
@@ -246,7 +249,8 @@ def run_reference(args, w):
 def workload_config(w):
     return {"workload": w.name, "T": w.T, "hidden": w.h, "topk": w.k, "experts": w.E, "ranks": w.R,
             "hosts": w.H, "src_ranks": w.R_src,
-            "x": "fp8 e4m3 + fp32 scale per 128 columns" if w.dtype == "fp8" else "bf16",
+            "x": ("bf16, quantised to fp8 e4m3 + fp32 scale per 128 columns inside dispatch" if w.quantize
+                  else "fp8 e4m3 + fp32 scale per 128 columns" if w.dtype == "fp8" else "bf16"),
             "y_out": "bf16", "routing": w.routing + (f" s={w.zipf_s}" if w.routing == "zipf" else ""),
             "l2": "inputs larger than L2: each step streams >1 GB (y, recv) through the 129 MB L2, "
                   "which evicts the previous step's x"}
@@ -276,7 +280,12 @@ def run_ours(args, w):
     stats = lay.stats
     ids_d = torch.from_numpy(ids).to(dev)
     gates_d = torch.from_numpy(gates).to(dev)
-    if fp8:
+    if fp8 and w.quantize:
+        x_d = torch.from_numpy(mw.gen_x_bf16(w).view(np.int16)).to(dev).view(torch.bfloat16)
+        xs_d = None
+        recv = torch.empty((w.slots, w.h), dtype=torch.uint8, device=dev)
+        recv_s = torch.empty((w.slots, w.h // w.scale_group), dtype=torch.float32, device=dev)
+    elif fp8:
         xq, xs = mw.gen_x_fp8(w)
         x_d, xs_d = torch.from_numpy(xq).to(dev), torch.from_numpy(xs).to(dev)
         recv = torch.empty((w.slots, w.h), dtype=torch.uint8, device=dev)
@@ -298,7 +307,10 @@ def run_ours(args, w):
         moe.moe_layout(prob, ids_d, ws, lay, stream)
         if ev is not None:
             ev[0].record(stream)
-        moe.moe_dispatch(prob, lay, x_d, xs_d, recv, recv_s, stream)
+        if w.quantize:
+            moe.moe_dispatch_quant(prob, lay, x_d, recv, recv_s, stream)
+        else:
+            moe.moe_dispatch(prob, lay, x_d, xs_d, recv, recv_s, stream)
         if ev is not None:
             ev[1].record(stream)
         moe.moe_combine(prob, lay, y_d, gates_d, out, stream)
@@ -360,7 +372,7 @@ def run_ours(args, w):
     h_ids = torch.from_numpy(ids).pin_memory()
     h_gates = torch.from_numpy(gates).pin_memory()
     h_x = x_d.cpu().pin_memory()
-    h_xs = xs_d.cpu().pin_memory() if fp8 else None
+    h_xs = xs_d.cpu().pin_memory() if xs_d is not None else None
     h_y = y_d.cpu().pin_memory() if fp8 else None
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_stats = torch.empty(stats.shape, dtype=stats.dtype).pin_memory()
@@ -371,8 +383,9 @@ def run_ours(args, w):
         ids_d.copy_(h_ids, non_blocking=True)
         gates_d.copy_(h_gates, non_blocking=True)
         x_d.copy_(h_x, non_blocking=True)
-        if fp8:
+        if h_xs is not None:
             xs_d.copy_(h_xs, non_blocking=True)
+        if h_y is not None:
             y_d.copy_(h_y, non_blocking=True)
         step()
         h_out.copy_(out, non_blocking=True)

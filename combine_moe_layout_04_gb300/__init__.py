@@ -43,7 +43,7 @@ STATS_SRC = ("src_tokens", "src_copies", "src_mode0", "src_mode1", "src_mode2",
 STATS_DST = ("recv_slots", "recv_tokens", "recv_self", "recv_local", "recv_remote", "recv_relay")
 EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
             "moe_combine", "moe_status", "moe_status_string", "moe_layout_noalloc",
-            "moe_move_faults", "moe_selftest_bounded_waits")
+            "moe_move_faults", "moe_selftest_bounded_waits", "moe_dispatch_quant")
 
 
 class MoeLibraryMissing(RuntimeError):
@@ -95,6 +95,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_stats.restype = i
     lib.moe_dispatch.argtypes = [P, L, vp, vp, vp, vp, vp]
     lib.moe_dispatch.restype = i
+    lib.moe_dispatch_quant.argtypes = [P, L, vp, vp, vp, vp]
+    lib.moe_dispatch_quant.restype = i
     lib.moe_combine.argtypes = [P, L, vp, vp, vp, vp]
     lib.moe_combine.restype = i
     lib.moe_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
@@ -231,6 +233,13 @@ def moe_dispatch(problem: Problem, layout: Layout, x, x_scales, recv, recv_scale
     _check(load_library().moe_dispatch(ctypes.byref(problem.c()), ctypes.byref(layout.c()), _ptr(x),
                                        _ptr(x_scales), _ptr(recv), _ptr(recv_scales), _stream(stream)),
            "moe_dispatch")
+
+
+def moe_dispatch_quant(problem: Problem, layout: Layout, x_bf16, recv, recv_scales, stream=None):
+    """Dispatch that converts bf16 rows to e4m3 codes + fp32 scales per 128 columns."""
+    _check(load_library().moe_dispatch_quant(ctypes.byref(problem.c()), ctypes.byref(layout.c()),
+                                             _ptr(x_bf16), _ptr(recv), _ptr(recv_scales), _stream(stream)),
+           "moe_dispatch_quant")
 
 
 def moe_combine(problem: Problem, layout: Layout, y, weights, out, stream=None):

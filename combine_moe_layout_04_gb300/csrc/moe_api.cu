@@ -132,6 +132,25 @@ int moe_dispatch(const moe_problem* problem, const moe_layout_t* layout, const v
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_dispatch_quant(const moe_problem* problem, const moe_layout_t* layout, const void* x_bf16,
+                       void* recv, float* recv_scales, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (!d.fp8 || layout == nullptr) return MOE_ERR_INVALID;
+    if (d.T == 0) return MOE_OK;
+    if (layout->pos == nullptr || x_bf16 == nullptr || recv == nullptr || recv_scales == nullptr)
+        return MOE_ERR_INVALID;
+    if (!aligned(x_bf16, 16) || !aligned(recv, 16) || !aligned(recv_scales, 4) || !aligned(layout->pos, 4))
+        return MOE_ERR_ALIGN;
+    moe::MoveArgs m{};
+    m.pos = layout->pos;
+    m.T = d.T;
+    m.k = d.k;
+    return cuda_status(moe::launch_dispatch_quant(m, x_bf16, recv, recv_scales, d.h,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_combine(const moe_problem* problem, const moe_layout_t* layout, const void* y,
                 const float* weights, void* out, moe_stream_t stream) {
     Dims d;

@@ -328,6 +328,8 @@ cudaError_t launch_dispatch(const MoveArgs& m, const void* x, const float* xs, v
                             float* rs, int groups, cudaStream_t s);
 cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, void* out,
                            cudaStream_t s);
+cudaError_t launch_dispatch_quant(const MoveArgs& m, const void* x, void* recv, float* rs, int h,
+                                  cudaStream_t s);
 cudaError_t read_move_faults(uint32_t* bits, cudaStream_t s);
 cudaError_t run_wait_selftest(uint32_t* bits, cudaStream_t s);
 

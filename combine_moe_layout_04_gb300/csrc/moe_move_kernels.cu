@@ -22,6 +22,7 @@
 // or contributes nothing (combine), so a bad layout cannot write out of bounds.
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "moe_internal.cuh"
@@ -150,6 +151,74 @@ combine_kernel(const MoveArgs m, const uint4* __restrict__ y, const float* __res
 #pragma unroll
         for (int i = 0; i < U; ++i)
             if (v0 + 32 * i < vend) st_v4(orow + v0 + 32 * i, pack_bf16x8(acc[i]));
+    }
+}
+
+// ---- quantise-in-dispatch ----------------------------------------------------
+
+// bf16 rows in, e4m3 rows + fp32 scales out, one scale per 128 columns: the
+// dispatch kernel converts to FP8 on its way ("Balancing and Beyond", section
+// 3.1).  A warp takes one (token, 512-column chunk) unit: lane L holds
+// columns 16L .. 16L+15, so lanes 8g .. 8g+7 share scale group g.  Per group:
+// scale = amax / 448 (1 for an all-zero group), code = e4m3(x / scale) with
+// round-to-nearest-even and saturation; the 16 codes of a lane go to every
+// receive row of the token as one 16-byte store.
+__global__ void __launch_bounds__(kMoveThreads)
+dispatch_quant_kernel(const MoveArgs m, const uint4* __restrict__ x, uint8_t* __restrict__ recv,
+                      float* __restrict__ rs, int h) {
+    const int lane = threadIdx.x & 31;
+    const int gwarp = blockIdx.x * kMoveWarps + (threadIdx.x >> 5);
+    const int nwarps = gridDim.x * kMoveWarps;
+    const int S = m.T * m.k;
+    const int groups = h / 128;
+    const long long units = (long long)m.T * m.nchunks;
+    for (long long u = gwarp; u < units; u += nwarps) {
+        const int t = (int)(u / m.nchunks);
+        const int c = (int)(u - (long long)t * m.nchunks);
+        int p = -1;
+        if (lane < m.k) {
+            p = m.pos[(size_t)t * m.k + lane];
+            if (p < 0 || p >= S) p = -1;
+        }
+        const int col = c * 512 + lane * 16;  // first of this lane's 16 columns
+        const bool active = col < h;          // h % 128 == 0: groups are whole
+        uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+        if (active) {
+            const uint4* src = x + ((size_t)t * h + col) / 8;
+            v0 = ld_stream_v4(src);
+            v1 = ld_stream_v4(src + 1);
+        }
+        float f[16];
+        const uint32_t q[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            f[2 * i] = __uint_as_float(q[i] << 16);
+            f[2 * i + 1] = __uint_as_float(q[i] & 0xffff0000u);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        uint32_t packed[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_fp8x2_storage_t lo =
+                __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i] / scale, f[4 * i + 1] / scale), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi =
+                __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2] / scale, f[4 * i + 3] / scale), __NV_SATFINITE,
+                                         __NV_E4M3);
+            packed[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
+        const uint4 codes = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        const int group = col / 128;
+        for (int j = 0; j < m.k; ++j) {
+            const int pj = __shfl_sync(0xffffffffu, p, j);
+            if (pj < 0 || !active) continue;
+            st_v4(reinterpret_cast<uint4*>(recv + (size_t)pj * h + col), codes);
+            if ((lane & 7) == 0) rs[(size_t)pj * groups + group] = scale;
+        }
     }
 }
 
@@ -502,6 +571,18 @@ cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, voi
                            cudaStream_t stream) {
     if (m.k <= 8) return launch_combine_bulk<kCombWarps, kCombStages, kCombChunk, kCombCtasPerSm>(m, y, w, out, stream);
     return launch_combine_lsu(m, y, w, out, stream);
+}
+
+cudaError_t launch_dispatch_quant(const MoveArgs& m0, const void* x, void* recv, float* rs, int h,
+                                  cudaStream_t stream) {
+    MoveArgs m = m0;
+    m.nchunks = (h + 511) / 512;
+    const long long units = (long long)m.T * m.nchunks;
+    if (units == 0) return cudaSuccess;
+    auto kern = dispatch_quant_kernel;
+    kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(m, static_cast<const uint4*>(x),
+                                                              static_cast<uint8_t*>(recv), rs, h);
+    return cudaGetLastError();
 }
 
 cudaError_t read_move_faults(uint32_t* bits, cudaStream_t stream) {

@@ -201,6 +201,20 @@ int moe_dispatch(const moe_problem* problem, const moe_layout_t* layout,
                  const void* x, const float* x_scales,
                  void* recv, float* recv_scales, moe_stream_t stream);
 
+/* Quantise-in-dispatch: dispatch of bf16 rows that converts them to FP8 on
+ * the way ("Balancing and Beyond", section 3.1: the dispatch kernel does the
+ * BF16-to-FP8 conversion).  For every token t and every group of 128 columns:
+ *   scale = amax / 448 over the group's |x| (fp32 division; 1 when all zero),
+ *   code  = e4m3(x / scale) (fp32 division, round to nearest even, saturated
+ *           at +-448; OCP 8-bit floating point E4M3),
+ * and recv[pos[t, j]] = codes, recv_scales[pos[t, j]] = scales for every j.
+ *   problem->dtype must be MOE_DTYPE_FP8_E4M3 (h % 128 == 0);
+ *   x_bf16: [T, h] bf16; recv: [T*k, h] e4m3 bytes; recv_scales: fp32
+ *   [T*k, h/128].  x_bf16 and recv 16-byte aligned, recv_scales 4-byte.
+ * Only pos is read from the layout. */
+int moe_dispatch_quant(const moe_problem* problem, const moe_layout_t* layout,
+                       const void* x_bf16, void* recv, float* recv_scales, moe_stream_t stream);
+
 /* Combine-unpermute: out[t] = bf16_rne(sum over j = 0..k-1, in ascending j,
  * of w[t, j] * y[pos[t, j]]) with one fp32 fma per term starting from 0.0f.
  *   y: bf16 [T*k, h] expert outputs in receive order; weights: fp32 [T, k];

@@ -61,6 +61,7 @@ class Workload:
     seed: int = 0
     steps: int = 1           # >1: routing re-drawn per step (per-step s table)
     scale_group: int = 128
+    quantize: bool = False   # fp8 receive rows made from bf16 x inside dispatch
 
     @property
     def H(self) -> int:
@@ -97,6 +98,9 @@ WORKLOADS = {
     # columns, Zipf(s=1.0) skew.
     "prefill-fp8": Workload("prefill-fp8", T=16384, h=7168, k=8, E=128, R=16, P=8, R_src=1,
                             dtype="fp8", routing="zipf", zipf_s=1.0),
+    # As prefill-fp8, but x arrives in bf16 and dispatch quantises it.
+    "prefill-fp8-quant": Workload("prefill-fp8-quant", T=16384, h=7168, k=8, E=128, R=16, P=8, R_src=1,
+                                  dtype="fp8", routing="zipf", zipf_s=1.0, quantize=True),
 }
 
 
