@@ -19,6 +19,10 @@ arrays through ctypes.  Each wrapper names the passage it follows:
               dispatch_with_permute).
 * combine  -- gate-weighted sum of the k expert outputs in ascending slot order,
               fp32 fma, bf16 round-to-nearest-even (combine_with_unpermute).
+* swap_plan -- per-step intra-host expert swap ("Balancing and Beyond",
+              section 3.1, Figure 2(b)): heaviest rank paired with lightest,
+              one best exchange per pair, accepted if the pair's maximum falls
+              by at least tau.
 * quantize_dispatch -- bf16 -> fp8 e4m3 with an fp32 scale per 128 columns,
               done inside dispatch ("Balancing and Beyond", section 3.1, where
               the dispatch kernel converts to FP8 on its way and overlaps the
@@ -92,6 +96,8 @@ def _load():
         lib.oracle_dispatch.restype = None
         lib.oracle_combine.argtypes = [ctypes.POINTER(Problem)] + [p] * 4
         lib.oracle_combine.restype = None
+        lib.oracle_swap_plan.argtypes = [ctypes.POINTER(Problem), p, ctypes.c_int32, p, p]
+        lib.oracle_swap_plan.restype = ctypes.c_int
         lib.oracle_quantize_dispatch.argtypes = [ctypes.POINTER(Problem)] + [p] * 4
         lib.oracle_quantize_dispatch.restype = None
         lib.oracle_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
@@ -196,6 +202,20 @@ def combine(prob: Problem, pos: np.ndarray, y: np.ndarray, w: np.ndarray) -> np.
     out = np.zeros((prob.T, prob.h), np.uint16)
     lib.oracle_combine(ctypes.byref(prob), _ptr(pos), _ptr(y), _ptr(w), _ptr(out))
     return out
+
+
+def swap_plan(prob: Problem, expert_count: np.ndarray, tau: int):
+    """Per-step intra-host expert swap.  Returns (new_expert_to_rank [E],
+    swaps [H, P//2, 6] = rank a, rank b, x, y, old max, new max)."""
+    lib = _load()
+    cnt = np.ascontiguousarray(expert_count, dtype=np.int32)
+    H = prob.R // prob.P
+    new_e2r = np.zeros(prob.E, np.int32)
+    swaps = np.zeros((H, prob.P // 2, 6), np.int32)
+    rc = lib.oracle_swap_plan(ctypes.byref(prob), _ptr(cnt), int(tau), _ptr(new_e2r), _ptr(swaps))
+    if rc != OK:
+        raise OracleError(rc)
+    return new_e2r, swaps
 
 
 def quantize_dispatch(prob: Problem, pos: np.ndarray, x_bf16: np.ndarray):

@@ -298,6 +298,48 @@ void oracle_dispatch(const oracle_problem* p, const int32_t* pos,
         }
 }
 
+int oracle_swap_plan(const oracle_problem* p, const int32_t* expert_count, int32_t tau,
+                     int32_t* new_expert_to_rank, int32_t* swaps) {
+    Placement pl;
+    if (!make_placement(p, &pl)) return ORACLE_ERR_INVALID;
+    const int P = pl.P, H = pl.H, pairs = P / 2;
+    std::vector<int64_t> load(p->R, 0);
+    for (int e = 0; e < p->E; ++e) load[pl.rank_of_expert[e]] += expert_count[e];
+    for (int e = 0; e < p->E; ++e) new_expert_to_rank[e] = pl.rank_of_expert[e];
+    const int64_t need = std::max<int64_t>(tau, 1);
+    for (int hh = 0; hh < H; ++hh) {
+        // Ranks of the host, heaviest first (ties by rank index).
+        std::vector<int> ranks(P);
+        for (int i = 0; i < P; ++i) ranks[i] = hh * P + i;
+        std::stable_sort(ranks.begin(), ranks.end(), [&](int x, int y) { return load[x] > load[y]; });
+        for (int i = 0; i < pairs; ++i) {
+            const int a = ranks[i], b = ranks[P - 1 - i];
+            const int64_t old_max = std::max(load[a], load[b]);
+            int64_t best = -1;
+            int bx = -1, by = -1;
+            for (int x = 0; x < p->E; ++x) {
+                if (pl.rank_of_expert[x] != a) continue;
+                for (int y = 0; y < p->E; ++y) {
+                    if (pl.rank_of_expert[y] != b) continue;
+                    const int64_t la = load[a] - expert_count[x] + expert_count[y];
+                    const int64_t lb = load[b] - expert_count[y] + expert_count[x];
+                    const int64_t m = std::max(la, lb);
+                    if (best < 0 || m < best) { best = m; bx = x; by = y; }
+                }
+            }
+            int32_t* rec = swaps + ((size_t)hh * pairs + i) * 6;
+            rec[0] = a; rec[1] = b; rec[2] = bx; rec[3] = by;
+            rec[4] = (int32_t)old_max;
+            rec[5] = (int32_t)(best < 0 ? old_max : best);
+            if (bx >= 0 && old_max - best >= need) {
+                new_expert_to_rank[bx] = b;
+                new_expert_to_rank[by] = a;
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 float oracle_e4m3_to_f32(uint8_t c) {
     const int sign = (c >> 7) & 1;
     const int exp = (c >> 3) & 0xF;

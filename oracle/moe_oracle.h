@@ -104,6 +104,22 @@ void oracle_dispatch(const oracle_problem* p, const int32_t* pos,
 void oracle_combine(const oracle_problem* p, const int32_t* pos,
                     const uint16_t* y, const float* w, uint16_t* out);
 
+/* Per-step intra-host expert swap ("Balancing and Beyond", section 3.1 and
+ * its Figure 2(b)).  Load of rank r: L_r = sum of expert_count over its
+ * experts.  In every host the ranks are ordered by load (descending, ties by
+ * rank index) and the i-th heaviest is paired with the i-th lightest.  For a
+ * pair (a, b) every exchange of one expert x of a with one expert y of b gives
+ * max(L_a - c_x + c_y, L_b - c_y + c_x); the exchange with the smallest such
+ * maximum is taken (ties: smallest x, then smallest y) and accepted when it
+ * lowers the pair's maximum max(L_a, L_b) by at least max(tau, 1) tokens.
+ * Outputs: new_expert_to_rank[E] (the placement after the accepted swaps) and
+ * swaps[H * (P/2) * 6] = for each host and pair: rank a, rank b, x, y (-1 when
+ * a rank has no expert), old max, new max; accepted pairs are those whose
+ * x is moved in new_expert_to_rank.  Returns ORACLE_ERR_INVALID for a bad
+ * problem. */
+int oracle_swap_plan(const oracle_problem* p, const int32_t* expert_count, int32_t tau,
+                     int32_t* new_expert_to_rank, int32_t* swaps);
+
 /* Quantise-in-dispatch: for every token row of bf16 x and every group of
  * scale_group columns, scale = amax / 448 (fp32 division; 1 when the group is
  * all zeros) and codes = e4m3(x / scale) (fp32 division, round to nearest

@@ -406,3 +406,59 @@ def test_quantize_dispatch_bounds_and_rows(oracle_mod):
     assert np.all(np.abs(np.take_along_axis(dq, top[:, :, None], axis=2)) == 448.0)
     assert np.array_equal(codes, codes[lay["pos"][:, 0]][src])
     assert np.array_equal(scales, scales[lay["pos"][:, 0]][src])
+
+
+# ------------------------------------------------ per-step intra-host expert swap
+
+def test_swap_plan_worked_example(oracle_mod):
+    """"Balancing and Beyond", Figure 2(b): G0 holds e0 (60 tokens) and 100
+    more, G1 holds e1 (30) and 70 more; swapping e0 and e1 turns 160 / 100 into
+    130 / 130.  The swap is taken when tau <= 30 and refused when tau = 31."""
+    # G0 = rank 0: e0 = 60, e2 = 50, e4 = 50;  G1 = rank 1: e1 = 30, e3 = 35, e5 = 35
+    e2r = np.array([0, 1, 0, 1, 0, 1], np.int32)
+    cnt = np.array([60, 30, 50, 35, 50, 35], np.int32)
+    prob, keep = _prob(oracle_mod, 1, 6, 2, 2, 1, e2r=e2r)
+    new, swaps = oracle_mod.swap_plan(prob, cnt, 30)
+    a, b, x, y, old, best = swaps[0, 0]
+    assert (a, b, x, y, old, best) == (0, 1, 0, 1, 160, 130)
+    assert list(new) == [1, 0, 0, 1, 0, 1]
+    loads = np.bincount(new, weights=cnt, minlength=2)
+    assert list(loads) == [130, 130]
+    new31, _ = oracle_mod.swap_plan(prob, cnt, 31)
+    assert np.array_equal(new31, e2r)
+
+
+def test_swap_plan_is_the_best_single_exchange(oracle_mod):
+    """Brute force on small random hosts: the chosen exchange attains the
+    smallest pair maximum, pairs are heaviest-with-lightest, and only accepted
+    pairs move experts."""
+    rng = np.random.default_rng(4)
+    for trial in range(40):
+        P = int(rng.choice([2, 3, 4, 6]))
+        H = int(rng.integers(1, 4))
+        R = P * H
+        per = int(rng.integers(1, 4))
+        E = R * per
+        e2r = rng.permutation(np.repeat(np.arange(R), per)).astype(np.int32)
+        cnt = rng.integers(0, 200, E).astype(np.int32)
+        tau = int(rng.integers(0, 40))
+        prob, keep = _prob(oracle_mod, 1, E, R, P, 1, e2r=e2r)
+        new, swaps = oracle_mod.swap_plan(prob, cnt, tau)
+        load = np.bincount(e2r, weights=cnt, minlength=R).astype(np.int64)
+        moved = set()
+        for hh in range(H):
+            order = sorted(range(hh * P, (hh + 1) * P), key=lambda r: (-load[r], r))
+            for i in range(P // 2):
+                a, b, x, y, old, best = swaps[hh, i]
+                assert (a, b) == (order[i], order[P - 1 - i])
+                assert old == max(load[a], load[b])
+                cands = [(max(load[a] - cnt[xx] + cnt[yy], load[b] - cnt[yy] + cnt[xx]), xx, yy)
+                         for xx in np.nonzero(e2r == a)[0] for yy in np.nonzero(e2r == b)[0]]
+                m, bx, by = min(cands)
+                assert (best, x, y) == (m, bx, by)
+                if old - best >= max(tau, 1):
+                    assert new[x] == b and new[y] == a
+                    moved |= {x, y}
+        for e in range(E):
+            if e not in moved:
+                assert new[e] == e2r[e]
