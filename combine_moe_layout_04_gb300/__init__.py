@@ -43,7 +43,7 @@ STATS_SRC = ("src_tokens", "src_copies", "src_mode0", "src_mode1", "src_mode2",
 STATS_DST = ("recv_slots", "recv_tokens", "recv_self", "recv_local", "recv_remote", "recv_relay")
 EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
             "moe_combine", "moe_status", "moe_status_string", "moe_layout_noalloc",
-            "moe_move_faults", "moe_selftest_bounded_waits", "moe_dispatch_quant")
+            "moe_move_faults", "moe_selftest_bounded_waits", "moe_dispatch_quant", "moe_swap_plan")
 
 
 class MoeLibraryMissing(RuntimeError):
@@ -95,6 +95,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_stats.restype = i
     lib.moe_dispatch.argtypes = [P, L, vp, vp, vp, vp, vp]
     lib.moe_dispatch.restype = i
+    lib.moe_swap_plan.argtypes = [P, L, ctypes.c_int32, vp, vp, vp]
+    lib.moe_swap_plan.restype = i
     lib.moe_dispatch_quant.argtypes = [P, L, vp, vp, vp, vp]
     lib.moe_dispatch_quant.restype = i
     lib.moe_combine.argtypes = [P, L, vp, vp, vp, vp]
@@ -233,6 +235,13 @@ def moe_dispatch(problem: Problem, layout: Layout, x, x_scales, recv, recv_scale
     _check(load_library().moe_dispatch(ctypes.byref(problem.c()), ctypes.byref(layout.c()), _ptr(x),
                                        _ptr(x_scales), _ptr(recv), _ptr(recv_scales), _stream(stream)),
            "moe_dispatch")
+
+
+def moe_swap_plan(problem: Problem, layout: Layout, tau: int, new_expert_to_rank, swaps=None, stream=None):
+    """Per-step intra-host expert swap plan from the layout's expert counts."""
+    _check(load_library().moe_swap_plan(ctypes.byref(problem.c()), ctypes.byref(layout.c()), int(tau),
+                                        _ptr(new_expert_to_rank), _ptr(swaps), _stream(stream)),
+           "moe_swap_plan")
 
 
 def moe_dispatch_quant(problem: Problem, layout: Layout, x_bf16, recv, recv_scales, stream=None):

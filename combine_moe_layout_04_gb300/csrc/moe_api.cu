@@ -184,6 +184,20 @@ int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream
     return MOE_OK;
 }
 
+int moe_swap_plan(const moe_problem* problem, const moe_layout_t* layout, int32_t tau,
+                  int32_t* new_expert_to_rank, int32_t* swaps, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (layout == nullptr || layout->expert_count == nullptr || new_expert_to_rank == nullptr)
+        return MOE_ERR_INVALID;
+    if (!aligned(layout->expert_count, 4) || !aligned(new_expert_to_rank, 4) || !aligned(swaps, 4))
+        return MOE_ERR_ALIGN;
+    return cuda_status(moe::launch_swap_plan(layout->expert_count, problem->expert_to_rank, d.E, d.R, d.P,
+                                             tau, new_expert_to_rank, swaps,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_move_faults(uint32_t* bits, moe_stream_t stream) {
     if (bits == nullptr) return MOE_ERR_INVALID;
     return cuda_status(moe::read_move_faults(bits, reinterpret_cast<cudaStream_t>(stream)));

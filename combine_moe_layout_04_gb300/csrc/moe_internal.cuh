@@ -331,6 +331,8 @@ cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, voi
 cudaError_t launch_dispatch_quant(const MoveArgs& m, const void* x, void* recv, float* rs, int h,
                                   cudaStream_t s);
 cudaError_t read_move_faults(uint32_t* bits, cudaStream_t s);
+cudaError_t launch_swap_plan(const int32_t* count, const int32_t* e2r, int E, int R, int P, int tau,
+                             int32_t* new_e2r, int32_t* swaps, cudaStream_t s);
 cudaError_t run_wait_selftest(uint32_t* bits, cudaStream_t s);
 
 }  // namespace moe

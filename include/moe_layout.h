@@ -256,6 +256,23 @@ int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream
 int moe_layout_noalloc(const moe_problem* problem, const int32_t* ids,
                        const moe_layout_t* layout, moe_stream_t stream);
 
+/* Per-step intra-host expert swap plan ("Balancing and Beyond", section 3.1
+ * and its Figure 2(b)).  Rank loads are the layout's expert_count summed over
+ * each rank's experts (the placement of `problem`).  In every host the ranks
+ * are ordered by load (descending, ties by rank index) and the i-th heaviest
+ * is paired with the i-th lightest; for each pair the one exchange of an
+ * expert x of the heavier rank with an expert y of the lighter that gives the
+ * smallest pair maximum is chosen (ties: smallest x, then smallest y) and
+ * applied when it lowers the pair's maximum by at least max(tau, 1) tokens.
+ *   new_expert_to_rank: device int32 [E], the placement after the swaps (pass
+ *     it as problem->expert_to_rank of the next step);
+ *   swaps: device int32 [H * (ranks_per_host / 2) * 6] or NULL: per host and
+ *     pair, rank a, rank b, x, y (-1 if a rank has no expert), old maximum,
+ *     best new maximum (the swap was applied when new_expert_to_rank moved x).
+ * Needs E <= 1024 (ids fit the search key) like every other call. */
+int moe_swap_plan(const moe_problem* problem, const moe_layout_t* layout, int32_t tau,
+                  int32_t* new_expert_to_rank, int32_t* swaps, moe_stream_t stream);
+
 /* Device faults of the row movers since the last call: bit
  * MOE_FAULT_WAIT_TIMEOUT is set when a bulk-copy pipeline of moe_dispatch or
  * moe_combine waited more than one second for its own copies, gave up, drained
