@@ -19,6 +19,10 @@ arrays through ctypes.  Each wrapper names the passage it follows:
               dispatch_with_permute).
 * combine  -- gate-weighted sum of the k expert outputs in ascending slot order,
               fp32 fma, bf16 round-to-nearest-even (combine_with_unpermute).
+* relay_layout / relay_dispatch / relay_combine -- Mode 2 on one buffer
+              ("Balancing and Beyond", section 3.2): one relay row per (token,
+              host), fan-out from it; per-host partial sums before the final
+              sum.
 * swap_plan -- per-step intra-host expert swap ("Balancing and Beyond",
               section 3.1, Figure 2(b)): heaviest rank paired with lightest,
               one best exchange per pair, accepted if the pair's maximum falls
@@ -96,6 +100,12 @@ def _load():
         lib.oracle_dispatch.restype = None
         lib.oracle_combine.argtypes = [ctypes.POINTER(Problem)] + [p] * 4
         lib.oracle_combine.restype = None
+        lib.oracle_relay_layout.argtypes = [ctypes.POINTER(Problem), p, p]
+        lib.oracle_relay_layout.restype = ctypes.c_int
+        lib.oracle_relay_dispatch.argtypes = [ctypes.POINTER(Problem)] + [p] * 9
+        lib.oracle_relay_dispatch.restype = None
+        lib.oracle_relay_combine.argtypes = [ctypes.POINTER(Problem)] + [p] * 7
+        lib.oracle_relay_combine.restype = None
         lib.oracle_swap_plan.argtypes = [ctypes.POINTER(Problem), p, ctypes.c_int32, p, p]
         lib.oracle_swap_plan.restype = ctypes.c_int
         lib.oracle_quantize_dispatch.argtypes = [ctypes.POINTER(Problem)] + [p] * 4
@@ -202,6 +212,57 @@ def combine(prob: Problem, pos: np.ndarray, y: np.ndarray, w: np.ndarray) -> np.
     out = np.zeros((prob.T, prob.h), np.uint16)
     lib.oracle_combine(ctypes.byref(prob), _ptr(pos), _ptr(y), _ptr(w), _ptr(out))
     return out
+
+
+def relay_layout(prob: Problem, ids: np.ndarray) -> np.ndarray:
+    """Relay row of every (token, host) with the mask bit, -1 otherwise: [T, H]."""
+    lib = _load()
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    H = prob.R // prob.P
+    rp = np.zeros((prob.T, H), np.int32)
+    rc = lib.oracle_relay_layout(ctypes.byref(prob), _ptr(ids), _ptr(rp))
+    if rc != OK:
+        raise OracleError(rc)
+    return rp
+
+
+def relay_dispatch(prob: Problem, ids, pos, relay_pos, x, x_scales=None):
+    """Two-hop dispatch through the relay rows.  Returns (relay, relay_scales,
+    recv, recv_scales) (scales None for bf16)."""
+    lib = _load()
+    ids = np.ascontiguousarray(ids, np.int32)
+    pos = np.ascontiguousarray(pos, np.int32)
+    rp = np.ascontiguousarray(relay_pos, np.int32)
+    x = np.ascontiguousarray(x)
+    n_relay = int((rp >= 0).sum())
+    S = prob.T * prob.k
+    relay = np.zeros((n_relay, prob.h), x.dtype)
+    recv = np.zeros((S, prob.h), x.dtype)
+    rs = rcv_s = None
+    if x_scales is not None:
+        x_scales = np.ascontiguousarray(x_scales, np.float32)
+        G = prob.h // prob.scale_group
+        rs = np.zeros((n_relay, G), np.float32)
+        rcv_s = np.zeros((S, G), np.float32)
+    lib.oracle_relay_dispatch(ctypes.byref(prob), _ptr(ids), _ptr(pos), _ptr(rp), _ptr(x), _ptr(x_scales),
+                              _ptr(relay), _ptr(rs), _ptr(recv), _ptr(rcv_s))
+    return relay, rs, recv, rcv_s
+
+
+def relay_combine(prob: Problem, ids, pos, relay_pos, y, w):
+    """Two-hop combine: bf16 per-host partials, then the ascending host sum.
+    Returns (partial, out) as bf16 bits."""
+    lib = _load()
+    ids = np.ascontiguousarray(ids, np.int32)
+    pos = np.ascontiguousarray(pos, np.int32)
+    rp = np.ascontiguousarray(relay_pos, np.int32)
+    y = np.ascontiguousarray(y, np.uint16)
+    w = np.ascontiguousarray(w, np.float32)
+    partial = np.zeros((int((rp >= 0).sum()), prob.h), np.uint16)
+    out = np.zeros((prob.T, prob.h), np.uint16)
+    lib.oracle_relay_combine(ctypes.byref(prob), _ptr(ids), _ptr(pos), _ptr(rp), _ptr(y), _ptr(w),
+                             _ptr(partial), _ptr(out))
+    return partial, out
 
 
 def swap_plan(prob: Problem, expert_count: np.ndarray, tau: int):

@@ -298,6 +298,86 @@ void oracle_dispatch(const oracle_problem* p, const int32_t* pos,
         }
 }
 
+int oracle_relay_layout(const oracle_problem* p, const int32_t* ids, int32_t* relay_pos) {
+    Placement pl;
+    if (!make_placement(p, &pl)) return ORACLE_ERR_INVALID;
+    if (!ids_valid(p, ids)) return ORACLE_ERR_BAD_IDS;
+    std::vector<uint8_t> m;
+    host_mask(p, pl, ids, &m);
+    // Relay segments in host order; inside a segment, ascending token order.
+    std::vector<int32_t> start(pl.H + 1, 0);
+    for (int hh = 0; hh < pl.H; ++hh) {
+        int32_t c = 0;
+        for (int t = 0; t < p->T; ++t) c += m[(size_t)t * pl.H + hh];
+        start[hh + 1] = start[hh] + c;
+    }
+    for (int hh = 0; hh < pl.H; ++hh) {
+        int32_t next = start[hh];
+        for (int t = 0; t < p->T; ++t)
+            relay_pos[(size_t)t * pl.H + hh] = m[(size_t)t * pl.H + hh] ? next++ : -1;
+    }
+    return ORACLE_OK;
+}
+
+void oracle_relay_dispatch(const oracle_problem* p, const int32_t* ids, const int32_t* pos,
+                           const int32_t* relay_pos, const uint8_t* x, const float* x_scales,
+                           uint8_t* relay, float* relay_scales, uint8_t* recv, float* recv_scales) {
+    Placement pl;
+    make_placement(p, &pl);
+    const size_t row = (size_t)p->h * p->elem_bytes;
+    const size_t groups = p->elem_bytes == 1 ? (size_t)(p->h / p->scale_group) : 0;
+    // hop 1: one copy per (token, host)
+    for (int t = 0; t < p->T; ++t)
+        for (int hh = 0; hh < pl.H; ++hh) {
+            const int32_t r = relay_pos[(size_t)t * pl.H + hh];
+            if (r < 0) continue;
+            std::memcpy(relay + (size_t)r * row, x + (size_t)t * row, row);
+            if (groups) std::memcpy(relay_scales + (size_t)r * groups, x_scales + (size_t)t * groups, groups * 4);
+        }
+    // hop 2: fan-out on the host, from the relay row
+    for (int t = 0; t < p->T; ++t)
+        for (int j = 0; j < p->k; ++j) {
+            const int hh = pl.rank_of_expert[ids[(size_t)t * p->k + j]] / pl.P;
+            const int32_t r = relay_pos[(size_t)t * pl.H + hh];
+            const size_t dst = (size_t)pos[(size_t)t * p->k + j];
+            std::memcpy(recv + dst * row, relay + (size_t)r * row, row);
+            if (groups) std::memcpy(recv_scales + dst * groups, relay_scales + (size_t)r * groups, groups * 4);
+        }
+}
+
+void oracle_relay_combine(const oracle_problem* p, const int32_t* ids, const int32_t* pos,
+                          const int32_t* relay_pos, const uint16_t* y, const float* w,
+                          uint16_t* partial, uint16_t* out) {
+    Placement pl;
+    make_placement(p, &pl);
+    const size_t h = (size_t)p->h;
+    // hop 1: per (token, host) partial sums, rounded to bf16 as they travel
+    for (int t = 0; t < p->T; ++t)
+        for (int hh = 0; hh < pl.H; ++hh) {
+            const int32_t r = relay_pos[(size_t)t * pl.H + hh];
+            if (r < 0) continue;
+            for (size_t c = 0; c < h; ++c) {
+                float acc = 0.0f;
+                for (int j = 0; j < p->k; ++j) {
+                    if (pl.rank_of_expert[ids[(size_t)t * p->k + j]] / pl.P != hh) continue;
+                    const size_t src = (size_t)pos[(size_t)t * p->k + j];
+                    acc = std::fma(w[(size_t)t * p->k + j], oracle_bf16_to_f32(y[src * h + c]), acc);
+                }
+                partial[(size_t)r * h + c] = oracle_f32_to_bf16_rne(acc);
+            }
+        }
+    // hop 2: the token's partials summed in ascending host order
+    for (int t = 0; t < p->T; ++t)
+        for (size_t c = 0; c < h; ++c) {
+            float acc = 0.0f;
+            for (int hh = 0; hh < pl.H; ++hh) {
+                const int32_t r = relay_pos[(size_t)t * pl.H + hh];
+                if (r >= 0) acc = acc + oracle_bf16_to_f32(partial[(size_t)r * h + c]);
+            }
+            out[(size_t)t * h + c] = oracle_f32_to_bf16_rne(acc);
+        }
+}
+
 int oracle_swap_plan(const oracle_problem* p, const int32_t* expert_count, int32_t tau,
                      int32_t* new_expert_to_rank, int32_t* swaps) {
     Placement pl;

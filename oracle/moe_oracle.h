@@ -104,6 +104,27 @@ void oracle_dispatch(const oracle_problem* p, const int32_t* pos,
 void oracle_combine(const oracle_problem* p, const int32_t* pos,
                     const uint16_t* y, const float* w, uint16_t* out);
 
+/* Mode 2 relay ("Balancing and Beyond", section 3.2: one network copy per
+ * token and remote host, fanned out there; combine sums on the relay GPU
+ * before sending back).  On one buffer:
+ *   relay_pos[T*H]: for a token t and host H with mask[t][H] = 1 the relay row
+ *     host_offset[H] + #{t' < t : mask[t'][H] = 1}, otherwise -1.
+ *   relay dispatch: relay[relay_pos[t][H]] = x[t] (hop 1), then
+ *     recv[pos[t, j]] = relay[relay_pos[t][host(e_j)]] (hop 2, the fan-out);
+ *     fp8 scales travel with their rows.
+ *   relay combine: partial[relay_pos[t][H]] = bf16_rne(fma chain over the
+ *     slots j of t on host H in ascending j, from 0.0f, of w[t, j] *
+ *     y[pos[t, j]]) (hop 1), then out[t] = bf16_rne(sum over hosts H with the
+ *     mask bit in ascending H, from 0.0f, of the fp32 value of the partial)
+ *     (hop 2). */
+int oracle_relay_layout(const oracle_problem* p, const int32_t* ids, int32_t* relay_pos);
+void oracle_relay_dispatch(const oracle_problem* p, const int32_t* ids, const int32_t* pos,
+                           const int32_t* relay_pos, const uint8_t* x, const float* x_scales,
+                           uint8_t* relay, float* relay_scales, uint8_t* recv, float* recv_scales);
+void oracle_relay_combine(const oracle_problem* p, const int32_t* ids, const int32_t* pos,
+                          const int32_t* relay_pos, const uint16_t* y, const float* w,
+                          uint16_t* partial, uint16_t* out);
+
 /* Per-step intra-host expert swap ("Balancing and Beyond", section 3.1 and
  * its Figure 2(b)).  Load of rank r: L_r = sum of expert_count over its
  * experts.  In every host the ranks are ordered by load (descending, ties by

@@ -462,3 +462,98 @@ def test_swap_plan_is_the_best_single_exchange(oracle_mod):
         for e in range(E):
             if e not in moved:
                 assert new[e] == e2r[e]
+
+
+# ------------------------------------------------ Mode 2 relay on one buffer
+
+def test_relay_layout_and_dispatch(oracle_mod):
+    """Relay rows: one per (token, host) with the mask bit, host segments at
+    host_offset in ascending token order; their number is the per-host
+    de-duplicated count (Mode 2 network copies plus one local copy per token
+    whose experts include its own host).  Two-hop dispatch equals the flat
+    dispatch byte for byte."""
+    w = mw.Workload("rel", T=150, h=64, k=4, E=24, R=6, P=2, R_src=3)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, R_src=w.R_src)
+    lay = oracle_mod.layout(prob, ids)
+    rp = oracle_mod.relay_layout(prob, ids)
+    assert np.array_equal(rp >= 0, lay["host_mask"].astype(bool))
+    for hh in range(w.H):
+        col = rp[:, hh][rp[:, hh] >= 0]
+        assert np.array_equal(col, lay["host_offset"][hh] + np.arange(lay["host_count"][hh]))
+    st = oracle_mod.stats(prob, ids)
+    own = np.arange(w.T) // (w.T // w.R_src) // w.P
+    local = lay["host_mask"][np.arange(w.T), own].sum()
+    assert (rp >= 0).sum() == st["sum_mode2_copies"] + local
+    x = mw.gen_x_bf16(w)
+    relay, _, recv, _ = oracle_mod.relay_dispatch(prob, ids, lay["pos"], rp, x)
+    assert np.array_equal(recv, oracle_mod.dispatch(prob, lay["pos"], x))
+    for hh in range(w.H):
+        toks = np.nonzero(rp[:, hh] >= 0)[0]
+        assert np.array_equal(relay[rp[toks, hh]], x[toks])
+
+
+def test_relay_combine_exact_when_no_rounding(oracle_mod):
+    """With small-integer expert outputs and unit weights every partial and
+    sum is exact, so two-hop combine equals flat combine bit for bit."""
+    w = mw.Workload("rel2", T=100, h=32, k=4, E=16, R=8, P=2, R_src=1)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h)
+    lay = oracle_mod.layout(prob, ids)
+    rp = oracle_mod.relay_layout(prob, ids)
+    y = mw.f32_to_bf16_bits(np.random.default_rng(3).integers(-20, 20, (w.slots, w.h)).astype(np.float32))
+    ones = np.ones((w.T, w.k), np.float32)
+    _, out = oracle_mod.relay_combine(prob, ids, lay["pos"], rp, y, ones)
+    assert np.array_equal(out, oracle_mod.combine(prob, lay["pos"], y, ones))
+
+
+def test_relay_combine_error_bound(oracle_mod):
+    """Two roundings to bf16 (the partial and the result) plus fp32 sums:
+    |out - exact| <= 2^-8 |exact| + 2^-8 sum_H |partial_H| + fp32 terms."""
+    w = mw.Workload("rel3", T=80, h=256, k=8, E=32, R=8, P=2, R_src=1)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h)
+    lay = oracle_mod.layout(prob, ids)
+    rp = oracle_mod.relay_layout(prob, ids)
+    y = mw.gen_y_host(w)
+    g = mw.gen_gates(w)
+    _, out = oracle_mod.relay_combine(prob, ids, lay["pos"], rp, y, g)
+    terms = g.astype(np.float64)[:, :, None] * mw.bf16_bits_to_f32(y).astype(np.float64)[lay["pos"]]
+    exact = terms.sum(axis=1)
+    host = (ids // (w.E // w.R)) // w.P
+    part = np.stack([np.where((host == hh)[:, :, None], terms, 0).sum(axis=1) for hh in range(w.H)])
+    bound = (2.0 ** -8 * np.abs(exact) + 2.0 ** -8 * np.abs(part).sum(axis=0)
+             + 2 * w.k * 2.0 ** -24 * np.abs(terms).sum(axis=1))
+    got = mw.bf16_bits_to_f32(out).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= bound * (1 + 1e-9))
+
+
+def test_relay_combine_one_host_is_flat(oracle_mod):
+    """With every rank on one host there is one partial per token, equal to the
+    flat combine; the final sum of that single partial adds nothing, so the
+    two-hop result equals the flat combine bit for bit at any values."""
+    w = mw.Workload("rel4", T=90, h=128, k=6, E=32, R=8, P=8, R_src=1)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h)
+    lay = oracle_mod.layout(prob, ids)
+    rp = oracle_mod.relay_layout(prob, ids)
+    assert np.array_equal(rp[:, 0], np.arange(w.T))
+    y, g = mw.gen_y_host(w), mw.gen_gates(w)
+    partial, out = oracle_mod.relay_combine(prob, ids, lay["pos"], rp, y, g)
+    flat = oracle_mod.combine(prob, lay["pos"], y, g)
+    assert np.array_equal(partial, flat) and np.array_equal(out, flat)
+
+
+def test_relay_dispatch_fp8_scales_travel(oracle_mod):
+    """fp8 rows take their per-128-column scales through both hops."""
+    w = mw.Workload("rel5", T=60, h=256, k=4, E=16, R=8, P=4, R_src=2, dtype="fp8")
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, R_src=w.R_src, elem_bytes=1)
+    lay = oracle_mod.layout(prob, ids)
+    rp = oracle_mod.relay_layout(prob, ids)
+    x, xs = mw.gen_x_fp8(w)
+    relay, rs, recv, rcs = oracle_mod.relay_dispatch(prob, ids, lay["pos"], rp, x, xs)
+    flat = lay["recv_src"] // w.k
+    assert np.array_equal(recv, x[flat]) and np.array_equal(rcs, xs[flat])
+    toks = np.nonzero(rp >= 0)[0]
+    assert np.array_equal(rs[rp[rp >= 0]], xs[toks])
