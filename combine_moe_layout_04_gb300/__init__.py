@@ -5,7 +5,8 @@ Argument marshalling only.  Every step runs in the library's CUDA kernels
 mirror the C-ABI declared in ``include/moe_layout.h``:
 
     moe_workspace_bytes, moe_layout, moe_stats_words, moe_stats,
-    moe_dispatch, moe_combine, moe_status, moe_status_string
+    moe_dispatch, moe_combine, moe_status, moe_status_string,
+    moe_relay_layout, moe_dispatch_relay, moe_combine_relay (the Mode 2 relay)
 
 ``Problem`` and ``Layout`` are conveniences that build the C structs and
 allocate the caller-owned device buffers.  If the shared library has not been
@@ -27,6 +28,7 @@ MOE_NOALLOC_SCRATCH_BYTES = 2 << 20
 MOE_DTYPE_BF16, MOE_DTYPE_FP8_E4M3 = 0, 1
 MOE_STATUS_ID_RANGE, MOE_STATUS_ID_REPEAT, MOE_STATUS_PLACEMENT, MOE_STATUS_SRC_OFFSET = 1, 2, 4, 8
 MOE_STATUS_TIMEOUT = 16
+MOE_STATUS_RELAY_CAPACITY = 32
 MOE_FP8_GROUP = 128
 MOE_STATS_HEADER_WORDS = 32
 MOE_FAULT_WAIT_TIMEOUT = 1
@@ -43,7 +45,8 @@ STATS_SRC = ("src_tokens", "src_copies", "src_mode0", "src_mode1", "src_mode2",
 STATS_DST = ("recv_slots", "recv_tokens", "recv_self", "recv_local", "recv_remote", "recv_relay")
 EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
             "moe_combine", "moe_status", "moe_status_string", "moe_layout_noalloc",
-            "moe_move_faults", "moe_selftest_bounded_waits", "moe_dispatch_quant", "moe_swap_plan")
+            "moe_move_faults", "moe_selftest_bounded_waits", "moe_dispatch_quant", "moe_swap_plan",
+            "moe_relay_layout", "moe_dispatch_relay", "moe_combine_relay")
 
 
 class MoeLibraryMissing(RuntimeError):
@@ -70,6 +73,11 @@ _LAYOUT_FIELDS = ("expert_count", "expert_offset", "rank_count", "rank_offset", 
 
 class _LayoutC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in _LAYOUT_FIELDS] + [("stats", ctypes.c_void_p)]
+
+
+class _RelayC(ctypes.Structure):
+    _fields_ = [("relay_pos", ctypes.c_void_p), ("relay_src", ctypes.c_void_p), ("slot_relay", ctypes.c_void_p),
+                ("capacity", ctypes.c_int64)]
 
 
 _lib = None
@@ -101,6 +109,13 @@ def load_library(path: str = LIB_PATH):
     lib.moe_dispatch_quant.restype = i
     lib.moe_combine.argtypes = [P, L, vp, vp, vp, vp]
     lib.moe_combine.restype = i
+    Q = ctypes.POINTER(_RelayC)
+    lib.moe_relay_layout.argtypes = [P, L, vp, Q, vp]
+    lib.moe_relay_layout.restype = i
+    lib.moe_dispatch_relay.argtypes = [P, L, Q, vp, vp, vp, vp, vp, vp, vp]
+    lib.moe_dispatch_relay.restype = i
+    lib.moe_combine_relay.argtypes = [P, L, Q, vp, vp, vp, vp, vp]
+    lib.moe_combine_relay.restype = i
     lib.moe_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.moe_status.restype = i
     lib.moe_layout_noalloc.argtypes = [P, vp, L, vp]
@@ -187,6 +202,24 @@ class Layout:
         return {n: getattr(self, n).cpu().numpy() for n in _LAYOUT_FIELDS}
 
 
+class Relay:
+    """Caller-owned device arrays of the Mode 2 relay rows (moe_relay_t).  The
+    default capacity, T * min(k, H), holds every layout of the problem."""
+
+    def __init__(self, problem: Problem, device="cuda", capacity: Optional[int] = None):
+        import torch
+        p = problem
+        i32 = dict(dtype=torch.int32, device=device)
+        self.capacity = p.num_tokens * min(p.topk, p.num_hosts) if capacity is None else int(capacity)
+        self.relay_pos = torch.empty((p.num_tokens, p.num_hosts), **i32)
+        self.relay_src = torch.empty(max(self.capacity, 1), **i32)
+        self.slot_relay = torch.empty((p.num_tokens, p.topk), **i32)
+
+    def c(self) -> _RelayC:
+        return _RelayC(self.relay_pos.data_ptr(), self.relay_src.data_ptr(), self.slot_relay.data_ptr(),
+                       self.capacity)
+
+
 def _check(rc: int, where: str):
     if rc != MOE_OK:
         raise MoeError(rc, where)
@@ -254,6 +287,28 @@ def moe_dispatch_quant(problem: Problem, layout: Layout, x_bf16, recv, recv_scal
 def moe_combine(problem: Problem, layout: Layout, y, weights, out, stream=None):
     _check(load_library().moe_combine(ctypes.byref(problem.c()), ctypes.byref(layout.c()), _ptr(y),
                                       _ptr(weights), _ptr(out), _stream(stream)), "moe_combine")
+
+
+def moe_relay_layout(problem: Problem, layout: Layout, workspace, relay: Relay, stream=None):
+    """Relay rows of a layout made with this workspace."""
+    _check(load_library().moe_relay_layout(ctypes.byref(problem.c()), ctypes.byref(layout.c()), _ptr(workspace),
+                                           ctypes.byref(relay.c()), _stream(stream)), "moe_relay_layout")
+
+
+def moe_dispatch_relay(problem: Problem, layout: Layout, relay: Relay, x, x_scales, relay_rows, relay_scales,
+                       recv, recv_scales, stream=None):
+    """Two-hop dispatch: x to the relay rows, then the relay rows to recv."""
+    _check(load_library().moe_dispatch_relay(ctypes.byref(problem.c()), ctypes.byref(layout.c()),
+                                             ctypes.byref(relay.c()), _ptr(x), _ptr(x_scales), _ptr(relay_rows),
+                                             _ptr(relay_scales), _ptr(recv), _ptr(recv_scales), _stream(stream)),
+           "moe_dispatch_relay")
+
+
+def moe_combine_relay(problem: Problem, layout: Layout, relay: Relay, y, weights, partial, out, stream=None):
+    """Two-hop combine: per-host bf16 partials, then their sum in host order."""
+    _check(load_library().moe_combine_relay(ctypes.byref(problem.c()), ctypes.byref(layout.c()),
+                                            ctypes.byref(relay.c()), _ptr(y), _ptr(weights), _ptr(partial),
+                                            _ptr(out), _stream(stream)), "moe_combine_relay")
 
 
 def moe_status(workspace, stream=None):

@@ -47,6 +47,27 @@ bool layout_complete(const moe_layout_t* l, int T) {
     return T == 0 || (l->host_mask && l->pos && l->recv_src);
 }
 
+// Relay arrays sized by T may be NULL when T == 0; capacity >= 0.
+bool relay_complete(const moe_relay_t* r, int T) {
+    if (r->capacity < 0) return false;
+    return T == 0 || (r->relay_pos && r->slot_relay && (r->relay_src || r->capacity == 0));
+}
+
+int relay_cap(const moe_relay_t* r) {
+    return r->capacity > (int64_t)INT32_MAX ? INT32_MAX : (int)r->capacity;
+}
+
+moe::RelayArgs relay_args(const moe_relay_t* relay, const moe_layout_t* layout, const Dims& d) {
+    moe::RelayArgs r{};
+    r.relay_pos = relay->relay_pos;
+    r.relay_src = relay->relay_src;
+    r.slot_relay = relay->slot_relay;
+    r.n_relay = layout->host_offset + d.H;
+    r.H = d.H;
+    r.cap = relay_cap(relay);
+    return r;
+}
+
 WsLayout ws_layout(const Dims& d) { return moe::make_ws_layout(d.T, d.E, d.R, d.H, d.Rs); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -169,6 +190,86 @@ int moe_combine(const moe_problem* problem, const moe_layout_t* layout, const vo
     return cuda_status(moe::launch_combine(m, y, weights, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_relay_layout(const moe_problem* problem, const moe_layout_t* layout, void* workspace,
+                     const moe_relay_t* relay, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (!layout_complete(layout, d.T) || workspace == nullptr || relay == nullptr || !relay_complete(relay, d.T))
+        return MOE_ERR_INVALID;
+    if (!aligned(workspace, 256) || !aligned(relay->relay_pos, 4) || !aligned(relay->relay_src, 4) ||
+        !aligned(relay->slot_relay, 4))
+        return MOE_ERR_ALIGN;
+    if (d.T == 0) return MOE_OK;
+    const WsLayout wl = ws_layout(d);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    moe::RelayLayoutArgs a{};
+    a.host_mask = layout->host_mask;
+    a.host_offset = layout->host_offset;
+    a.rank_offset = layout->rank_offset;
+    a.pos = layout->pos;
+    a.relay_pos = relay->relay_pos;
+    a.relay_src = relay->relay_src;
+    a.slot_relay = relay->slot_relay;
+    a.tiles = reinterpret_cast<int32_t*>(ws + wl.relay_tiles);
+    a.status = reinterpret_cast<uint32_t*>(ws + wl.status);
+    a.T = d.T; a.k = d.k; a.H = d.H; a.P = d.P;
+    a.cap = relay_cap(relay);
+    return cuda_status(moe::launch_relay_layout(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_dispatch_relay(const moe_problem* problem, const moe_layout_t* layout, const moe_relay_t* relay,
+                       const void* x, const float* x_scales, void* relay_rows, float* relay_scales,
+                       void* recv, float* recv_scales, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (layout == nullptr || relay == nullptr || !relay_complete(relay, d.T)) return MOE_ERR_INVALID;
+    if (d.T == 0) return MOE_OK;
+    if (layout->pos == nullptr || layout->host_offset == nullptr || x == nullptr || relay_rows == nullptr ||
+        recv == nullptr)
+        return MOE_ERR_INVALID;
+    if (d.fp8 && (x_scales == nullptr || relay_scales == nullptr || recv_scales == nullptr)) return MOE_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(relay_rows, 16) || !aligned(recv, 16) || !aligned(layout->pos, 4) ||
+        !aligned(relay->relay_pos, 4) || !aligned(relay->relay_src, 4) || !aligned(relay->slot_relay, 4))
+        return MOE_ERR_ALIGN;
+    if (d.fp8 && (!aligned(x_scales, 4) || !aligned(relay_scales, 4) || !aligned(recv_scales, 4)))
+        return MOE_ERR_ALIGN;
+    moe::MoveArgs m{};
+    m.pos = layout->pos;
+    m.T = d.T;
+    m.k = d.k;
+    m.nvec = (int)((d.fp8 ? (int64_t)d.h : 2LL * d.h) / 16);
+    const moe::RelayArgs r = relay_args(relay, layout, d);
+    return cuda_status(moe::launch_relay_dispatch(m, r, x, x_scales, relay_rows, relay_scales, recv, recv_scales,
+                                                  d.fp8 ? d.h / MOE_FP8_GROUP : 0,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_combine_relay(const moe_problem* problem, const moe_layout_t* layout, const moe_relay_t* relay,
+                      const void* y, const float* weights, void* partial, void* out, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (layout == nullptr || relay == nullptr || !relay_complete(relay, d.T)) return MOE_ERR_INVALID;
+    if (d.T == 0) return MOE_OK;
+    if (layout->pos == nullptr || layout->host_offset == nullptr || y == nullptr || weights == nullptr ||
+        partial == nullptr || out == nullptr)
+        return MOE_ERR_INVALID;
+    if (!aligned(y, 16) || !aligned(partial, 16) || !aligned(out, 16) || !aligned(weights, 4) ||
+        !aligned(layout->pos, 4) || !aligned(relay->relay_pos, 4) || !aligned(relay->relay_src, 4) ||
+        !aligned(relay->slot_relay, 4))
+        return MOE_ERR_ALIGN;
+    moe::MoveArgs m{};
+    m.pos = layout->pos;
+    m.T = d.T;
+    m.k = d.k;
+    m.nvec = d.h / 8;  // combine is bf16 in and out
+    const moe::RelayArgs r = relay_args(relay, layout, d);
+    return cuda_status(moe::launch_relay_combine(m, r, y, weights, partial, out,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream) {
     if (workspace == nullptr || status_bits == nullptr) return MOE_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -181,6 +282,7 @@ int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream
     if (bits & MOE_STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
     if (bits & (MOE_STATUS_ID_RANGE | MOE_STATUS_ID_REPEAT)) return MOE_ERR_BAD_IDS;
     if (bits & (MOE_STATUS_PLACEMENT | MOE_STATUS_SRC_OFFSET)) return MOE_ERR_INVALID;
+    if (bits & MOE_STATUS_RELAY_CAPACITY) return MOE_ERR_CAPACITY;
     return MOE_OK;
 }
 

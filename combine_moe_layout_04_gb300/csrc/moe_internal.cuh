@@ -40,10 +40,23 @@ struct WsLayout {
     size_t agg;     // int32 [B][E]  per-block expert counts (fully rewritten each call)
     size_t stats;   // int64 [stats_words]  statistics record of the last layout
     size_t stats_words;
+    size_t relay_tiles;  // int32 [relay_tile_count(T)][H]  relay rows per token tile
     size_t total;
     int blocks;     // B
     int groups;     // G
 };
+
+// Relay layout tiles: a multiple of 256 tokens, at most 256 tiles.
+constexpr int kRelayThreads = 256;
+__host__ __device__ inline int relay_tile_tokens(int T) {
+    const int per = (T + 255) / 256;
+    const int t = (per + 255) / 256 * 256;
+    return t > 256 ? t : 256;
+}
+__host__ __device__ inline int relay_tile_count(int T) {
+    const int tile = relay_tile_tokens(T);
+    return T > 0 ? (T + tile - 1) / tile : 0;
+}
 
 inline WsLayout make_ws_layout(int T, int E, int R, int H, int Rs) {
     WsLayout w{};
@@ -70,6 +83,7 @@ inline WsLayout make_ws_layout(int T, int E, int R, int H, int Rs) {
     w.agg = take(4 * (size_t)w.blocks * E);
     w.stats_words = MOE_STATS_HEADER_WORDS + (size_t)MOE_SRC_FIELDS * Rs + (size_t)MOE_DST_FIELDS * R;
     w.stats = take(8 * w.stats_words);
+    w.relay_tiles = take(4 * (size_t)relay_tile_count(T) * H);
     w.total = align_up(o, 256);
     return w;
 }
@@ -93,6 +107,30 @@ struct MoveArgs {
     int nvec;        // 16-byte vectors per row
     int nchunks;     // column chunks per row (one warp per (token, chunk))
     int chunk_vecs;  // vectors per chunk
+};
+
+// Mode 2 relay rows of one layout (moe_relay_t plus the device word that
+// holds how many are in use).
+struct RelayArgs {
+    const int32_t* relay_pos;   // [T][H]
+    const int32_t* relay_src;   // [cap]
+    const int32_t* slot_relay;  // [T * k]
+    const int32_t* n_relay;     // host_offset[H]
+    int H;
+    int cap;
+};
+
+struct RelayLayoutArgs {
+    const uint8_t* host_mask;    // [T][H]
+    const int32_t* host_offset;  // [H+1]
+    const int32_t* rank_offset;  // [R+1]
+    const int32_t* pos;          // [T*k]
+    int32_t* relay_pos;          // [T][H]
+    int32_t* relay_src;          // [cap]
+    int32_t* slot_relay;         // [T*k]
+    int32_t* tiles;              // workspace: [tiles][H]
+    uint32_t* status;            // workspace status word
+    int T, k, H, P, cap;
 };
 
 // ---- inline PTX helpers --------------------------------------------------
@@ -330,6 +368,11 @@ cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, voi
                            cudaStream_t s);
 cudaError_t launch_dispatch_quant(const MoveArgs& m, const void* x, void* recv, float* rs, int h,
                                   cudaStream_t s);
+cudaError_t launch_relay_dispatch(const MoveArgs& m, const RelayArgs& r, const void* x, const float* xs, void* relay,
+                                  float* relay_s, void* recv, float* recv_s, int groups, cudaStream_t s);
+cudaError_t launch_relay_combine(const MoveArgs& m, const RelayArgs& r, const void* y, const float* w, void* partial,
+                                 void* out, cudaStream_t s);
+cudaError_t launch_relay_layout(const RelayLayoutArgs& a, cudaStream_t s);
 cudaError_t read_move_faults(uint32_t* bits, cudaStream_t s);
 cudaError_t launch_swap_plan(const int32_t* count, const int32_t* e2r, int E, int R, int P, int tau,
                              int32_t* new_e2r, int32_t* swaps, cudaStream_t s);

@@ -17,9 +17,12 @@
 //    one warp per (token, column chunk) unit with 16-byte vector loads and
 //    stores, every load of a unit issued before any is used.
 //
-// Both walk a persistent grid over T x chunks units with a tail of at most one
-// unit per warp.  A receive row index outside [0, T*k) is skipped (dispatch)
-// or contributes nothing (combine), so a bad layout cannot write out of bounds.
+// Both walk a persistent grid over units x chunks with a tail of at most one
+// unit per warp.  Which rows a unit touches is a route (below): the flat path
+// pairs a token with its k receive rows; the two hops of the Mode 2 relay pair
+// a token with its relay rows, and a relay row with the receive rows it feeds.
+// A partner row outside its buffer is skipped (dispatch) or contributes
+// nothing (combine), so a bad layout cannot write out of bounds.
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -32,50 +35,101 @@ namespace {
 
 constexpr int kMoveThreads = 256;
 constexpr int kMoveWarps = kMoveThreads / 32;
+constexpr unsigned kAll = 0xffffffffu;
 
-template <int U>
-__global__ void __launch_bounds__(kMoveThreads)
-dispatch_kernel(const MoveArgs m, const uint4* __restrict__ x, const float* __restrict__ xs,
-                uint4* __restrict__ recv, float* __restrict__ rs, int groups) {
-    const int lane = threadIdx.x & 31;
-    const int gwarp = blockIdx.x * kMoveWarps + (threadIdx.x >> 5);
-    const int nwarps = gridDim.x * kMoveWarps;
-    const int S = m.T * m.k;
-    const long long units = (long long)m.T * m.nchunks;
-    for (long long u = gwarp; u < units; u += nwarps) {
-        const int t = (int)(u / m.nchunks);
-        const int c = (int)(u - (long long)t * m.nchunks);
-        int p = -1;
-        if (lane < m.k) {
-            p = m.pos[(size_t)t * m.k + lane];
-            if (p < 0 || p >= S) p = -1;
+// ---- routes ------------------------------------------------------------------
+//
+// A mover walks units; unit u owns one row of its own (the row a dispatch
+// reads, the row a combine writes: self_row) and up to 32 partner rows, one
+// per lane (the rows a dispatch writes, the rows a combine sums, with their
+// weights).  partner() is called by all 32 lanes of a warp with the same u;
+// live is false for a u past the end, which yields no partners.
+
+// Flat: unit = token t; lane j < k: receive row pos[t, j], gate weight w[t, j].
+struct SlotRoute {
+    const int32_t* pos;
+    const float* w;  // NULL for dispatch
+    int T, k;
+    int rows;        // receive rows: T * k
+    __device__ __forceinline__ long long units() const { return T; }
+    __device__ __forceinline__ int self_row(long long u) const { return (int)u; }
+    __device__ __forceinline__ void partner(long long u, bool live, int lane, int& row, float& wt) const {
+        row = -1;
+        wt = 0.0f;
+        if (live && lane < k) {
+            const size_t i = (size_t)u * k + lane;
+            row = pos[i];
+            if (w != nullptr) wt = w[i];
+            if (row < 0 || row >= rows) row = -1;
         }
-        const int v0 = c * m.chunk_vecs + lane;
-        const int vend = min(m.nvec, (c + 1) * m.chunk_vecs);
-        const uint4* xrow = x + (size_t)t * m.nvec;
-        uint4 v[U];
-#pragma unroll
-        for (int i = 0; i < U; ++i)
-            if (v0 + 32 * i < vend) v[i] = ld_stream_v4(xrow + v0 + 32 * i);
-        for (int j = 0; j < m.k; ++j) {
-            const int pj = __shfl_sync(0xffffffffu, p, j);
-            if (pj < 0) continue;
-            uint4* dst = recv + (size_t)pj * m.nvec;
-#pragma unroll
-            for (int i = 0; i < U; ++i)
-                if (v0 + 32 * i < vend) st_v4(dst + v0 + 32 * i, v[i]);
+    }
+};
+
+// Relay hop between a token and its relay rows: unit = token t; lane i: the
+// relay row of the i-th host (ascending) that t reaches, weight 1.  A token
+// reaches at most min(k, H) hosts.
+struct HostRoute {
+    const int32_t* relay_pos;  // [T][H]
+    int T, H;
+    int rows;                  // relay buffer rows
+    __device__ __forceinline__ long long units() const { return T; }
+    __device__ __forceinline__ int self_row(long long u) const { return (int)u; }
+    __device__ __forceinline__ void partner(long long u, bool live, int lane, int& row, float& wt) const {
+        int lo = -1, hi = -1;  // hosts lane and lane + 32
+        if (live) {
+            const int32_t* rp = relay_pos + (size_t)u * H;
+            if (lane < H) lo = rp[lane];
+            if (lane + 32 < H) hi = rp[lane + 32];
+            if (lo >= rows) lo = -1;
+            if (hi >= rows) hi = -1;
         }
-        if (groups > 0 && c == 0) {
-            // fp8 scales: h/128 floats per row, moved with the first chunk.
-            for (int j = 0; j < m.k; ++j) {
-                const int pj = __shfl_sync(0xffffffffu, p, j);
-                if (pj < 0) continue;
-                for (int g = lane; g < groups; g += 32)
-                    rs[(size_t)pj * groups + g] = xs[(size_t)t * groups + g];
+        const unsigned mlo = __ballot_sync(kAll, lo >= 0), mhi = __ballot_sync(kAll, hi >= 0);
+        const int nlo = __popc(mlo), n = nlo + __popc(mhi);
+        // lane i takes the i-th set bit of (mhi:mlo)
+        unsigned m = lane < nlo ? mlo : mhi;
+        const int skip = lane < nlo ? lane : lane - nlo;
+        for (int i = 0; i < skip && lane < n; ++i) m &= m - 1;
+        const int from = lane < n ? __ffs(m) - 1 : 0;
+        const int vlo = __shfl_sync(kAll, lo, from), vhi = __shfl_sync(kAll, hi, from);
+        row = lane < n ? (lane < nlo ? vlo : vhi) : -1;
+        wt = row >= 0 ? 1.0f : 0.0f;
+    }
+};
+
+// Relay hop between a relay row and the receive rows it feeds: unit = relay
+// row r of token t = relay_src[r]; lane j < k: receive row pos[t, j] with
+// weight w[t, j] when slot j is fed by r (slot_relay[t, j] == r).  The number
+// of relay rows is read on the device.
+struct RelaySlotRoute {
+    const int32_t* relay_src;   // [cap]
+    const int32_t* slot_relay;  // [T * k]
+    const int32_t* pos;
+    const float* w;             // NULL for dispatch
+    const int32_t* n_relay;     // device word: relay rows in use
+    int T, k;
+    int rows;                   // receive rows: T * k
+    int cap;                    // relay buffer rows
+    __device__ __forceinline__ long long units() const {
+        const int n = __ldg(n_relay);
+        return n < 0 ? 0 : (n < cap ? n : cap);
+    }
+    __device__ __forceinline__ int self_row(long long u) const { return (int)u; }
+    __device__ __forceinline__ void partner(long long u, bool live, int lane, int& row, float& wt) const {
+        row = -1;
+        wt = 0.0f;
+        if (live && lane < k) {
+            const int t = relay_src[u];
+            if (t >= 0 && t < T) {
+                const size_t i = (size_t)t * k + lane;
+                if (slot_relay[i] == (int)u) {
+                    row = pos[i];
+                    if (w != nullptr) wt = w[i];
+                    if (row < 0 || row >= rows) row = -1;
+                }
             }
         }
     }
-}
+};
 
 __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4& v) {
     const uint32_t q[4] = {v.x, v.y, v.z, v.w};
@@ -96,27 +150,23 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
     return make_uint4(q[0], q[1], q[2], q[3]);
 }
 
-// KB slots are gathered per round (all KB x U loads issued first), then
-// accumulated in ascending slot order; k > KB takes several rounds.
-template <int KB, int U>
+// KB partners are gathered per round (all KB x U loads issued first), then
+// accumulated in ascending lane order; more than KB partners take several
+// rounds.  Lanes >= nl carry no partner.
+template <int KB, int U, class Route>
 __global__ void __launch_bounds__(kMoveThreads)
-combine_kernel(const MoveArgs m, const uint4* __restrict__ y, const float* __restrict__ w,
+combine_kernel(const Route rt, const MoveArgs m, int nl, const uint4* __restrict__ y,
                uint4* __restrict__ out) {
     const int lane = threadIdx.x & 31;
     const int gwarp = blockIdx.x * kMoveWarps + (threadIdx.x >> 5);
     const int nwarps = gridDim.x * kMoveWarps;
-    const int S = m.T * m.k;
-    const long long units = (long long)m.T * m.nchunks;
+    const long long units = rt.units() * m.nchunks;
     for (long long u = gwarp; u < units; u += nwarps) {
-        const int t = (int)(u / m.nchunks);
-        const int c = (int)(u - (long long)t * m.nchunks);
-        int p = -1;
-        float wt = 0.0f;
-        if (lane < m.k) {
-            p = m.pos[(size_t)t * m.k + lane];
-            wt = w[(size_t)t * m.k + lane];
-            if (p < 0 || p >= S) p = -1;
-        }
+        const long long ui = u / m.nchunks;
+        const int c = (int)(u - ui * m.nchunks);
+        int p;
+        float wt;
+        rt.partner(ui, true, lane, p, wt);
         const int v0 = c * m.chunk_vecs + lane;
         const int vend = min(m.nvec, (c + 1) * m.chunk_vecs);
         float acc[U][8];
@@ -124,14 +174,14 @@ combine_kernel(const MoveArgs m, const uint4* __restrict__ y, const float* __res
         for (int i = 0; i < U; ++i)
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[i][q] = 0.0f;
-        for (int jb = 0; jb < m.k; jb += KB) {
+        for (int jb = 0; jb < nl; jb += KB) {
             uint4 v[KB][U];
             float wj[KB];
 #pragma unroll
             for (int j = 0; j < KB; ++j) {
-                const int pj = __shfl_sync(0xffffffffu, p, (jb + j) & 31);
-                wj[j] = __shfl_sync(0xffffffffu, wt, (jb + j) & 31);
-                const bool use = (jb + j < m.k) && pj >= 0;
+                const int pj = __shfl_sync(kAll, p, (jb + j) & 31);
+                wj[j] = __shfl_sync(kAll, wt, (jb + j) & 31);
+                const bool use = (jb + j < nl) && pj >= 0;
                 const uint4* src = y + (size_t)(use ? pj : 0) * m.nvec;
 #pragma unroll
                 for (int i = 0; i < U; ++i) {
@@ -142,12 +192,12 @@ combine_kernel(const MoveArgs m, const uint4* __restrict__ y, const float* __res
             }
 #pragma unroll
             for (int j = 0; j < KB; ++j) {
-                if (jb + j >= m.k) break;
+                if (jb + j >= nl) break;
 #pragma unroll
                 for (int i = 0; i < U; ++i) fma_bf16x8(acc[i], wj[j], v[j][i]);
             }
         }
-        uint4* orow = out + (size_t)t * m.nvec;
+        uint4* orow = out + (size_t)rt.self_row(ui) * m.nvec;
 #pragma unroll
         for (int i = 0; i < U; ++i)
             if (v0 + 32 * i < vend) st_v4(orow + v0 + 32 * i, pack_bf16x8(acc[i]));
@@ -241,10 +291,10 @@ __device__ __forceinline__ void drain_stages(uint32_t bar0, const bool (&pending
 }
 
 // Combine: each warp owns STAGES stages of 8 rows x CHUNK bytes; a stage holds
-// the k row pieces of one (token, column chunk) unit.
-template <int WARPS, int STAGES, int CHUNK>
+// the partner row pieces (at most 8) of one (unit, column chunk).
+template <int WARPS, int STAGES, int CHUNK, class Route>
 __global__ void __launch_bounds__(WARPS * 32, 1)
-combine_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ y, const float* __restrict__ w,
+combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y,
                     uint8_t* __restrict__ out, int row_bytes) {
     constexpr int KMAX = 8;
     constexpr int STAGE_BYTES = KMAX * CHUNK;
@@ -260,32 +310,23 @@ combine_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ y, const float
     }
     __syncwarp();
 
-    const int S = m.T * m.k;
-    const int nch = m.nchunks;
-    const long long units = (long long)m.T * nch;
+    const long long units = rt.units() * nch;
     const long long nw = (long long)gridDim.x * WARPS;
     const long long gw = (long long)blockIdx.x * WARPS + warp;
 
-    long long su[STAGES];   // unit held by each stage
-    unsigned vm[STAGES];    // rows of that unit that were fetched
-    float wr[STAGES];       // lane j < k: gate weight of row j of that unit
+    long long su[STAGES];   // (unit, chunk) held by each stage
+    unsigned vm[STAGES];    // partner rows of that unit that were fetched
+    float wr[STAGES];       // lane j: weight of partner j of that unit
     bool pending[STAGES];
     uint32_t ph[STAGES];
 
     auto fetch_meta = [&](long long u, int& p, float& wv) {
-        p = -1;
-        wv = 0.0f;
-        if (u < units && lane < m.k) {
-            const int t = (int)(u / nch);
-            p = m.pos[(size_t)t * m.k + lane];
-            wv = w[(size_t)t * m.k + lane];
-            if (p < 0 || p >= S) p = -1;
-        }
+        rt.partner(u / nch, u < units, lane, p, wv);
+        if (lane >= KMAX) p = -1;  // routes launched here have at most 8 partners
     };
-    // Issues the k bulk copies of unit u into stage s (all lanes call it).
+    // Issues the partner bulk copies of unit u into stage s (all lanes call it).
     auto issue = [&](int s, long long u, int p) -> unsigned {
-        const int t = (int)(u / nch);
-        const int c = (int)(u - (long long)t * nch);
+        const int c = (int)(u % nch);
         const int cb = min(CHUNK, row_bytes - c * CHUNK);
         const unsigned mask = __ballot_sync(0xffffffffu, p >= 0);
         if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(__popc(mask) * cb));
@@ -325,23 +366,21 @@ combine_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ y, const float
             }
             ph[s] += 1;
             pending[s] = false;
-            const int t = (int)(u / nch);
-            const int c = (int)(u - (long long)t * nch);
+            const long long ui = u / nch;
+            const int c = (int)(u - ui * nch);
             const int cb = min(CHUNK, row_bytes - c * CHUNK);
             float wj[KMAX];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) wj[j] = __shfl_sync(0xffffffffu, wr[s], j);
             const uint32_t st = stage0 + s * STAGE_BYTES;
-            uint4* orow = reinterpret_cast<uint4*>(out + (size_t)t * row_bytes + (size_t)c * CHUNK);
+            uint4* orow = reinterpret_cast<uint4*>(out + (size_t)rt.self_row(ui) * row_bytes + (size_t)c * CHUNK);
             for (int v = lane; v < cb / 16; v += 32) {
                 float acc[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j) {
-                    if (j >= m.k) break;
+                for (int j = 0; j < KMAX; ++j)
                     if ((vm[s] >> j) & 1u) fma_bf16x8(acc, wj[j], lds_v4(st + j * CHUNK + v * 16));
-                }
                 st_v4(orow + v, pack_bf16x8(acc));
             }
             __syncwarp();
@@ -361,11 +400,12 @@ combine_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ y, const float
     }
 }
 
-// Dispatch: each warp owns STAGES stages of CHUNK bytes of x; a stage holds one
-// (token, column chunk) unit, written to its k receive rows by k bulk stores.
-template <int WARPS, int STAGES, int CHUNK, bool EVICT_FIRST = false>
+// Dispatch: each warp owns STAGES stages of CHUNK bytes of source rows; a stage
+// holds one (unit, column chunk), written to the unit's partner rows by one
+// bulk store each.
+template <int WARPS, int STAGES, int CHUNK, class Route>
 __global__ void __launch_bounds__(WARPS * 32, 1)
-dispatch_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ x, const float* __restrict__ xs,
+dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ x, const float* __restrict__ xs,
                      uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
@@ -379,29 +419,22 @@ dispatch_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ x, const floa
     }
     __syncwarp();
 
-    const int S = m.T * m.k;
-    const int nch = m.nchunks;
-    const long long units = (long long)m.T * nch;
+    const long long units = rt.units() * nch;
     const long long nw = (long long)gridDim.x * WARPS;
     const long long gw = (long long)blockIdx.x * WARPS + warp;
 
     long long su[STAGES];
     bool pending[STAGES];
     uint32_t ph[STAGES];
-    const uint64_t pol = EVICT_FIRST ? l2_evict_first_policy() : 0ull;
     // Lane 0 issues the bulk load of unit u into stage s.
     auto issue = [&](int s, long long u) {
         if (lane == 0) {
-            const int t = (int)(u / nch);
-            const int c = (int)(u - (long long)t * nch);
+            const long long ui = u / nch;
+            const int c = (int)(u - ui * nch);
             const int cb = min(CHUNK, row_bytes - c * CHUNK);
             mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)cb);
-            if (EVICT_FIRST)
-                bulk_g2s_hint(stage0 + s * CHUNK, x + (size_t)t * row_bytes + (size_t)c * CHUNK, (uint32_t)cb,
-                              bar0 + 8 * s, pol);
-            else
-                bulk_g2s(stage0 + s * CHUNK, x + (size_t)t * row_bytes + (size_t)c * CHUNK, (uint32_t)cb,
-                         bar0 + 8 * s);
+            bulk_g2s(stage0 + s * CHUNK, x + (size_t)rt.self_row(ui) * row_bytes + (size_t)c * CHUNK, (uint32_t)cb,
+                     bar0 + 8 * s);
         }
     };
 
@@ -419,14 +452,12 @@ dispatch_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ x, const floa
         for (int s = 0; s < STAGES; ++s) {
             if (!pending[s] || failed) continue;
             const long long u = su[s];
-            const int t = (int)(u / nch);
-            const int c = (int)(u - (long long)t * nch);
+            const long long ui = u / nch;
+            const int c = (int)(u - ui * nch);
             const int cb = min(CHUNK, row_bytes - c * CHUNK);
-            int p = -1;
-            if (lane < m.k) {
-                p = m.pos[(size_t)t * m.k + lane];
-                if (p < 0 || p >= S) p = -1;
-            }
+            int p;
+            float unused;
+            rt.partner(ui, true, lane, p, unused);
             // give up as a warp, so that no lane runs ahead into a shuffle
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs))) {
                 failed = true;
@@ -435,21 +466,14 @@ dispatch_bulk_kernel(const MoveArgs m, const uint8_t* __restrict__ x, const floa
             ph[s] += 1;
             pending[s] = false;
             fence_proxy_async_smem();
-            if (p >= 0) {
-                if (EVICT_FIRST)
-                    bulk_s2g_hint(recv + (size_t)p * row_bytes + (size_t)c * CHUNK, stage0 + s * CHUNK,
-                                  (uint32_t)cb, pol);
-                else
-                    bulk_s2g(recv + (size_t)p * row_bytes + (size_t)c * CHUNK, stage0 + s * CHUNK, (uint32_t)cb);
-            }
+            if (p >= 0) bulk_s2g(recv + (size_t)p * row_bytes + (size_t)c * CHUNK, stage0 + s * CHUNK, (uint32_t)cb);
             bulk_commit();
             if (groups > 0 && c == 0) {
                 // fp8 scales: h/128 floats per row, moved with the first chunk.
-                for (int j = 0; j < m.k; ++j) {
-                    const int pj = __shfl_sync(0xffffffffu, p, j);
-                    if (pj < 0) continue;
-                    for (int g = lane; g < groups; g += 32)
-                        rs[(size_t)pj * groups + g] = xs[(size_t)t * groups + g];
+                const size_t src = (size_t)rt.self_row(ui) * groups;
+                for (unsigned mm = __ballot_sync(0xffffffffu, p >= 0); mm; mm &= mm - 1) {
+                    const int pj = __shfl_sync(0xffffffffu, p, __ffs(mm) - 1);
+                    for (int g = lane; g < groups; g += 32) rs[(size_t)pj * groups + g] = xs[src + g];
                 }
             }
             // The stage may be refilled once every lane's stores have read it.
@@ -487,13 +511,14 @@ int grid_for(K kernel, long long units) {
 constexpr int kCombWarps = 8, kCombStages = 2, kCombChunk = 512, kCombCtasPerSm = 3;
 constexpr int kDispWarps = 4, kDispStages = 4, kDispChunk = 7168, kDispCtasPerSm = 1;
 
-template <int WARPS, int STAGES, int CHUNK, int PER_SM>
-cudaError_t launch_combine_bulk(MoveArgs m, const void* y, const float* w, void* out, cudaStream_t stream) {
-    const int row_bytes = m.nvec * 16;
-    m.nchunks = (row_bytes + CHUNK - 1) / CHUNK;
-    const long long units = (long long)m.T * m.nchunks;
+template <int WARPS, int STAGES, int CHUNK, int PER_SM, class Route>
+cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, const void* y, void* out,
+                                cudaStream_t stream) {
+    const int row_bytes = nvec * 16;
+    const int nch = (row_bytes + CHUNK - 1) / CHUNK;
+    const long long units = max_units * nch;
     if (units == 0) return cudaSuccess;
-    auto kern = combine_bulk_kernel<WARPS, STAGES, CHUNK>;
+    auto kern = combine_bulk_kernel<WARPS, STAGES, CHUNK, Route>;
     const size_t smem = (size_t)WARPS * STAGES * 8 * CHUNK;
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -501,19 +526,18 @@ cudaError_t launch_combine_bulk(MoveArgs m, const void* y, const float* w, void*
     const long long need = (units + WARPS - 1) / WARPS;
     const long long cap = (long long)sms * PER_SM;
     const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
-    kern<<<grid, WARPS * 32, smem, stream>>>(m, static_cast<const uint8_t*>(y), w, static_cast<uint8_t*>(out),
+    kern<<<grid, WARPS * 32, smem, stream>>>(rt, nch, static_cast<const uint8_t*>(y), static_cast<uint8_t*>(out),
                                              row_bytes);
     return cudaGetLastError();
 }
 
-template <int WARPS, int STAGES, int CHUNK, int PER_SM>
-cudaError_t launch_dispatch_bulk(MoveArgs m, const void* x, const float* xs, void* recv, float* rs,
-                                 int groups, cudaStream_t stream) {
-    const int row_bytes = m.nvec * 16;
-    m.nchunks = (row_bytes + CHUNK - 1) / CHUNK;
-    const long long units = (long long)m.T * m.nchunks;
+template <int WARPS, int STAGES, int CHUNK, int PER_SM, class Route>
+cudaError_t launch_dispatch_bulk(const Route& rt, long long max_units, int row_bytes, const void* x, const float* xs,
+                                 void* dst, float* ds, int groups, cudaStream_t stream) {
+    const int nch = (row_bytes + CHUNK - 1) / CHUNK;
+    const long long units = max_units * nch;
     if (units == 0) return cudaSuccess;
-    auto kern = dispatch_bulk_kernel<WARPS, STAGES, CHUNK>;
+    auto kern = dispatch_bulk_kernel<WARPS, STAGES, CHUNK, Route>;
     const size_t smem = (size_t)WARPS * STAGES * CHUNK;
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -521,56 +545,79 @@ cudaError_t launch_dispatch_bulk(MoveArgs m, const void* x, const float* xs, voi
     const long long need = (units + WARPS - 1) / WARPS;
     const long long cap = (long long)sms * PER_SM;
     const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
-    kern<<<grid, WARPS * 32, smem, stream>>>(m, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(recv), rs,
-                                             row_bytes, groups);
+    kern<<<grid, WARPS * 32, smem, stream>>>(rt, nch, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(dst),
+                                             ds, row_bytes, groups);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dispatch_lsu(const MoveArgs& m0, const void* x, const float* xs, void* recv,
-                                float* rs, int groups, cudaStream_t stream) {
-    constexpr int U = 4;
-    MoveArgs m = m0;
+template <int KB, int U, class Route>
+cudaError_t launch_combine_t(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
+                             cudaStream_t stream) {
+    MoveArgs m{};
+    m.nvec = nvec;
     m.chunk_vecs = 32 * U;
     m.nchunks = (m.nvec + m.chunk_vecs - 1) / m.chunk_vecs;
-    const long long units = (long long)m.T * m.nchunks;
+    const long long units = max_units * m.nchunks;
     if (units == 0) return cudaSuccess;
-    auto kern = dispatch_kernel<U>;
-    kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(m, static_cast<const uint4*>(x), xs,
-                                                              static_cast<uint4*>(recv), rs, groups);
-    return cudaGetLastError();
-}
-
-template <int KB, int U>
-cudaError_t launch_combine_t(MoveArgs m, const void* y, const float* w, void* out, cudaStream_t stream) {
-    m.chunk_vecs = 32 * U;
-    m.nchunks = (m.nvec + m.chunk_vecs - 1) / m.chunk_vecs;
-    const long long units = (long long)m.T * m.nchunks;
-    if (units == 0) return cudaSuccess;
-    auto kern = combine_kernel<KB, U>;
-    kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(m, static_cast<const uint4*>(y), w,
+    auto kern = combine_kernel<KB, U, Route>;
+    kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(rt, m, nl, static_cast<const uint4*>(y),
                                                               static_cast<uint4*>(out));
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine_lsu(const MoveArgs& m, const void* y, const float* w, void* out,
-                               cudaStream_t stream) {
-    if (m.k >= 8) return launch_combine_t<8, 1>(m, y, w, out, stream);
-    if (m.k >= 4) return launch_combine_t<4, 2>(m, y, w, out, stream);
-    if (m.k >= 2) return launch_combine_t<2, 4>(m, y, w, out, stream);
-    return launch_combine_t<1, 4>(m, y, w, out, stream);
+// Sums at most nl partner rows per unit: the bulk pipeline holds 8 per stage,
+// more go to the LSU kernel.
+template <class Route>
+cudaError_t launch_combine_route(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
+                                 cudaStream_t stream) {
+    if (nl <= 8)
+        return launch_combine_bulk<kCombWarps, kCombStages, kCombChunk, kCombCtasPerSm>(rt, max_units, nvec, y, out,
+                                                                                        stream);
+    return launch_combine_t<8, 1>(rt, max_units, nvec, nl, y, out, stream);
+}
+
+long long relay_units_bound(const MoveArgs& m, const RelayArgs& r) {
+    const long long most = (long long)m.T * (m.k < r.H ? m.k : r.H);
+    return most < r.cap ? most : r.cap;
 }
 
 }  // namespace
 
 cudaError_t launch_dispatch(const MoveArgs& m, const void* x, const float* xs, void* recv,
                             float* rs, int groups, cudaStream_t stream) {
-    return launch_dispatch_bulk<kDispWarps, kDispStages, kDispChunk, kDispCtasPerSm>(m, x, xs, recv, rs, groups, stream);
+    const SlotRoute rt{m.pos, nullptr, m.T, m.k, m.T * m.k};
+    return launch_dispatch_bulk<kDispWarps, kDispStages, kDispChunk, kDispCtasPerSm>(rt, m.T, m.nvec * 16, x, xs, recv,
+                                                                                     rs, groups, stream);
 }
 
 cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, void* out,
                            cudaStream_t stream) {
-    if (m.k <= 8) return launch_combine_bulk<kCombWarps, kCombStages, kCombChunk, kCombCtasPerSm>(m, y, w, out, stream);
-    return launch_combine_lsu(m, y, w, out, stream);
+    const SlotRoute rt{m.pos, w, m.T, m.k, m.T * m.k};
+    return launch_combine_route(rt, m.T, m.nvec, m.k, y, out, stream);
+}
+
+cudaError_t launch_relay_dispatch(const MoveArgs& m, const RelayArgs& r, const void* x, const float* xs, void* relay,
+                                  float* relay_s, void* recv, float* recv_s, int groups, cudaStream_t stream) {
+    // hop 1: each token to its relay rows, one per host it reaches
+    const HostRoute hop1{r.relay_pos, m.T, r.H, r.cap};
+    cudaError_t e = launch_dispatch_bulk<kDispWarps, kDispStages, kDispChunk, kDispCtasPerSm>(
+        hop1, m.T, m.nvec * 16, x, xs, relay, relay_s, groups, stream);
+    if (e != cudaSuccess) return e;
+    // hop 2: each relay row to the receive rows of its host's slots
+    const RelaySlotRoute hop2{r.relay_src, r.slot_relay, m.pos, nullptr, r.n_relay, m.T, m.k, m.T * m.k, r.cap};
+    return launch_dispatch_bulk<kDispWarps, kDispStages, kDispChunk, kDispCtasPerSm>(
+        hop2, relay_units_bound(m, r), m.nvec * 16, relay, relay_s, recv, recv_s, groups, stream);
+}
+
+cudaError_t launch_relay_combine(const MoveArgs& m, const RelayArgs& r, const void* y, const float* w, void* partial,
+                                 void* out, cudaStream_t stream) {
+    // hop 1: each relay row sums the weighted expert rows of its host's slots
+    const RelaySlotRoute hop1{r.relay_src, r.slot_relay, m.pos, w, r.n_relay, m.T, m.k, m.T * m.k, r.cap};
+    cudaError_t e = launch_combine_route(hop1, relay_units_bound(m, r), m.nvec, m.k, y, partial, stream);
+    if (e != cudaSuccess) return e;
+    // hop 2: each token sums its relay rows in ascending host order
+    const HostRoute hop2{r.relay_pos, m.T, r.H, r.cap};
+    return launch_combine_route(hop2, m.T, m.nvec, m.k < r.H ? m.k : r.H, partial, out, stream);
 }
 
 cudaError_t launch_dispatch_quant(const MoveArgs& m0, const void* x, void* recv, float* rs, int h,

@@ -52,7 +52,8 @@ typedef enum {
     MOE_ERR_BAD_IDS = 3,   /* an expert id out of [0, E) or repeated in a row */
     MOE_ERR_ALIGN = 4,     /* a row buffer is not 16-byte aligned */
     MOE_ERR_CAPACITY = 5,  /* the problem needs more scratch than
-                              moe_layout_noalloc's fixed buffer holds */
+                              moe_layout_noalloc's fixed buffer holds, or
+                              more relay rows than moe_relay_t holds */
     MOE_ERR_TIMEOUT = 6    /* a bounded device wait gave up (see
                               MOE_STATUS_TIMEOUT); outputs are incomplete */
 } moe_status_code;
@@ -69,6 +70,9 @@ typedef enum {
 #define MOE_STATUS_SRC_OFFSET 0x8u   /* src_rank_offsets not ascending 0..T */
 #define MOE_STATUS_TIMEOUT    0x10u  /* the layout's grid barrier waited more
                                         than one second and gave up */
+#define MOE_STATUS_RELAY_CAPACITY 0x20u  /* moe_relay_layout: the layout has
+                                        more relay rows than moe_relay_t's
+                                        capacity (rows past it are dropped) */
 
 /* Limits checked on the host. */
 #define MOE_MAX_TOPK     32
@@ -223,9 +227,66 @@ int moe_dispatch_quant(const moe_problem* problem, const moe_layout_t* layout,
 int moe_combine(const moe_problem* problem, const moe_layout_t* layout,
                 const void* y, const float* weights, void* out, moe_stream_t stream);
 
+/* ---- Mode 2 relay on one buffer ------------------------------------------
+ * The hierarchical path of "Balancing and Beyond", section 3.2 (and the
+ * "Mode 2" accounting of "Poor HybridEP performance on dual-node 16x B300
+ * GPUs"): a token crosses to each remote host it needs once, to the GPU of
+ * its own index there, which fans it out to the expert rows on that host; on
+ * the way back that GPU sums the host's weighted expert outputs for the token
+ * first, so one row per (token, host) crosses again.  On one GPU both hops
+ * run through a relay buffer with one row per (token, host) of the layout's
+ * host_mask: the token's own host included, so that every slot takes the same
+ * two hops.
+ *
+ * Relay rows (caller-allocated device int32 arrays):
+ *   relay_pos[t][H] = host_offset[H] + #{t' < t : host_mask[t'][H] = 1} when
+ *                     host_mask[t][H] = 1, else -1        [T, H]
+ *   relay_src[r]    = the token of relay row r             [capacity]
+ *   slot_relay[t*k + j] = relay_pos[t][host of slot (t, j)]  [T * k]
+ * Relay row count = host_offset[H] (the Mode 2 network copies plus one local
+ * copy per token whose experts include its own host) <= T * min(k, H). */
+typedef struct moe_relay_t {
+    int32_t* relay_pos;
+    int32_t* relay_src;
+    int32_t* slot_relay;
+    int64_t capacity;   /* rows the relay buffers hold; T * min(k, H) always fits */
+} moe_relay_t;
+
+/* Relay rows of a layout made by moe_layout with this workspace.  Reads the
+ * layout's host_mask, host_offset, rank_offset and pos.  Sets
+ * MOE_STATUS_RELAY_CAPACITY in the workspace's status word when host_offset[H]
+ * exceeds capacity (moe_status then returns MOE_ERR_CAPACITY).  All arrays
+ * 4-byte aligned, the workspace 256-byte aligned. */
+int moe_relay_layout(const moe_problem* problem, const moe_layout_t* layout, void* workspace,
+                     const moe_relay_t* relay, moe_stream_t stream);
+
+/* Two-hop dispatch: relay[relay_pos[t][H]] = x[t] for every (t, H) with the
+ * mask bit (hop 1), then recv[pos[t, j]] = relay[slot_relay[t*k + j]] for every
+ * slot (hop 2); fp8 scales travel with their rows.  recv equals what
+ * moe_dispatch writes, byte for byte.
+ *   relay_rows: [capacity, h] bf16 or e4m3; relay_scales: fp32
+ *   [capacity, h/128] (fp8) or NULL; the rest as for moe_dispatch.  Row
+ *   buffers 16-byte aligned. */
+int moe_dispatch_relay(const moe_problem* problem, const moe_layout_t* layout, const moe_relay_t* relay,
+                       const void* x, const float* x_scales, void* relay_rows, float* relay_scales,
+                       void* recv, float* recv_scales, moe_stream_t stream);
+
+/* Two-hop combine, bf16 in and out:
+ *   hop 1: partial[r] = bf16_rne(sum over the slots j of token t = relay_src[r]
+ *          with slot_relay[t*k + j] = r, in ascending j, of w[t, j] *
+ *          y[pos[t, j]]), one fp32 fma per term from 0.0f;
+ *   hop 2: out[t] = bf16_rne(sum over the hosts H with host_mask[t][H] = 1, in
+ *          ascending H, of partial[relay_pos[t][H]]), fp32 adds from 0.0f.
+ * With one host this equals moe_combine bit for bit; otherwise it differs
+ * from it by the rounding of the partials to bf16.
+ *   partial: bf16 [capacity, h]; y, weights, out as for moe_combine. */
+int moe_combine_relay(const moe_problem* problem, const moe_layout_t* layout, const moe_relay_t* relay,
+                      const void* y, const float* weights, void* partial, void* out, moe_stream_t stream);
+
 /* Waits for the stream, then reads the device status bits of the workspace
- * (the faults found by the last moe_layout).  *status_bits receives them;
- * returns MOE_OK, MOE_ERR_BAD_IDS, MOE_ERR_INVALID or MOE_ERR_CUDA. */
+ * (the faults found by the last moe_layout and moe_relay_layout).
+ * *status_bits receives them; returns MOE_OK, MOE_ERR_BAD_IDS,
+ * MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT or MOE_ERR_CUDA. */
 int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream);
 
 /* Layout without a caller workspace -- this entry point has no counterpart

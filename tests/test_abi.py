@@ -103,3 +103,32 @@ def test_host_rejects_misaligned_rows(moe):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_dispatch(pf, lay, good, None, good, None, stream=0)   # fp8 needs scales
     assert ei.value.code == moe.MOE_ERR_INVALID
+
+
+def test_host_rejects_bad_relay_calls(moe):
+    """Relay entry points: NULL arrays, negative capacity and misaligned rows
+    are rejected on the host."""
+    p = _p(moe)
+    lay = moe.Layout.__new__(moe.Layout)
+    for n in moe._LAYOUT_FIELDS:
+        setattr(lay, n, _Fake(0x10000))
+    rel = moe.Relay.__new__(moe.Relay)
+    rel.relay_pos, rel.relay_src, rel.slot_relay, rel.capacity = _Fake(0x60000), _Fake(0x61000), _Fake(0x62000), 512
+    good, odd = _Fake(0x20000), _Fake(0x20008)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_relay_layout(p, lay, _Fake(0x50010), rel, stream=0)      # workspace not 256-aligned
+    assert ei.value.code == moe.MOE_ERR_ALIGN
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_dispatch_relay(p, lay, rel, good, None, odd, None, good, None, stream=0)
+    assert ei.value.code == moe.MOE_ERR_ALIGN
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_combine_relay(p, lay, rel, good, _Fake(0x30000), good, odd, stream=0)
+    assert ei.value.code == moe.MOE_ERR_ALIGN
+    rel.capacity = -1
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_combine_relay(p, lay, rel, good, _Fake(0x30000), good, good, stream=0)
+    assert ei.value.code == moe.MOE_ERR_INVALID
+    rel.capacity, rel.slot_relay = 512, _Fake(0)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_dispatch_relay(p, lay, rel, good, None, good, None, good, None, stream=0)
+    assert ei.value.code == moe.MOE_ERR_INVALID
