@@ -258,6 +258,71 @@ def workload_config(w):
 
 # ----------------------------------------------------------------- GPU arm
 
+def relay_bytes(w, n_relay):
+    """Mode 2 relay on one buffer: dispatch reads each token row, writes and
+    reads back its relay rows, writes k receive rows; combine reads k expert
+    rows, writes and reads back the per-host partials, writes one row."""
+    rho = w.h + 4 * (w.h // w.scale_group) if w.dtype == "fp8" else 2 * w.h
+    dispatch = rho * (w.T + 2 * n_relay + w.T * w.k)
+    combine = 2 * w.h * (w.T * w.k + 2 * n_relay + w.T)
+    return dispatch, combine
+
+
+def relay_measure(args, w, moe, prob, lay, ws, ids_d, x_d, xs_d, recv, recv_s, y_d, gates_d, out,
+                  stream, world, dev):
+    """Times the Mode 2 relay calls (relay layout, two-hop dispatch, two-hop
+    combine) after a flat layout of the same batch; reported beside the flat
+    step, not part of it.  Quantise-in-dispatch has no relay form."""
+    import torch
+    if w.quantize:
+        return None
+    rel = moe.Relay(prob, dev)
+    moe.moe_layout(prob, ids_d, ws, lay, stream)
+    n_relay = int(lay.host_offset[-1].item())
+    row_dtype = x_d.dtype
+    relay_rows = torch.empty((n_relay, w.h), dtype=row_dtype, device=dev)
+    relay_s = (torch.empty((n_relay, w.h // w.scale_group), dtype=torch.float32, device=dev)
+               if xs_d is not None else None)
+    partial = torch.empty((n_relay, w.h), dtype=torch.bfloat16, device=dev)
+    rel.capacity = n_relay
+
+    def relay_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_relay_layout(prob, lay, ws, rel, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.moe_dispatch_relay(prob, lay, rel, x_d, xs_d, relay_rows, relay_s, recv, recv_s, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        moe.moe_combine_relay(prob, lay, rel, y_d, gates_d, partial, out, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        relay_step()
+    rc, bits = moe.moe_status(ws, stream)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"relay device status {bits:#x}")
+    n = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(n):
+        relay_step(evs[i])
+    torch.cuda.synchronize(dev)
+    import numpy as np
+    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs]) * 1e3  # µs
+    lay_us, d_us, c_us = [max_over_ranks(v, world) for v in per.mean(axis=0).tolist()]
+    d_bytes, c_bytes = relay_bytes(w, n_relay)
+    return {"relay_rows": n_relay, "steps": n, "relay_layout_us": round(lay_us, 2),
+            "dispatch_us": round(d_us, 2), "combine_us": round(c_us, 2),
+            "algorithmic_bytes": {"dispatch": d_bytes, "combine": c_bytes},
+            "dispatch_gbs": round(d_bytes / (d_us * 1e-6) / 1e9, 1),
+            "combine_gbs": round(c_bytes / (c_us * 1e-6) / 1e9, 1),
+            "gbs": round((d_bytes + c_bytes) / ((d_us + c_us) * 1e-6) / 1e9, 1)}
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -357,6 +422,9 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     ms_step_plain = max_over_ranks(p0.elapsed_time(p1), world) / args.steps
 
+    relay = relay_measure(args, w, moe, prob, lay, ws, ids_d, x_d, xs_d, recv, recv_s, y_d, gates_d, out,
+                          stream, world, dev)
+
     d_bytes, c_bytes = algorithmic_bytes(w)
     peak, peak_src = read_peak()
     value = world * (d_bytes + c_bytes) / (ms_step * 1e-3) / 1e9
@@ -426,6 +494,7 @@ def run_ours(args, w):
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "mode2_relay": dict(relay, frac_of_peak=round(relay["gbs"] / peak, 4)) if relay else None,
         "clocks": sampler.summary(h0, h1),
     }
     if not args.no_cpu_baseline:

@@ -96,6 +96,35 @@ struct HostRoute {
     }
 };
 
+// Grouped relay hop of combine: unit = token t; lane j < k: receive row
+// pos[t, j] with weight w[t, j], and key(j) = slot_relay[t, j], the relay row
+// (one per host the token reaches) whose partial sum slot j joins.
+struct TokenRelayRoute {
+    const int32_t* pos;
+    const float* w;
+    const int32_t* slot_relay;  // [T * k]
+    int T, k;
+    int rows;                   // receive rows: T * k
+    int cap;                    // relay buffer rows
+    __device__ __forceinline__ long long units() const { return T; }
+    __device__ __forceinline__ int self_row(long long u) const { return (int)u; }
+    __device__ __forceinline__ void partner(long long u, bool live, int lane, int& row, float& wt) const {
+        row = -1;
+        wt = 0.0f;
+        if (live && lane < k) {
+            const size_t i = (size_t)u * k + lane;
+            row = pos[i];
+            wt = w[i];
+            if (row < 0 || row >= rows) row = -1;
+        }
+    }
+    __device__ __forceinline__ int key(long long u, bool live, int lane) const {
+        if (!live || lane >= k) return -1;
+        const int r = slot_relay[(size_t)u * k + lane];
+        return (r >= 0 && r < cap) ? r : -1;
+    }
+};
+
 // Relay hop between a relay row and the receive rows it feeds: unit = relay
 // row r of token t = relay_src[r]; lane j < k: receive row pos[t, j] with
 // weight w[t, j] when slot j is fed by r (slot_relay[t, j] == r).  The number
@@ -290,13 +319,15 @@ __device__ __forceinline__ void drain_stages(uint32_t bar0, const bool (&pending
         if (pending[s]) mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs);
 }
 
-// Combine: each warp owns STAGES stages of 8 rows x CHUNK bytes; a stage holds
-// the partner row pieces (at most 8) of one (unit, column chunk).
-template <int WARPS, int STAGES, int CHUNK, class Route>
+// Combine: each warp owns STAGES stages of KMAX rows x CHUNK bytes; a stage
+// holds the partner row pieces (at most KMAX) of one (unit, column chunk).
+// Plain: the partners are summed into the unit's own row.  GROUPED: partners
+// with the same key are summed into output row `key` (one sum per key, each
+// in ascending lane order).
+template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, class Route>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y,
                     uint8_t* __restrict__ out, int row_bytes) {
-    constexpr int KMAX = 8;
     constexpr int STAGE_BYTES = KMAX * CHUNK;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
@@ -317,12 +348,19 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
     long long su[STAGES];   // (unit, chunk) held by each stage
     unsigned vm[STAGES];    // partner rows of that unit that were fetched
     float wr[STAGES];       // lane j: weight of partner j of that unit
+    int kr[STAGES];         // GROUPED, lane j: output row of partner j
+    unsigned gr[STAGES];    // GROUPED, lane j: partners sharing that output row
     bool pending[STAGES];
     uint32_t ph[STAGES];
 
-    auto fetch_meta = [&](long long u, int& p, float& wv) {
+    auto fetch_meta = [&](long long u, int& p, float& wv, int& kk) {
         rt.partner(u / nch, u < units, lane, p, wv);
-        if (lane >= KMAX) p = -1;  // routes launched here have at most 8 partners
+        kk = -1;
+        if constexpr (GROUPED) {
+            kk = rt.key(u / nch, u < units, lane);
+            if (kk < 0) p = -1;
+        }
+        if (lane >= KMAX) p = -1;  // routes launched here have at most KMAX partners
     };
     // Issues the partner bulk copies of unit u into stage s (all lanes call it).
     auto issue = [&](int s, long long u, int p) -> unsigned {
@@ -342,10 +380,12 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
         su[s] = gw + s * nw;
         ph[s] = 0;
         pending[s] = su[s] < units;
-        int p;
+        int p, kk;
         float wv;
-        fetch_meta(su[s], p, wv);
+        fetch_meta(su[s], p, wv, kk);
         wr[s] = wv;
+        kr[s] = kk;
+        gr[s] = GROUPED ? __match_any_sync(0xffffffffu, p >= 0 ? kk : -1) : 0u;
         vm[s] = pending[s] ? issue(s, su[s], p) : 0u;
     }
     bool failed = false, busy = true;
@@ -356,9 +396,9 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
             if (!pending[s] || failed) continue;
             const long long u = su[s];
             const long long un = u + STAGES * nw;
-            int pn;
+            int pn, kn;
             float wn;
-            fetch_meta(un, pn, wn);  // overlaps the wait below
+            fetch_meta(un, pn, wn, kn);  // overlaps the wait below
             // give up as a warp, so that no lane runs ahead into a shuffle
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs))) {
                 failed = true;
@@ -373,20 +413,36 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) wj[j] = __shfl_sync(0xffffffffu, wr[s], j);
             const uint32_t st = stage0 + s * STAGE_BYTES;
-            uint4* orow = reinterpret_cast<uint4*>(out + (size_t)rt.self_row(ui) * row_bytes + (size_t)c * CHUNK);
-            for (int v = lane; v < cb / 16; v += 32) {
-                float acc[8];
+            // one output row per group of partners (a single group when not GROUPED)
+            unsigned rem = vm[s];
+            bool first = true;
+            while (GROUPED ? rem != 0u : first) {
+                first = false;
+                unsigned grp = rem;
+                int orow_i = rt.self_row(ui);
+                if constexpr (GROUPED) {
+                    const int lead = __ffs(rem) - 1;
+                    grp = __shfl_sync(0xffffffffu, gr[s], lead) & rem;
+                    orow_i = __shfl_sync(0xffffffffu, kr[s], lead);
+                }
+                rem &= ~grp;
+                uint4* orow = reinterpret_cast<uint4*>(out + (size_t)orow_i * row_bytes + (size_t)c * CHUNK);
+                for (int v = lane; v < cb / 16; v += 32) {
+                    float acc[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+                    for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j)
-                    if ((vm[s] >> j) & 1u) fma_bf16x8(acc, wj[j], lds_v4(st + j * CHUNK + v * 16));
-                st_v4(orow + v, pack_bf16x8(acc));
+                    for (int j = 0; j < KMAX; ++j)
+                        if ((grp >> j) & 1u) fma_bf16x8(acc, wj[j], lds_v4(st + j * CHUNK + v * 16));
+                    st_v4(orow + v, pack_bf16x8(acc));
+                }
             }
             __syncwarp();
             fence_proxy_async_smem();
             su[s] = un;
             wr[s] = wn;
+            kr[s] = kn;
+            gr[s] = GROUPED ? __match_any_sync(0xffffffffu, pn >= 0 ? kn : -1) : 0u;
             if (un < units) {
                 vm[s] = issue(s, un, pn);
                 pending[s] = true;
@@ -511,15 +567,15 @@ int grid_for(K kernel, long long units) {
 constexpr int kCombWarps = 8, kCombStages = 2, kCombChunk = 512, kCombCtasPerSm = 3;
 constexpr int kDispWarps = 4, kDispStages = 4, kDispChunk = 7168, kDispCtasPerSm = 1;
 
-template <int WARPS, int STAGES, int CHUNK, int PER_SM, class Route>
+template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, int PER_SM, class Route>
 cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, const void* y, void* out,
                                 cudaStream_t stream) {
     const int row_bytes = nvec * 16;
     const int nch = (row_bytes + CHUNK - 1) / CHUNK;
     const long long units = max_units * nch;
     if (units == 0) return cudaSuccess;
-    auto kern = combine_bulk_kernel<WARPS, STAGES, CHUNK, Route>;
-    const size_t smem = (size_t)WARPS * STAGES * 8 * CHUNK;
+    auto kern = combine_bulk_kernel<WARPS, STAGES, CHUNK, KMAX, GROUPED, Route>;
+    const size_t smem = (size_t)WARPS * STAGES * KMAX * CHUNK;
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
@@ -565,14 +621,19 @@ cudaError_t launch_combine_t(const Route& rt, long long max_units, int nvec, int
     return cudaGetLastError();
 }
 
-// Sums at most nl partner rows per unit: the bulk pipeline holds 8 per stage,
-// more go to the LSU kernel.
+// Sums at most nl partner rows per unit.  The bulk pipeline's stage holds
+// kCombStageBytes: 8 partners x 512 B, or fewer partners with longer pieces
+// so that a warp keeps the same bytes in flight; more than 8 partners go to
+// the LSU kernel.
+constexpr int kCombStageBytes = 8 * kCombChunk;
+
 template <class Route>
 cudaError_t launch_combine_route(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
                                  cudaStream_t stream) {
-    if (nl <= 8)
-        return launch_combine_bulk<kCombWarps, kCombStages, kCombChunk, kCombCtasPerSm>(rt, max_units, nvec, y, out,
-                                                                                        stream);
+    constexpr int W = kCombWarps, S = kCombStages, B = kCombStageBytes, C = kCombCtasPerSm;
+    if (nl <= 2) return launch_combine_bulk<W, S, B / 2, 2, false, C>(rt, max_units, nvec, y, out, stream);
+    if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C>(rt, max_units, nvec, y, out, stream);
+    if (nl <= 8) return launch_combine_bulk<W, S, B / 8, 8, false, C>(rt, max_units, nvec, y, out, stream);
     return launch_combine_t<8, 1>(rt, max_units, nvec, nl, y, out, stream);
 }
 
@@ -611,9 +672,16 @@ cudaError_t launch_relay_dispatch(const MoveArgs& m, const RelayArgs& r, const v
 
 cudaError_t launch_relay_combine(const MoveArgs& m, const RelayArgs& r, const void* y, const float* w, void* partial,
                                  void* out, cudaStream_t stream) {
-    // hop 1: each relay row sums the weighted expert rows of its host's slots
-    const RelaySlotRoute hop1{r.relay_src, r.slot_relay, m.pos, w, r.n_relay, m.T, m.k, m.T * m.k, r.cap};
-    cudaError_t e = launch_combine_route(hop1, relay_units_bound(m, r), m.nvec, m.k, y, partial, stream);
+    // hop 1: each token's k expert rows, summed per host into its relay rows
+    cudaError_t e;
+    if (m.k <= 8) {
+        const TokenRelayRoute hop1{m.pos, w, r.slot_relay, m.T, m.k, m.T * m.k, r.cap};
+        e = launch_combine_bulk<kCombWarps, kCombStages, kCombChunk, 8, true, kCombCtasPerSm>(hop1, m.T, m.nvec, y,
+                                                                                            partial, stream);
+    } else {
+        const RelaySlotRoute hop1{r.relay_src, r.slot_relay, m.pos, w, r.n_relay, m.T, m.k, m.T * m.k, r.cap};
+        e = launch_combine_route(hop1, relay_units_bound(m, r), m.nvec, m.k, y, partial, stream);
+    }
     if (e != cudaSuccess) return e;
     // hop 2: each token sums its relay rows in ascending host order
     const HostRoute hop2{r.relay_pos, m.T, r.H, r.cap};
