@@ -23,6 +23,9 @@ arrays through ctypes.  Each wrapper names the passage it follows:
               ("Balancing and Beyond", section 3.2): one relay row per (token,
               host), fan-out from it; per-host partial sums before the final
               sum.
+* expert_groups / dispatch_group / combine_groups -- per-expert-group
+              overlap ("Balancing and Beyond", section 3.3): the calls of one
+              expert group; combine continues one fp32 chain across groups.
 * swap_plan -- per-step intra-host expert swap ("Balancing and Beyond",
               section 3.1, Figure 2(b)): heaviest rank paired with lightest,
               one best exchange per pair, accepted if the pair's maximum falls
@@ -106,6 +109,13 @@ def _load():
         lib.oracle_relay_dispatch.restype = None
         lib.oracle_relay_combine.argtypes = [ctypes.POINTER(Problem)] + [p] * 7
         lib.oracle_relay_combine.restype = None
+        lib.oracle_expert_groups.argtypes = [ctypes.POINTER(Problem), ctypes.c_int, p]
+        lib.oracle_expert_groups.restype = ctypes.c_int
+        lib.oracle_dispatch_group.argtypes = [ctypes.POINTER(Problem), p, p, p, ctypes.c_int, p, p, p, p]
+        lib.oracle_dispatch_group.restype = None
+        lib.oracle_combine_group.argtypes = [ctypes.POINTER(Problem), p, p, p, ctypes.c_int, ctypes.c_int,
+                                             p, p, p, p]
+        lib.oracle_combine_group.restype = None
         lib.oracle_swap_plan.argtypes = [ctypes.POINTER(Problem), p, ctypes.c_int32, p, p]
         lib.oracle_swap_plan.restype = ctypes.c_int
         lib.oracle_quantize_dispatch.argtypes = [ctypes.POINTER(Problem)] + [p] * 4
@@ -263,6 +273,56 @@ def relay_combine(prob: Problem, ids, pos, relay_pos, y, w):
     lib.oracle_relay_combine(ctypes.byref(prob), _ptr(ids), _ptr(pos), _ptr(rp), _ptr(y), _ptr(w),
                              _ptr(partial), _ptr(out))
     return partial, out
+
+
+def expert_groups(prob: Problem, G: int) -> np.ndarray:
+    """Group of every expert: G contiguous runs of each rank's experts."""
+    lib = _load()
+    grp = np.zeros(prob.E, np.int32)
+    rc = lib.oracle_expert_groups(ctypes.byref(prob), int(G), _ptr(grp))
+    if rc != OK:
+        raise OracleError(rc)
+    return grp
+
+
+def dispatch_group(prob: Problem, ids, pos, group, g, x, x_scales=None, recv=None, recv_scales=None):
+    """Dispatch of group g's slots into recv (and recv_scales), in place when
+    given; returns them."""
+    lib = _load()
+    ids = np.ascontiguousarray(ids, np.int32)
+    pos = np.ascontiguousarray(pos, np.int32)
+    group = np.ascontiguousarray(group, np.int32)
+    x = np.ascontiguousarray(x)
+    S = prob.T * prob.k
+    if recv is None:
+        recv = np.zeros((S, prob.h), x.dtype)
+    if x_scales is not None:
+        x_scales = np.ascontiguousarray(x_scales, np.float32)
+        if recv_scales is None:
+            recv_scales = np.zeros((S, prob.h // prob.scale_group), np.float32)
+    lib.oracle_dispatch_group(ctypes.byref(prob), _ptr(ids), _ptr(pos), _ptr(group), int(g), _ptr(x),
+                              _ptr(x_scales), _ptr(recv), _ptr(recv_scales))
+    return recv, recv_scales
+
+
+def combine_groups(prob: Problem, ids, pos, group, G, y, w):
+    """All G group combines in order; returns (acc after each group but the
+    last as a list of fp32 arrays, out as bf16 bits)."""
+    lib = _load()
+    ids = np.ascontiguousarray(ids, np.int32)
+    pos = np.ascontiguousarray(pos, np.int32)
+    group = np.ascontiguousarray(group, np.int32)
+    y = np.ascontiguousarray(y, np.uint16)
+    w = np.ascontiguousarray(w, np.float32)
+    acc = np.zeros((prob.T, prob.h), np.float32)
+    out = np.zeros((prob.T, prob.h), np.uint16)
+    accs = []
+    for g in range(G):
+        lib.oracle_combine_group(ctypes.byref(prob), _ptr(ids), _ptr(pos), _ptr(group), g, int(G), _ptr(y),
+                                 _ptr(w), _ptr(acc), _ptr(out))
+        if g < G - 1:
+            accs.append(acc.copy())
+    return accs, out
 
 
 def swap_plan(prob: Problem, expert_count: np.ndarray, tau: int):

@@ -378,6 +378,50 @@ void oracle_relay_combine(const oracle_problem* p, const int32_t* ids, const int
         }
 }
 
+int oracle_expert_groups(const oracle_problem* p, int G, int32_t* group) {
+    Placement pl;
+    if (!make_placement(p, &pl) || G < 1) return ORACLE_ERR_INVALID;
+    std::vector<int32_t> n(pl.R, 0), li(pl.E, 0);
+    for (int e = 0; e < pl.E; ++e) li[e] = n[pl.rank_of_expert[e]]++;  // ascending e inside a rank
+    for (int e = 0; e < pl.E; ++e)
+        group[e] = (int32_t)(((int64_t)li[e] * G) / n[pl.rank_of_expert[e]]);
+    return ORACLE_OK;
+}
+
+void oracle_dispatch_group(const oracle_problem* p, const int32_t* ids, const int32_t* pos,
+                           const int32_t* group, int g, const uint8_t* x, const float* x_scales,
+                           uint8_t* recv, float* recv_scales) {
+    const size_t row = (size_t)p->h * p->elem_bytes;
+    const size_t groups = p->elem_bytes == 1 ? (size_t)(p->h / p->scale_group) : 0;
+    for (int t = 0; t < p->T; ++t)
+        for (int j = 0; j < p->k; ++j) {
+            const size_t s = (size_t)t * p->k + j;
+            if (group[ids[s]] != g) continue;
+            const size_t dst = (size_t)pos[s];
+            std::memcpy(recv + dst * row, x + (size_t)t * row, row);
+            if (groups) std::memcpy(recv_scales + dst * groups, x_scales + (size_t)t * groups, groups * 4);
+        }
+}
+
+void oracle_combine_group(const oracle_problem* p, const int32_t* ids, const int32_t* pos,
+                          const int32_t* group, int g, int G, const uint16_t* y, const float* w,
+                          float* acc, uint16_t* out) {
+    const size_t h = (size_t)p->h;
+    for (int t = 0; t < p->T; ++t)
+        for (size_t c = 0; c < h; ++c) {
+            float a = g == 0 ? 0.0f : acc[(size_t)t * h + c];
+            for (int j = 0; j < p->k; ++j) {
+                const size_t s = (size_t)t * p->k + j;
+                if (group[ids[s]] != g) continue;
+                a = std::fma(w[s], oracle_bf16_to_f32(y[(size_t)pos[s] * h + c]), a);
+            }
+            if (g == G - 1)
+                out[(size_t)t * h + c] = oracle_f32_to_bf16_rne(a);
+            else
+                acc[(size_t)t * h + c] = a;
+        }
+}
+
 int oracle_swap_plan(const oracle_problem* p, const int32_t* expert_count, int32_t tau,
                      int32_t* new_expert_to_rank, int32_t* swaps) {
     Placement pl;

@@ -125,6 +125,28 @@ void oracle_relay_combine(const oracle_problem* p, const int32_t* ids, const int
                           const int32_t* relay_pos, const uint16_t* y, const float* w,
                           uint16_t* partial, uint16_t* out);
 
+/* Per-expert-group overlap ("Balancing and Beyond", section 3.3 and its
+ * Figure 4: the experts are split into G groups, each dispatched, computed
+ * and combined in turn, so that a group's combine can overlap the next
+ * group's dispatch and every expert weight is loaded once).
+ *   expert groups: every rank's experts, in ascending e, are cut into G
+ *     contiguous runs: group(e) = floor(li(e) * G / n(rank(e))), li(e) the
+ *     index of e among its rank's experts and n(r) their number.
+ *   group dispatch g: recv[pos[t, j]] = x[t] for the slots whose expert is in
+ *     group g (scales with them); other receive rows are not written.
+ *   group combine g of G: one fp32 fma chain per token runs through the groups
+ *     in ascending g and, inside a group, the token's slots of that group in
+ *     ascending j; group 0 starts it from 0.0f, every other group continues
+ *     from acc[t]; groups before the last write the chain to acc[t] (fp32),
+ *     the last writes out[t] = bf16_rne(chain). */
+int oracle_expert_groups(const oracle_problem* p, int G, int32_t* group);
+void oracle_dispatch_group(const oracle_problem* p, const int32_t* ids, const int32_t* pos,
+                           const int32_t* group, int g, const uint8_t* x, const float* x_scales,
+                           uint8_t* recv, float* recv_scales);
+void oracle_combine_group(const oracle_problem* p, const int32_t* ids, const int32_t* pos,
+                          const int32_t* group, int g, int G, const uint16_t* y, const float* w,
+                          float* acc, uint16_t* out);
+
 /* Per-step intra-host expert swap ("Balancing and Beyond", section 3.1 and
  * its Figure 2(b)).  Load of rank r: L_r = sum of expert_count over its
  * experts.  In every host the ranks are ordered by load (descending, ties by

@@ -557,3 +557,109 @@ def test_relay_dispatch_fp8_scales_travel(oracle_mod):
     assert np.array_equal(recv, x[flat]) and np.array_equal(rcs, xs[flat])
     toks = np.nonzero(rp >= 0)[0]
     assert np.array_equal(rs[rp[rp >= 0]], xs[toks])
+
+
+# ------------------------------------------------ per-expert-group overlap
+
+@pytest.mark.parametrize("E,R,G,custom", [(128, 16, 2, False), (256, 32, 4, False), (48, 12, 4, True),
+                                          (64, 8, 1, False), (30, 6, 4, True)])
+def test_expert_groups_split_every_rank(oracle_mod, E, R, G, custom):
+    """Every rank's experts, in ascending order, form G contiguous runs whose
+    sizes differ by at most one (no run empty when the rank has >= G experts)."""
+    rng = np.random.default_rng(E + G)
+    e2r = rng.integers(0, R, size=E).astype(np.int32) if custom else None
+    prob, keep = _prob(oracle_mod, 64, E, R, 2, 2, e2r=e2r)
+    grp = oracle_mod.expert_groups(prob, G)
+    rank = e2r if custom else np.arange(E) // (E // R)
+    for r in range(R):
+        seq = grp[np.nonzero(rank == r)[0]]
+        if len(seq) == 0:
+            continue
+        assert np.all(np.diff(seq) >= 0) and seq.min() >= 0 and seq.max() < G
+        sizes = np.bincount(seq, minlength=G)
+        if len(seq) >= G:
+            assert sizes.min() >= 1
+        assert sizes.max() - sizes.min() <= 1
+
+
+def _group_case(oracle_mod, T=120, h=64, k=8, E=64, R=8, P=4, G=2, dtype="bf16", sort_by_group=False, seed=0):
+    w = mw.Workload("peo", T=T, h=h, k=k, E=E, R=R, P=P, R_src=1, dtype=dtype, seed=seed)
+    ids = mw.gen_ids(w)
+    prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, elem_bytes=1 if dtype == "fp8" else 2)
+    grp = oracle_mod.expert_groups(prob, G)
+    if sort_by_group:
+        order = np.argsort(grp[ids], axis=1, kind="stable")
+        ids = np.take_along_axis(ids, order, axis=1)
+    lay = oracle_mod.layout(prob, ids)
+    return w, ids, prob, keep, grp, lay
+
+
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_group_dispatch_partitions_flat_dispatch(oracle_mod, G):
+    """The G group dispatches write disjoint receive rows whose union is the
+    flat dispatch (bf16 and fp8 with scales)."""
+    for dtype in ("bf16", "fp8"):
+        w, ids, prob, keep, grp, lay = _group_case(oracle_mod, G=G, dtype=dtype, h=256)
+        if dtype == "fp8":
+            x, xs = mw.gen_x_fp8(w)
+            flat = (oracle_mod.dispatch(prob, lay["pos"], x, xs))
+        else:
+            x, xs = mw.gen_x_bf16(w), None
+            flat = (oracle_mod.dispatch(prob, lay["pos"], x),)
+        written = np.zeros(w.slots, np.int32)
+        recv = rs = None
+        for g in range(G):
+            before = None if recv is None else recv.copy()
+            recv, rs = oracle_mod.dispatch_group(prob, ids, lay["pos"], grp, g, x, xs, recv, rs)
+            rows = lay["pos"][grp[ids] == g]
+            written[rows] += 1
+            if before is not None:   # rows of other groups untouched
+                others = np.setdiff1d(np.arange(w.slots), rows)
+                assert np.array_equal(recv[others][written[others] == 0], before[others][written[others] == 0])
+        assert np.all(written == 1)
+        assert np.array_equal(recv, flat[0])
+        if dtype == "fp8":
+            assert np.array_equal(rs, flat[1])
+
+
+def test_group_combine_one_group_is_flat(oracle_mod):
+    w, ids, prob, keep, grp, lay = _group_case(oracle_mod, G=1, h=128)
+    y, g = mw.gen_y_host(w), mw.gen_gates(w)
+    accs, out = oracle_mod.combine_groups(prob, ids, lay["pos"], grp, 1, y, g)
+    assert accs == [] and np.array_equal(out, oracle_mod.combine(prob, lay["pos"], y, g))
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_group_combine_in_slot_order_is_flat(oracle_mod, G):
+    """When every token lists its experts group by group, the group-major
+    chain is the ascending-slot chain: bit-exact equal to the flat combine."""
+    w, ids, prob, keep, grp, lay = _group_case(oracle_mod, G=G, h=128, sort_by_group=True)
+    y, g = mw.gen_y_host(w), mw.gen_gates(w)
+    accs, out = oracle_mod.combine_groups(prob, ids, lay["pos"], grp, G, y, g)
+    assert np.array_equal(out, oracle_mod.combine(prob, lay["pos"], y, g))
+    # the fp32 accumulator after group 0 holds the sum of the group-0 terms
+    # only, within the error of an fp32 chain of k terms
+    terms = g.astype(np.float64)[:, :, None] * mw.bf16_bits_to_f32(y).astype(np.float64)[lay["pos"]]
+    in0 = (grp[ids] == 0)[:, :, None]
+    exact0 = np.where(in0, terms, 0.0).sum(axis=1)
+    bound0 = w.k * 2.0 ** -24 * np.abs(np.where(in0, terms, 0.0)).sum(axis=1)
+    assert np.all(np.abs(accs[0].astype(np.float64) - exact0) <= bound0)
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_group_combine_exact_and_bounded(oracle_mod, G):
+    """Any slot order: integer data with unit weights is exact (equal to the
+    flat combine); random data is within the fp32-chain + bf16 bound of the
+    exact sum."""
+    w, ids, prob, keep, grp, lay = _group_case(oracle_mod, G=G, h=64)
+    yi = mw.f32_to_bf16_bits(np.random.default_rng(4).integers(-30, 30, (w.slots, w.h)).astype(np.float32))
+    ones = np.ones((w.T, w.k), np.float32)
+    _, out = oracle_mod.combine_groups(prob, ids, lay["pos"], grp, G, yi, ones)
+    assert np.array_equal(out, oracle_mod.combine(prob, lay["pos"], yi, ones))
+    y, g = mw.gen_y_host(w), mw.gen_gates(w)
+    _, out = oracle_mod.combine_groups(prob, ids, lay["pos"], grp, G, y, g)
+    terms = g.astype(np.float64)[:, :, None] * mw.bf16_bits_to_f32(y).astype(np.float64)[lay["pos"]]
+    exact = terms.sum(axis=1)
+    bound = 2.0 ** -8 * np.abs(exact) + (1 + 2.0 ** -8) * w.k * 2.0 ** -24 * np.abs(terms).sum(axis=1)
+    got = mw.bf16_bits_to_f32(out).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= bound)
