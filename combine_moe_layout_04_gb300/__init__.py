@@ -6,7 +6,8 @@ mirror the C-ABI declared in ``include/moe_layout.h``:
 
     moe_workspace_bytes, moe_layout, moe_stats_words, moe_stats,
     moe_dispatch, moe_combine, moe_status, moe_status_string,
-    moe_relay_layout, moe_dispatch_relay, moe_combine_relay (the Mode 2 relay)
+    moe_relay_layout, moe_dispatch_relay, moe_combine_relay (the Mode 2 relay),
+    moe_expert_groups, moe_dispatch_group, moe_combine_group (per-expert groups)
 
 ``Problem`` and ``Layout`` are conveniences that build the C structs and
 allocate the caller-owned device buffers.  If the shared library has not been
@@ -30,6 +31,7 @@ MOE_STATUS_ID_RANGE, MOE_STATUS_ID_REPEAT, MOE_STATUS_PLACEMENT, MOE_STATUS_SRC_
 MOE_STATUS_TIMEOUT = 16
 MOE_STATUS_RELAY_CAPACITY = 32
 MOE_FP8_GROUP = 128
+MOE_MAX_GROUPS = 64
 MOE_STATS_HEADER_WORDS = 32
 MOE_FAULT_WAIT_TIMEOUT = 1
 
@@ -46,7 +48,8 @@ STATS_DST = ("recv_slots", "recv_tokens", "recv_self", "recv_local", "recv_remot
 EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
             "moe_combine", "moe_status", "moe_status_string", "moe_layout_noalloc",
             "moe_move_faults", "moe_selftest_bounded_waits", "moe_dispatch_quant", "moe_swap_plan",
-            "moe_relay_layout", "moe_dispatch_relay", "moe_combine_relay")
+            "moe_relay_layout", "moe_dispatch_relay", "moe_combine_relay",
+            "moe_expert_groups", "moe_dispatch_group", "moe_combine_group")
 
 
 class MoeLibraryMissing(RuntimeError):
@@ -116,6 +119,13 @@ def load_library(path: str = LIB_PATH):
     lib.moe_dispatch_relay.restype = i
     lib.moe_combine_relay.argtypes = [P, L, Q, vp, vp, vp, vp, vp]
     lib.moe_combine_relay.restype = i
+    i32 = ctypes.c_int32
+    lib.moe_expert_groups.argtypes = [P, i32, vp, vp]
+    lib.moe_expert_groups.restype = i
+    lib.moe_dispatch_group.argtypes = [P, L, vp, vp, i32, vp, vp, vp, vp, vp]
+    lib.moe_dispatch_group.restype = i
+    lib.moe_combine_group.argtypes = [P, L, vp, vp, i32, i32, vp, vp, vp, vp, vp]
+    lib.moe_combine_group.restype = i
     lib.moe_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.moe_status.restype = i
     lib.moe_layout_noalloc.argtypes = [P, vp, L, vp]
@@ -309,6 +319,30 @@ def moe_combine_relay(problem: Problem, layout: Layout, relay: Relay, y, weights
     _check(load_library().moe_combine_relay(ctypes.byref(problem.c()), ctypes.byref(layout.c()),
                                             ctypes.byref(relay.c()), _ptr(y), _ptr(weights), _ptr(partial),
                                             _ptr(out), _stream(stream)), "moe_combine_relay")
+
+
+def moe_expert_groups(problem: Problem, num_groups: int, expert_group, stream=None):
+    """Group of every expert: G contiguous runs of each rank's experts."""
+    _check(load_library().moe_expert_groups(ctypes.byref(problem.c()), int(num_groups), _ptr(expert_group),
+                                            _stream(stream)), "moe_expert_groups")
+
+
+def moe_dispatch_group(problem: Problem, layout: Layout, ids, expert_group, group: int, x, x_scales, recv,
+                       recv_scales, stream=None):
+    """Dispatch of the slots whose expert is in `group`."""
+    _check(load_library().moe_dispatch_group(ctypes.byref(problem.c()), ctypes.byref(layout.c()), _ptr(ids),
+                                             _ptr(expert_group), int(group), _ptr(x), _ptr(x_scales), _ptr(recv),
+                                             _ptr(recv_scales), _stream(stream)), "moe_dispatch_group")
+
+
+def moe_combine_group(problem: Problem, layout: Layout, ids, expert_group, group: int, num_groups: int, y, weights,
+                      acc, out, stream=None):
+    """Combine of one expert group; the groups continue one fp32 chain per
+    token through `acc` and the last writes `out`."""
+    _check(load_library().moe_combine_group(ctypes.byref(problem.c()), ctypes.byref(layout.c()), _ptr(ids),
+                                            _ptr(expert_group), int(group), int(num_groups), _ptr(y),
+                                            _ptr(weights), _ptr(acc), _ptr(out), _stream(stream)),
+           "moe_combine_group")
 
 
 def moe_status(workspace, stream=None):

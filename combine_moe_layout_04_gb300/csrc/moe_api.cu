@@ -270,6 +270,68 @@ int moe_combine_relay(const moe_problem* problem, const moe_layout_t* layout, co
                                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_expert_groups(const moe_problem* problem, int32_t num_groups, int32_t* expert_group,
+                      moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (num_groups < 1 || num_groups > MOE_MAX_GROUPS || expert_group == nullptr) return MOE_ERR_INVALID;
+    if (!aligned(expert_group, 4)) return MOE_ERR_ALIGN;
+    return cuda_status(moe::launch_expert_groups(problem->expert_to_rank, d.E, d.R, num_groups, expert_group,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_dispatch_group(const moe_problem* problem, const moe_layout_t* layout, const int32_t* ids,
+                       const int32_t* expert_group, int32_t group, const void* x, const float* x_scales,
+                       void* recv, float* recv_scales, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (layout == nullptr || expert_group == nullptr || group < 0 || group >= MOE_MAX_GROUPS) return MOE_ERR_INVALID;
+    if (d.T == 0) return MOE_OK;
+    if (layout->pos == nullptr || ids == nullptr || x == nullptr || recv == nullptr) return MOE_ERR_INVALID;
+    if (d.fp8 && (x_scales == nullptr || recv_scales == nullptr)) return MOE_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(layout->pos, 4) || !aligned(ids, 4) ||
+        !aligned(expert_group, 4))
+        return MOE_ERR_ALIGN;
+    if (d.fp8 && (!aligned(x_scales, 4) || !aligned(recv_scales, 4))) return MOE_ERR_ALIGN;
+    moe::MoveArgs m{};
+    m.pos = layout->pos;
+    m.T = d.T;
+    m.k = d.k;
+    m.nvec = (int)((d.fp8 ? (int64_t)d.h : 2LL * d.h) / 16);
+    const moe::GroupArgs ga{ids, expert_group, group, 0, d.E};
+    return cuda_status(moe::launch_dispatch_group(m, ga, x, x_scales, recv, recv_scales,
+                                                  d.fp8 ? d.h / MOE_FP8_GROUP : 0,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_combine_group(const moe_problem* problem, const moe_layout_t* layout, const int32_t* ids,
+                      const int32_t* expert_group, int32_t group, int32_t num_groups, const void* y,
+                      const float* weights, float* acc, void* out, moe_stream_t stream) {
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (layout == nullptr || expert_group == nullptr || num_groups < 1 || num_groups > MOE_MAX_GROUPS ||
+        group < 0 || group >= num_groups)
+        return MOE_ERR_INVALID;
+    if (d.T == 0) return MOE_OK;
+    if (layout->pos == nullptr || ids == nullptr || y == nullptr || weights == nullptr || out == nullptr ||
+        (num_groups > 1 && acc == nullptr))
+        return MOE_ERR_INVALID;
+    if (!aligned(y, 16) || !aligned(out, 16) || !aligned(acc, 16) || !aligned(weights, 4) ||
+        !aligned(layout->pos, 4) || !aligned(ids, 4) || !aligned(expert_group, 4))
+        return MOE_ERR_ALIGN;
+    moe::MoveArgs m{};
+    m.pos = layout->pos;
+    m.T = d.T;
+    m.k = d.k;
+    m.nvec = d.h / 8;  // combine is bf16 in and out
+    const moe::GroupArgs ga{ids, expert_group, group, num_groups, d.E};
+    return cuda_status(moe::launch_combine_group(m, ga, y, weights, acc, out,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream) {
     if (workspace == nullptr || status_bits == nullptr) return MOE_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -120,6 +120,13 @@ struct RelayArgs {
     int cap;
 };
 
+// One expert group of the per-expert-group calls.
+struct GroupArgs {
+    const int32_t* ids;    // [T * k]
+    const int32_t* group;  // [E] expert group
+    int g, G, E;
+};
+
 struct RelayLayoutArgs {
     const uint8_t* host_mask;    // [T][H]
     const int32_t* host_offset;  // [H+1]
@@ -373,6 +380,11 @@ cudaError_t launch_relay_dispatch(const MoveArgs& m, const RelayArgs& r, const v
 cudaError_t launch_relay_combine(const MoveArgs& m, const RelayArgs& r, const void* y, const float* w, void* partial,
                                  void* out, cudaStream_t s);
 cudaError_t launch_relay_layout(const RelayLayoutArgs& a, cudaStream_t s);
+cudaError_t launch_dispatch_group(const MoveArgs& m, const GroupArgs& ga, const void* x, const float* xs, void* recv,
+                                  float* rs, int groups, cudaStream_t s);
+cudaError_t launch_combine_group(const MoveArgs& m, const GroupArgs& ga, const void* y, const float* w, float* acc,
+                                 void* out, cudaStream_t s);
+cudaError_t launch_expert_groups(const int32_t* e2r, int E, int R, int G, int32_t* group, cudaStream_t s);
 cudaError_t read_move_faults(uint32_t* bits, cudaStream_t s);
 cudaError_t launch_swap_plan(const int32_t* count, const int32_t* e2r, int E, int R, int P, int tau,
                              int32_t* new_e2r, int32_t* swaps, cudaStream_t s);

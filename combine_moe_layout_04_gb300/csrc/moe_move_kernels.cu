@@ -37,6 +37,9 @@ constexpr int kMoveThreads = 256;
 constexpr int kMoveWarps = kMoveThreads / 32;
 constexpr unsigned kAll = 0xffffffffu;
 
+// How a combine pipeline treats an fp32 chain carried across launches.
+constexpr int kAccNone = 0, kAccFirst = 1, kAccMid = 2, kAccLast = 3;
+
 // ---- routes ------------------------------------------------------------------
 //
 // A mover walks units; unit u owns one row of its own (the row a dispatch
@@ -125,6 +128,33 @@ struct TokenRelayRoute {
     }
 };
 
+// One expert group of the flat path: unit = token t; lane j < k: receive row
+// pos[t, j] with weight w[t, j] when expert ids[t, j] is in group g.
+struct GroupSlotRoute {
+    const int32_t* pos;
+    const float* w;             // NULL for dispatch
+    const int32_t* ids;
+    const int32_t* group;       // [E]
+    int g;
+    int T, k, E;
+    int rows;                   // receive rows: T * k
+    __device__ __forceinline__ long long units() const { return T; }
+    __device__ __forceinline__ int self_row(long long u) const { return (int)u; }
+    __device__ __forceinline__ void partner(long long u, bool live, int lane, int& row, float& wt) const {
+        row = -1;
+        wt = 0.0f;
+        if (live && lane < k) {
+            const size_t i = (size_t)u * k + lane;
+            const int e = ids[i];
+            if (e >= 0 && e < E && group[e] == g) {
+                row = pos[i];
+                if (w != nullptr) wt = w[i];
+                if (row < 0 || row >= rows) row = -1;
+            }
+        }
+    }
+};
+
 // Relay hop between a relay row and the receive rows it feeds: unit = relay
 // row r of token t = relay_src[r]; lane j < k: receive row pos[t, j] with
 // weight w[t, j] when slot j is fed by r (slot_relay[t, j] == r).  The number
@@ -182,10 +212,10 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 // KB partners are gathered per round (all KB x U loads issued first), then
 // accumulated in ascending lane order; more than KB partners take several
 // rounds.  Lanes >= nl carry no partner.
-template <int KB, int U, class Route>
+template <int KB, int U, class Route, int ACC>
 __global__ void __launch_bounds__(kMoveThreads)
 combine_kernel(const Route rt, const MoveArgs m, int nl, const uint4* __restrict__ y,
-               uint4* __restrict__ out) {
+               uint4* __restrict__ out, float* __restrict__ acc_rows) {
     const int lane = threadIdx.x & 31;
     const int gwarp = blockIdx.x * kMoveWarps + (threadIdx.x >> 5);
     const int nwarps = gridDim.x * kMoveWarps;
@@ -196,13 +226,22 @@ combine_kernel(const Route rt, const MoveArgs m, int nl, const uint4* __restrict
         int p;
         float wt;
         rt.partner(ui, true, lane, p, wt);
+        if (ACC == kAccMid && __ballot_sync(kAll, p >= 0) == 0u) continue;  // acc stays
         const int v0 = c * m.chunk_vecs + lane;
         const int vend = min(m.nvec, (c + 1) * m.chunk_vecs);
+        float* arow = ACC == kAccNone ? nullptr : acc_rows + (size_t)rt.self_row(ui) * m.nvec * 8;
         float acc[U][8];
 #pragma unroll
         for (int i = 0; i < U; ++i)
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[i][q] = 0.0f;
+        if constexpr (ACC == kAccMid || ACC == kAccLast) {
+#pragma unroll
+            for (int i = 0; i < U; ++i)
+                if (v0 + 32 * i < vend)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[i][q] = arow[8 * (v0 + 32 * i) + q];
+        }
         for (int jb = 0; jb < nl; jb += KB) {
             uint4 v[KB][U];
             float wj[KB];
@@ -228,8 +267,15 @@ combine_kernel(const Route rt, const MoveArgs m, int nl, const uint4* __restrict
         }
         uint4* orow = out + (size_t)rt.self_row(ui) * m.nvec;
 #pragma unroll
-        for (int i = 0; i < U; ++i)
-            if (v0 + 32 * i < vend) st_v4(orow + v0 + 32 * i, pack_bf16x8(acc[i]));
+        for (int i = 0; i < U; ++i) {
+            if (v0 + 32 * i >= vend) continue;
+            if constexpr (ACC == kAccFirst || ACC == kAccMid) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) arow[8 * (v0 + 32 * i) + q] = acc[i][q];
+            } else {
+                st_v4(orow + v0 + 32 * i, pack_bf16x8(acc[i]));
+            }
+        }
     }
 }
 
@@ -324,11 +370,16 @@ __device__ __forceinline__ void drain_stages(uint32_t bar0, const bool (&pending
 // Plain: the partners are summed into the unit's own row.  GROUPED: partners
 // with the same key are summed into output row `key` (one sum per key, each
 // in ascending lane order).
-template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, class Route>
+//
+// ACC chains the sum across launches through an fp32 row per unit (acc, h
+// floats): kAccFirst starts from 0 and writes acc, kAccMid adds to acc (and
+// skips units with no partner), kAccLast adds to acc and writes the bf16 row.
+template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, int ACC, class Route>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y,
-                    uint8_t* __restrict__ out, int row_bytes) {
+                    uint8_t* __restrict__ out, int row_bytes, float* __restrict__ acc_rows) {
     constexpr int STAGE_BYTES = KMAX * CHUNK;
+    static_assert(ACC == kAccNone || !GROUPED, "an fp32 chain has one output row per unit");
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -426,15 +477,35 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
                     orow_i = __shfl_sync(0xffffffffu, kr[s], lead);
                 }
                 rem &= ~grp;
+                if (ACC == kAccMid && grp == 0u) break;  // nothing to add: acc stays
                 uint4* orow = reinterpret_cast<uint4*>(out + (size_t)orow_i * row_bytes + (size_t)c * CHUNK);
+                float* arow = ACC == kAccNone ? nullptr
+                                              : acc_rows + (size_t)orow_i * (row_bytes / 2) + (size_t)c * (CHUNK / 2);
                 for (int v = lane; v < cb / 16; v += 32) {
                     float acc[8];
+                    if constexpr (ACC == kAccMid || ACC == kAccLast) {
+                        const uint4 a0 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v));
+                        const uint4 a1 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v + 4));
+                        acc[0] = __uint_as_float(a0.x); acc[1] = __uint_as_float(a0.y);
+                        acc[2] = __uint_as_float(a0.z); acc[3] = __uint_as_float(a0.w);
+                        acc[4] = __uint_as_float(a1.x); acc[5] = __uint_as_float(a1.y);
+                        acc[6] = __uint_as_float(a1.z); acc[7] = __uint_as_float(a1.w);
+                    } else {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+                        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+                    }
 #pragma unroll
                     for (int j = 0; j < KMAX; ++j)
                         if ((grp >> j) & 1u) fma_bf16x8(acc, wj[j], lds_v4(st + j * CHUNK + v * 16));
-                    st_v4(orow + v, pack_bf16x8(acc));
+                    if constexpr (ACC == kAccFirst || ACC == kAccMid) {
+                        uint4* a4 = reinterpret_cast<uint4*>(arow + 8 * v);
+                        st_v4(a4, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                                             __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+                        st_v4(a4 + 1, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                                 __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+                    } else {
+                        st_v4(orow + v, pack_bf16x8(acc));
+                    }
                 }
             }
             __syncwarp();
@@ -567,14 +638,14 @@ int grid_for(K kernel, long long units) {
 constexpr int kCombWarps = 8, kCombStages = 2, kCombChunk = 512, kCombCtasPerSm = 3;
 constexpr int kDispWarps = 4, kDispStages = 4, kDispChunk = 7168, kDispCtasPerSm = 1;
 
-template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, int PER_SM, class Route>
+template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, int PER_SM, class Route, int ACC = kAccNone>
 cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, const void* y, void* out,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, float* acc = nullptr) {
     const int row_bytes = nvec * 16;
     const int nch = (row_bytes + CHUNK - 1) / CHUNK;
     const long long units = max_units * nch;
     if (units == 0) return cudaSuccess;
-    auto kern = combine_bulk_kernel<WARPS, STAGES, CHUNK, KMAX, GROUPED, Route>;
+    auto kern = combine_bulk_kernel<WARPS, STAGES, CHUNK, KMAX, GROUPED, ACC, Route>;
     const size_t smem = (size_t)WARPS * STAGES * KMAX * CHUNK;
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -583,7 +654,7 @@ cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, 
     const long long cap = (long long)sms * PER_SM;
     const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
     kern<<<grid, WARPS * 32, smem, stream>>>(rt, nch, static_cast<const uint8_t*>(y), static_cast<uint8_t*>(out),
-                                             row_bytes);
+                                             row_bytes, acc);
     return cudaGetLastError();
 }
 
@@ -606,18 +677,18 @@ cudaError_t launch_dispatch_bulk(const Route& rt, long long max_units, int row_b
     return cudaGetLastError();
 }
 
-template <int KB, int U, class Route>
+template <int KB, int U, class Route, int ACC = kAccNone>
 cudaError_t launch_combine_t(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, float* acc = nullptr) {
     MoveArgs m{};
     m.nvec = nvec;
     m.chunk_vecs = 32 * U;
     m.nchunks = (m.nvec + m.chunk_vecs - 1) / m.chunk_vecs;
     const long long units = max_units * m.nchunks;
     if (units == 0) return cudaSuccess;
-    auto kern = combine_kernel<KB, U, Route>;
+    auto kern = combine_kernel<KB, U, Route, ACC>;
     kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(rt, m, nl, static_cast<const uint4*>(y),
-                                                              static_cast<uint4*>(out));
+                                                              static_cast<uint4*>(out), acc);
     return cudaGetLastError();
 }
 
@@ -627,14 +698,14 @@ cudaError_t launch_combine_t(const Route& rt, long long max_units, int nvec, int
 // the LSU kernel.
 constexpr int kCombStageBytes = 8 * kCombChunk;
 
-template <class Route>
+template <class Route, int ACC = kAccNone>
 cudaError_t launch_combine_route(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, float* acc = nullptr) {
     constexpr int W = kCombWarps, S = kCombStages, B = kCombStageBytes, C = kCombCtasPerSm;
-    if (nl <= 2) return launch_combine_bulk<W, S, B / 2, 2, false, C>(rt, max_units, nvec, y, out, stream);
-    if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C>(rt, max_units, nvec, y, out, stream);
-    if (nl <= 8) return launch_combine_bulk<W, S, B / 8, 8, false, C>(rt, max_units, nvec, y, out, stream);
-    return launch_combine_t<8, 1>(rt, max_units, nvec, nl, y, out, stream);
+    if (nl <= 2) return launch_combine_bulk<W, S, B / 2, 2, false, C, Route, ACC>(rt, max_units, nvec, y, out, stream, acc);
+    if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C, Route, ACC>(rt, max_units, nvec, y, out, stream, acc);
+    if (nl <= 8) return launch_combine_bulk<W, S, B / 8, 8, false, C, Route, ACC>(rt, max_units, nvec, y, out, stream, acc);
+    return launch_combine_t<8, 1, Route, ACC>(rt, max_units, nvec, nl, y, out, stream, acc);
 }
 
 long long relay_units_bound(const MoveArgs& m, const RelayArgs& r) {
@@ -655,6 +726,23 @@ cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, voi
                            cudaStream_t stream) {
     const SlotRoute rt{m.pos, w, m.T, m.k, m.T * m.k};
     return launch_combine_route(rt, m.T, m.nvec, m.k, y, out, stream);
+}
+
+cudaError_t launch_dispatch_group(const MoveArgs& m, const GroupArgs& ga, const void* x, const float* xs, void* recv,
+                                  float* rs, int groups, cudaStream_t stream) {
+    const GroupSlotRoute rt{m.pos, nullptr, ga.ids, ga.group, ga.g, m.T, m.k, ga.E, m.T * m.k};
+    return launch_dispatch_bulk<kDispWarps, kDispStages, kDispChunk, kDispCtasPerSm>(rt, m.T, m.nvec * 16, x, xs, recv,
+                                                                                     rs, groups, stream);
+}
+
+cudaError_t launch_combine_group(const MoveArgs& m, const GroupArgs& ga, const void* y, const float* w, float* acc,
+                                 void* out, cudaStream_t stream) {
+    const GroupSlotRoute rt{m.pos, w, ga.ids, ga.group, ga.g, m.T, m.k, ga.E, m.T * m.k};
+    if (ga.G == 1) return launch_combine_route(rt, m.T, m.nvec, m.k, y, out, stream);
+    if (ga.g == 0) return launch_combine_route<GroupSlotRoute, kAccFirst>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
+    if (ga.g == ga.G - 1)
+        return launch_combine_route<GroupSlotRoute, kAccLast>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
+    return launch_combine_route<GroupSlotRoute, kAccMid>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
 }
 
 cudaError_t launch_relay_dispatch(const MoveArgs& m, const RelayArgs& r, const void* x, const float* xs, void* relay,

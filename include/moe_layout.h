@@ -283,6 +283,45 @@ int moe_dispatch_relay(const moe_problem* problem, const moe_layout_t* layout, c
 int moe_combine_relay(const moe_problem* problem, const moe_layout_t* layout, const moe_relay_t* relay,
                       const void* y, const float* weights, void* partial, void* out, moe_stream_t stream);
 
+/* ---- Per-expert-group calls ----------------------------------------------
+ * Per-expert overlap ("Balancing and Beyond", section 3.3 and Figure 4): the
+ * experts are split into G groups (2 or 4 on the page); each group is
+ * dispatched, computed and combined in turn, so one group's combine can run
+ * while the next group's dispatch does, and each expert's weights load once.
+ * A caller issues, per group g = 0 .. G-1, moe_dispatch_group, its expert
+ * computation and moe_combine_group, on streams of its choice.
+ *
+ * Expert groups: every rank's experts, in ascending order, are cut into G
+ * contiguous runs: group(e) = floor(li(e) * G / n(rank(e))), li(e) the index
+ * of e among its rank's experts and n(r) their number (placement of
+ * `problem`).  The page does not say how experts are grouped; this gives
+ * every rank work in every group.
+ *   expert_group: device int32 [E]; num_groups in [1, MOE_MAX_GROUPS]. */
+#define MOE_MAX_GROUPS 64
+int moe_expert_groups(const moe_problem* problem, int32_t num_groups, int32_t* expert_group,
+                      moe_stream_t stream);
+
+/* Dispatch of one expert group: recv[pos[t, j]] = x[t] (scales with it) for
+ * the slots whose expert ids[t, j] has expert_group = group; no other receive
+ * row is written.  The G groups together write what moe_dispatch writes.
+ *   ids: the [T, k] ids the layout was made from; other arguments as for
+ *   moe_dispatch. */
+int moe_dispatch_group(const moe_problem* problem, const moe_layout_t* layout, const int32_t* ids,
+                       const int32_t* expert_group, int32_t group, const void* x, const float* x_scales,
+                       void* recv, float* recv_scales, moe_stream_t stream);
+
+/* Combine of one expert group.  One fp32 fma chain per token runs through the
+ * groups in ascending order and, inside a group, through the token's slots of
+ * that group in ascending j: group 0 starts it from 0.0f; every later group
+ * continues it from acc[t]; every group but the last stores it to acc[t]
+ * (fp32), the last writes out[t] = bf16_rne(chain).  The groups must run in
+ * order.  With one group this is moe_combine.
+ *   acc: device fp32 [T, h], 16-byte aligned (may be NULL when num_groups is
+ *   1); y, weights, out as for moe_combine. */
+int moe_combine_group(const moe_problem* problem, const moe_layout_t* layout, const int32_t* ids,
+                      const int32_t* expert_group, int32_t group, int32_t num_groups, const void* y,
+                      const float* weights, float* acc, void* out, moe_stream_t stream);
+
 /* Waits for the stream, then reads the device status bits of the workspace
  * (the faults found by the last moe_layout and moe_relay_layout).
  * *status_bits receives them; returns MOE_OK, MOE_ERR_BAD_IDS,

@@ -132,3 +132,27 @@ def test_host_rejects_bad_relay_calls(moe):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_dispatch_relay(p, lay, rel, good, None, good, None, good, None, stream=0)
     assert ei.value.code == moe.MOE_ERR_INVALID
+
+
+def test_host_rejects_bad_group_calls(moe):
+    p = _p(moe)
+    lay = moe.Layout.__new__(moe.Layout)
+    for n in moe._LAYOUT_FIELDS:
+        setattr(lay, n, _Fake(0x10000))
+    good, odd, ids, grp = _Fake(0x20000), _Fake(0x20008), _Fake(0x70000), _Fake(0x71000)
+    for bad_g in (0, moe.MOE_MAX_GROUPS + 1):
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_expert_groups(p, bad_g, grp, stream=0)
+        assert ei.value.code == moe.MOE_ERR_INVALID
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_combine_group(p, lay, ids, grp, 2, 2, good, _Fake(0x30000), good, good, stream=0)  # group >= G
+    assert ei.value.code == moe.MOE_ERR_INVALID
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_combine_group(p, lay, ids, grp, 0, 2, good, _Fake(0x30000), None, good, stream=0)  # acc needed
+    assert ei.value.code == moe.MOE_ERR_INVALID
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_combine_group(p, lay, ids, grp, 0, 2, good, _Fake(0x30000), odd, good, stream=0)
+    assert ei.value.code == moe.MOE_ERR_ALIGN
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_dispatch_group(p, lay, ids, grp, 0, odd, None, good, None, stream=0)
+    assert ei.value.code == moe.MOE_ERR_ALIGN
