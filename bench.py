@@ -268,6 +268,79 @@ def relay_bytes(w, n_relay):
     return dispatch, combine
 
 
+def peo_bytes(w, ids, group, G):
+    """Per-expert-group calls: group g's dispatch reads a token row once if the
+    token has a slot in g and writes its slots of g; the combine chain reads
+    the k expert rows once, writes the fp32 accumulator after the first group,
+    reads and writes it in every middle group where the token has a slot, and
+    reads it once more before writing the bf16 row."""
+    import numpy as np
+    rho = w.h + 4 * (w.h // w.scale_group) if w.dtype == "fp8" else 2 * w.h
+    tg = group[ids]                                              # [T, k]
+    has = np.stack([(tg == g).any(axis=1) for g in range(G)])    # [G, T]
+    dispatch = rho * (int(has.sum()) + w.T * w.k)
+    mids = int(has[1:G - 1].sum()) if G > 2 else 0
+    combine = 2 * w.h * w.T * w.k + 4 * w.h * w.T + 8 * w.h * mids + (4 * w.h + 2 * w.h) * w.T
+    return dispatch, combine
+
+
+def peo_measure(args, w, moe, prob, lay, ws, ids, ids_d, x_d, xs_d, recv, recv_s, y_d, gates_d, out,
+                stream, world, dev, G):
+    """Times the per-expert-group calls (G groups), run back to back on one
+    stream and in the overlap schedule (dispatches on one stream, each group's
+    combine on a second stream once its dispatch is done, so a combine runs
+    beside the next group's dispatch).  The expert computation between a
+    group's dispatch and combine is the identity (bf16) or the fixed y buffer
+    (fp8); reported beside the flat step, not part of it."""
+    import numpy as np
+    import torch
+    if w.quantize:
+        return None
+    grp = torch.empty(w.E, dtype=torch.int32, device=dev)
+    moe.moe_expert_groups(prob, G, grp, stream)
+    acc = torch.empty((w.T, w.h), dtype=torch.float32, device=dev)
+    moe.moe_layout(prob, ids_d, ws, lay, stream)
+    side = torch.cuda.Stream(dev)
+
+    def serial():
+        for g in range(G):
+            moe.moe_dispatch_group(prob, lay, ids_d, grp, g, x_d, xs_d, recv, recv_s, stream)
+            moe.moe_combine_group(prob, lay, ids_d, grp, g, G, y_d, gates_d, acc, out, stream)
+
+    def overlapped():
+        side.wait_stream(stream)
+        for g in range(G):
+            moe.moe_dispatch_group(prob, lay, ids_d, grp, g, x_d, xs_d, recv, recv_s, stream)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            side.wait_event(ev)
+            moe.moe_combine_group(prob, lay, ids_d, grp, g, G, y_d, gates_d, acc, out, side)
+        stream.wait_stream(side)
+
+    res = {"groups": G}
+    n = min(args.steps, 200)
+    for name, fn in (("serial", serial), ("overlap", overlapped)):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name + "_us"] = round(max_over_ranks(e0.elapsed_time(e1), world) * 1e3 / n, 2)
+    rc, bits = moe.moe_status(ws, stream)
+    if rc != moe.MOE_OK:
+        raise RuntimeError(f"group device status {bits:#x}")
+    d_bytes, c_bytes = peo_bytes(w, ids, grp.cpu().numpy(), G)
+    res["steps"] = n
+    res["algorithmic_bytes"] = {"dispatch": d_bytes, "combine": c_bytes}
+    res["overlap_gbs"] = round((d_bytes + c_bytes) / (res["overlap_us"] * 1e-6) / 1e9, 1)
+    return res
+
+
 def relay_measure(args, w, moe, prob, lay, ws, ids_d, x_d, xs_d, recv, recv_s, y_d, gates_d, out,
                   stream, world, dev):
     """Times the Mode 2 relay calls (relay layout, two-hop dispatch, two-hop
@@ -425,6 +498,9 @@ def run_ours(args, w):
     relay = relay_measure(args, w, moe, prob, lay, ws, ids_d, x_d, xs_d, recv, recv_s, y_d, gates_d, out,
                           stream, world, dev)
 
+    peo = [peo_measure(args, w, moe, prob, lay, ws, ids, ids_d, x_d, xs_d, recv, recv_s, y_d, gates_d, out,
+                       stream, world, dev, G) for G in (2, 4)]
+
     d_bytes, c_bytes = algorithmic_bytes(w)
     peak, peak_src = read_peak()
     value = world * (d_bytes + c_bytes) / (ms_step * 1e-3) / 1e9
@@ -495,6 +571,7 @@ def run_ours(args, w):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "mode2_relay": dict(relay, frac_of_peak=round(relay["gbs"] / peak, 4)) if relay else None,
+        "per_expert_groups": [p for p in peo if p],
         "clocks": sampler.summary(h0, h1),
     }
     if not args.no_cpu_baseline:
