@@ -65,12 +65,16 @@ def read_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# The sources a mover's DRAM traffic depends on: its kernels and the shared
+# device helpers.  A traffic figure taken on other sources is not reported.
+MOVER_SOURCES = ("moe_move_kernels.cu", "moe_internal.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_moe_layout_04_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        if n.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, n), "rb").read())
+    for n in MOVER_SOURCES:
+        h.update(open(os.path.join(csrc, n), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -319,6 +323,18 @@ def peo_measure(args, w, moe, prob, lay, ws, ids, ids_d, x_d, xs_d, recv, recv_s
 
     res = {"groups": G}
     n = min(args.steps, 200)
+    # one serial pass with an event around every call: where the time goes
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * G + 1)]
+    for _ in range(3):
+        evs[0].record(stream)
+        for g in range(G):
+            moe.moe_dispatch_group(prob, lay, ids_d, grp, g, x_d, xs_d, recv, recv_s, stream)
+            evs[2 * g + 1].record(stream)
+            moe.moe_combine_group(prob, lay, ids_d, grp, g, G, y_d, gates_d, acc, out, stream)
+            evs[2 * g + 2].record(stream)
+        torch.cuda.synchronize(dev)
+    res["dispatch_us_per_group"] = [round(evs[2 * g].elapsed_time(evs[2 * g + 1]) * 1e3, 1) for g in range(G)]
+    res["combine_us_per_group"] = [round(evs[2 * g + 1].elapsed_time(evs[2 * g + 2]) * 1e3, 1) for g in range(G)]
     for name, fn in (("serial", serial), ("overlap", overlapped)):
         for _ in range(max(3, args.warmup)):
             fn()

@@ -529,8 +529,10 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
 
 // Dispatch: each warp owns STAGES stages of CHUNK bytes of source rows; a stage
 // holds one (unit, column chunk), written to the unit's partner rows by one
-// bulk store each.
-template <int WARPS, int STAGES, int CHUNK, class Route>
+// bulk store each.  SKIP_EMPTY (routes where many units have no partner, such
+// as one expert group): partners are looked up before the load, and a unit
+// without any is not loaded.
+template <int WARPS, int STAGES, int CHUNK, class Route, bool SKIP_EMPTY = false>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ x, const float* __restrict__ xs,
                      uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups) {
@@ -553,24 +555,36 @@ dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ 
     long long su[STAGES];
     bool pending[STAGES];
     uint32_t ph[STAGES];
-    // Lane 0 issues the bulk load of unit u into stage s.
-    auto issue = [&](int s, long long u) {
+    int pr[STAGES];  // SKIP_EMPTY: this lane's partner row of the stage's unit
+    // Issues the bulk load of unit u into stage s (lane 0); with SKIP_EMPTY
+    // (all lanes call it) returns false, loading nothing, when u has no partner.
+    auto issue = [&](int s, long long u) -> bool {
+        const long long ui = u / nch;
+        if constexpr (SKIP_EMPTY) {
+            float unused;
+            rt.partner(ui, true, lane, pr[s], unused);
+            if (__ballot_sync(0xffffffffu, pr[s] >= 0) == 0u) return false;
+        }
         if (lane == 0) {
-            const long long ui = u / nch;
             const int c = (int)(u - ui * nch);
             const int cb = min(CHUNK, row_bytes - c * CHUNK);
             mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)cb);
             bulk_g2s(stage0 + s * CHUNK, x + (size_t)rt.self_row(ui) * row_bytes + (size_t)c * CHUNK, (uint32_t)cb,
                      bar0 + 8 * s);
         }
+        return true;
+    };
+    // First unit at or after u, in this warp's stride, that needs a load.
+    auto next_loaded = [&](int s, long long u) -> long long {
+        while (u < units && !issue(s, u)) u += STAGES * nw;
+        return u;
     };
 
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
-        su[s] = gw + s * nw;
         ph[s] = 0;
+        su[s] = next_loaded(s, gw + s * nw);
         pending[s] = su[s] < units;
-        if (pending[s]) issue(s, su[s]);
     }
     bool failed = false, busy = true;
     while (busy && !failed) {
@@ -582,9 +596,11 @@ dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ 
             const long long ui = u / nch;
             const int c = (int)(u - ui * nch);
             const int cb = min(CHUNK, row_bytes - c * CHUNK);
-            int p;
-            float unused;
-            rt.partner(ui, true, lane, p, unused);
+            int p = pr[s];
+            if constexpr (!SKIP_EMPTY) {
+                float unused;
+                rt.partner(ui, true, lane, p, unused);
+            }
             // give up as a warp, so that no lane runs ahead into a shuffle
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs))) {
                 failed = true;
@@ -606,9 +622,8 @@ dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ 
             // The stage may be refilled once every lane's stores have read it.
             bulk_wait_read<0>();
             __syncwarp();
-            su[s] = u + STAGES * nw;
+            su[s] = next_loaded(s, u + STAGES * nw);
             if (su[s] < units) {
-                issue(s, su[s]);
                 pending[s] = true;
                 busy = true;
             }
@@ -658,13 +673,13 @@ cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, 
     return cudaGetLastError();
 }
 
-template <int WARPS, int STAGES, int CHUNK, int PER_SM, class Route>
+template <int WARPS, int STAGES, int CHUNK, int PER_SM, class Route, bool SKIP_EMPTY = false>
 cudaError_t launch_dispatch_bulk(const Route& rt, long long max_units, int row_bytes, const void* x, const float* xs,
                                  void* dst, float* ds, int groups, cudaStream_t stream) {
     const int nch = (row_bytes + CHUNK - 1) / CHUNK;
     const long long units = max_units * nch;
     if (units == 0) return cudaSuccess;
-    auto kern = dispatch_bulk_kernel<WARPS, STAGES, CHUNK, Route>;
+    auto kern = dispatch_bulk_kernel<WARPS, STAGES, CHUNK, Route, SKIP_EMPTY>;
     const size_t smem = (size_t)WARPS * STAGES * CHUNK;
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -702,8 +717,10 @@ template <class Route, int ACC = kAccNone>
 cudaError_t launch_combine_route(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
                                  cudaStream_t stream, float* acc = nullptr) {
     constexpr int W = kCombWarps, S = kCombStages, B = kCombStageBytes, C = kCombCtasPerSm;
-    if (nl <= 2) return launch_combine_bulk<W, S, B / 2, 2, false, C, Route, ACC>(rt, max_units, nvec, y, out, stream, acc);
-    if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C, Route, ACC>(rt, max_units, nvec, y, out, stream, acc);
+    if constexpr (ACC == kAccNone) {
+        if (nl <= 2) return launch_combine_bulk<W, S, B / 2, 2, false, C, Route>(rt, max_units, nvec, y, out, stream);
+        if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C, Route>(rt, max_units, nvec, y, out, stream);
+    }
     if (nl <= 8) return launch_combine_bulk<W, S, B / 8, 8, false, C, Route, ACC>(rt, max_units, nvec, y, out, stream, acc);
     return launch_combine_t<8, 1, Route, ACC>(rt, max_units, nvec, nl, y, out, stream, acc);
 }
@@ -731,8 +748,8 @@ cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, voi
 cudaError_t launch_dispatch_group(const MoveArgs& m, const GroupArgs& ga, const void* x, const float* xs, void* recv,
                                   float* rs, int groups, cudaStream_t stream) {
     const GroupSlotRoute rt{m.pos, nullptr, ga.ids, ga.group, ga.g, m.T, m.k, ga.E, m.T * m.k};
-    return launch_dispatch_bulk<kDispWarps, kDispStages, kDispChunk, kDispCtasPerSm>(rt, m.T, m.nvec * 16, x, xs, recv,
-                                                                                     rs, groups, stream);
+    return launch_dispatch_bulk<kDispWarps, kDispStages, kDispChunk, kDispCtasPerSm, GroupSlotRoute, true>(
+        rt, m.T, m.nvec * 16, x, xs, recv, rs, groups, stream);
 }
 
 cudaError_t launch_combine_group(const MoveArgs& m, const GroupArgs& ga, const void* y, const float* w, float* acc,
