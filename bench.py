@@ -140,15 +140,21 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "note": note}
 
 
-def dist_setup():
+def dist_setup(backend="nccl"):
+    """Rank of this replica from the torchrun environment.  Each rank works on
+    its own GPU (LOCAL_RANK); the process group only carries the barrier and
+    the max over ranks of the timings ("gloo" runs the same logic on CPU)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return world, rank, local
 
 
@@ -159,13 +165,21 @@ def barrier(world):
 
 
 def max_over_ranks(value, world):
+    """The largest value over the ranks (every rank gets it)."""
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(units_per_rank, ms_max, world):
+    """Whole-job throughput: every rank processed units_per_rank (bytes) in at
+    most ms_max milliseconds."""
+    return world * units_per_rank / (ms_max * 1e-3) / 1e9
 
 
 # ----------------------------------------------------------------- oracle (CPU)
@@ -519,7 +533,7 @@ def run_ours(args, w):
 
     d_bytes, c_bytes = algorithmic_bytes(w)
     peak, peak_src = read_peak()
-    value = world * (d_bytes + c_bytes) / (ms_step * 1e-3) / 1e9
+    value = job_value(d_bytes + c_bytes, ms_step, world)
     dc_us = dispatch_us + combine_us
     dc_gbs = (d_bytes + c_bytes) / (dc_us * 1e-6) / 1e9
     comb_gbs = c_bytes / (combine_us * 1e-6) / 1e9
