@@ -364,7 +364,10 @@ def peo_measure(args, w, moe, prob, lay, ws, ids, ids_d, x_d, xs_d, recv, recv_s
     rc, bits = moe.moe_status(ws, stream)
     if rc != moe.MOE_OK:
         raise RuntimeError(f"group device status {bits:#x}")
-    d_bytes, c_bytes = peo_bytes(w, ids, grp.cpu().numpy(), G)
+    grp_h = grp.cpu().numpy()
+    d_bytes, c_bytes = peo_bytes(w, ids, grp_h, G)
+    # routing skew makes the groups unequal: their shares of the slots
+    res["slot_share"] = [round(float(v), 3) for v in np.bincount(grp_h[ids].ravel(), minlength=G) / ids.size]
     res["steps"] = n
     res["algorithmic_bytes"] = {"dispatch": d_bytes, "combine": c_bytes}
     res["overlap_gbs"] = round((d_bytes + c_bytes) / (res["overlap_us"] * 1e-6) / 1e9, 1)

@@ -527,6 +527,199 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
     }
 }
 
+// Packed combine: a stage always holds kPackSlots pieces of kPiece bytes,
+// filled with as many column pieces of the unit's partners as fit.  A unit is
+// (output row, span of kPackSlots pieces); with n partners each stage takes
+// floor(kPackSlots / n) pieces of every partner (a round), so a unit with one
+// or two partners fills its stages as fully as one with eight.  Rounds are
+// issued in order through the warp's stages; the partners of the next unit
+// are looked up while the current unit's rounds are in flight.  ACC as for
+// combine_bulk_kernel (a round that continues an fp32 chain reads the chain's
+// values directly; bringing them through the stage left fewer slots for the
+// partners and measured slower).  At most kPackSlots partners (compacted,
+// ascending lane order, so each sum keeps the route's partner order).
+constexpr int kPiece = 512, kPackSlots = 8;
+constexpr int kCombCtasPerSmPacked = 3;  // registers capped so that 3 CTAs of 8 warps fit an SM
+
+__device__ __forceinline__ void compact_partners(int lane, int p, float w, int& cp, float& cw, int& n) {
+    const unsigned m = __ballot_sync(kAll, p >= 0);
+    n = __popc(m);
+    unsigned mm = m;
+    for (int i = 0; i < lane && i < n; ++i) mm &= mm - 1;  // lane-th partner
+    const int from = lane < n ? __ffs(mm) - 1 : 0;
+    cp = __shfl_sync(kAll, p, from);
+    cw = __shfl_sync(kAll, w, from);
+    if (lane >= n) {
+        cp = -1;
+        cw = 0.0f;
+    }
+}
+
+template <int WARPS, int STAGES, int ACC, class Route>
+__global__ void __launch_bounds__(WARPS * 32, kCombCtasPerSmPacked)
+combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __restrict__ out, int row_bytes,
+                      float* __restrict__ acc_rows) {
+    constexpr int STAGE_BYTES = kPackSlots * kPiece;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t stage0 = smem_u32(smem + (size_t)warp * STAGES * STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(&s_bar[warp][0]);
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int npieces = (row_bytes + kPiece - 1) / kPiece;      // pieces per row
+    const int nspan = (npieces + kPackSlots - 1) / kPackSlots;  // spans per row
+    const long long units = rt.units() * nspan;
+    const long long nw = (long long)gridDim.x * WARPS;
+    const long long gw = (long long)blockIdx.x * WARPS + warp;
+
+    // The unit whose rounds are being issued, and the next one.
+    struct Meta {
+        long long u;
+        int p;     // lane j < n: row of partner j
+        float w;   // lane j < n: its weight
+        int n;     // partners
+        int per;   // pieces of each partner per round
+        int rounds;
+    };
+    auto fetch = [&](long long u) {
+        Meta m;
+        m.u = u;
+        int p;
+        float w;
+        rt.partner(u / nspan, u < units, lane, p, w);
+        if (lane >= kPackSlots) p = -1;
+        compact_partners(lane, p, w, m.p, m.w, m.n);
+        const int span = (int)(u % nspan);
+        const int cnt = min(kPackSlots, npieces - span * kPackSlots);  // pieces in this span
+        m.per = m.n > 0 ? kPackSlots / m.n : kPackSlots;
+        const bool skip = ACC == kAccMid && m.n == 0;  // nothing to add: the chain stays
+        m.rounds = (u < units && !skip) ? (cnt + m.per - 1) / m.per : 0;
+        return m;
+    };
+
+    // per stage: unit, first piece, pieces, partners, weights
+    long long su[STAGES];
+    int sp0[STAGES], scnt[STAGES], sn[STAGES];
+    float sw[STAGES];
+    bool pending[STAGES];
+    uint32_t ph[STAGES];
+
+    Meta cur = fetch(gw), nxt = fetch(gw + nw);
+    int cround = 0;
+    // Skips units with no rounds; false when the warp has no item left.
+    auto settle = [&]() -> bool {
+        while (cur.u < units && cround >= cur.rounds) {
+            cur = nxt;
+            nxt = fetch(cur.u + nw);
+            cround = 0;
+        }
+        return cur.u < units;
+    };
+    // Issues the next round of the current unit into stage s (all lanes).
+    auto issue = [&](int s) {
+        const int span = (int)(cur.u % nspan);
+        const int first = span * kPackSlots + cround * cur.per;  // first piece of the round
+        const int cnt = min(cur.per, min(kPackSlots, npieces - span * kPackSlots) - cround * cur.per);
+        su[s] = cur.u;
+        sp0[s] = first;
+        scnt[s] = cnt;
+        sn[s] = cur.n;
+        sw[s] = cur.w;
+        // lane L < cnt * n copies piece first + L / n of partner L % n into slot L
+        const int j = cur.n > 0 ? lane % cur.n : 0;
+        const int pj = __shfl_sync(kAll, cur.p, j);
+        uint32_t bytes = 0;
+        for (int i = 0; i < cnt; ++i) bytes += (uint32_t)min(kPiece, row_bytes - (first + i) * kPiece);
+        if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * s, bytes * (uint32_t)cur.n);
+        __syncwarp();
+        if (lane < cnt * cur.n) {
+            const int piece = first + lane / cur.n;
+            const int pb = min(kPiece, row_bytes - piece * kPiece);
+            bulk_g2s(stage0 + s * STAGE_BYTES + lane * kPiece, y + (size_t)pj * row_bytes + (size_t)piece * kPiece,
+                     (uint32_t)pb, bar0 + 8 * s);
+        }
+        cround += 1;
+    };
+
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+        ph[s] = 0;
+        pending[s] = settle();
+        if (pending[s]) issue(s);
+    }
+    bool failed = false, busy = true;
+    while (busy && !failed) {
+        busy = false;
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            if (!pending[s] || failed) continue;
+            if (!__all_sync(kAll, mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs))) {
+                failed = true;
+                continue;
+            }
+            ph[s] += 1;
+            pending[s] = false;
+            const int n = sn[s];
+            const long long orow = rt.self_row(su[s] / nspan);
+            const uint32_t st = stage0 + s * STAGE_BYTES;
+            float wj[kPackSlots];
+#pragma unroll
+            for (int j = 0; j < kPackSlots; ++j) wj[j] = __shfl_sync(kAll, sw[s], j);
+            for (int i = 0; i < scnt[s]; ++i) {
+                const int piece = sp0[s] + i;
+                const int pb = min(kPiece, row_bytes - piece * kPiece);
+                uint4* o = reinterpret_cast<uint4*>(out + (size_t)orow * row_bytes + (size_t)piece * kPiece);
+                float* arow = ACC == kAccNone ? nullptr
+                                              : acc_rows + (size_t)orow * (row_bytes / 2) + (size_t)piece * (kPiece / 2);
+                if (lane < pb / 16) {
+                    const int v = lane;
+                    float acc[8];
+                    if constexpr (ACC == kAccMid || ACC == kAccLast) {
+                        const uint4 a0 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v));
+                        const uint4 a1 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v + 4));
+                        acc[0] = __uint_as_float(a0.x); acc[1] = __uint_as_float(a0.y);
+                        acc[2] = __uint_as_float(a0.z); acc[3] = __uint_as_float(a0.w);
+                        acc[4] = __uint_as_float(a1.x); acc[5] = __uint_as_float(a1.y);
+                        acc[6] = __uint_as_float(a1.z); acc[7] = __uint_as_float(a1.w);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < kPackSlots; ++j)
+                        if (j < n) fma_bf16x8(acc, wj[j], lds_v4(st + (i * n + j) * kPiece + v * 16));
+                    if constexpr (ACC == kAccFirst || ACC == kAccMid) {
+                        uint4* a4 = reinterpret_cast<uint4*>(arow + 8 * v);
+                        st_v4(a4, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                                             __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+                        st_v4(a4 + 1, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                                 __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+                    } else {
+                        st_v4(o + v, pack_bf16x8(acc));
+                    }
+                }
+            }
+            __syncwarp();
+            fence_proxy_async_smem();
+            if (settle()) {
+                issue(s);
+                pending[s] = true;
+                busy = true;
+            }
+        }
+    }
+    if (failed) {
+        if (lane == 0) atomicOr(&g_move_faults, kFaultWaitTimeout);
+        drain_stages<STAGES>(bar0, pending, ph);
+    }
+}
+
 // Dispatch: each warp owns STAGES stages of CHUNK bytes of source rows; a stage
 // holds one (unit, column chunk), written to the unit's partner rows by one
 // bulk store each.  SKIP_EMPTY (routes where many units have no partner, such
@@ -725,6 +918,26 @@ cudaError_t launch_combine_route(const Route& rt, long long max_units, int nvec,
     return launch_combine_t<8, 1, Route, ACC>(rt, max_units, nvec, nl, y, out, stream, acc);
 }
 
+template <int ACC, class Route>
+cudaError_t launch_combine_packed(const Route& rt, long long max_units, int nvec, const void* y, void* out,
+                                  cudaStream_t stream, float* acc = nullptr) {
+    const int row_bytes = nvec * 16;
+    const int nspan = ((row_bytes + kPiece - 1) / kPiece + kPackSlots - 1) / kPackSlots;
+    const long long units = max_units * nspan;
+    if (units == 0) return cudaSuccess;
+    constexpr int W = kCombWarps, S = kCombStages;
+    auto kern = combine_packed_kernel<W, S, ACC, Route>;
+    const size_t smem = (size_t)W * S * kPackSlots * kPiece;
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
+    const long long need = (units + W - 1) / W;
+    const long long cap = (long long)device_sm_count() * kCombCtasPerSmPacked;
+    const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
+    kern<<<grid, W * 32, smem, stream>>>(rt, static_cast<const uint8_t*>(y), static_cast<uint8_t*>(out), row_bytes,
+                                         acc);
+    return cudaGetLastError();
+}
+
 long long relay_units_bound(const MoveArgs& m, const RelayArgs& r) {
     const long long most = (long long)m.T * (m.k < r.H ? m.k : r.H);
     return most < r.cap ? most : r.cap;
@@ -756,6 +969,11 @@ cudaError_t launch_combine_group(const MoveArgs& m, const GroupArgs& ga, const v
                                  void* out, cudaStream_t stream) {
     const GroupSlotRoute rt{m.pos, w, ga.ids, ga.group, ga.g, m.T, m.k, ga.E, m.T * m.k};
     if (ga.G == 1) return launch_combine_route(rt, m.T, m.nvec, m.k, y, out, stream);
+    if (m.k <= kPackSlots) {  // a group holds about k / G of a token's slots: pack the stages
+        if (ga.g == 0) return launch_combine_packed<kAccFirst>(rt, m.T, m.nvec, y, out, stream, acc);
+        if (ga.g == ga.G - 1) return launch_combine_packed<kAccLast>(rt, m.T, m.nvec, y, out, stream, acc);
+        return launch_combine_packed<kAccMid>(rt, m.T, m.nvec, y, out, stream, acc);
+    }
     if (ga.g == 0) return launch_combine_route<GroupSlotRoute, kAccFirst>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
     if (ga.g == ga.G - 1)
         return launch_combine_route<GroupSlotRoute, kAccLast>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
