@@ -546,6 +546,8 @@ def run_ours(args, w):
     ms_step_eager = max_over_ranks(p0.elapsed_time(p1), world) / args.steps
     per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(2)] for e in evs])  # ms
     dispatch_us, combine_us = (per.mean(axis=0) * 1e3).tolist()
+    pct = {name: [round(float(v), 2) for v in np.percentile(per[:, i] * 1e3, [10, 50, 90])]
+           for i, name in enumerate(("dispatch", "combine"))}
     layout_stats_us = ms_step_eager * 1e3 - dispatch_us - combine_us
     if not torch.equal(out.view(torch.int16), out_graph.view(torch.int16)):
         raise RuntimeError("the replayed step and the eager calls disagree")
@@ -613,6 +615,9 @@ def run_ours(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_config(w),
         "dispatch_us": round(dispatch_us, 2), "combine_us": round(combine_us, 2),
+        "p10_p50_p90_us": pct,
+        "tokens_per_s": round(world * w.T / (ms_step * 1e-3), 1),
+        "tokens_per_s_dc": round(w.T / ((dispatch_us + combine_us) * 1e-6), 1),
         "layout_stats_us": round(layout_stats_us, 2), "dc_us": round(dc_us, 2),
         "ms_per_step_eager": round(ms_step_eager, 5),
         "timed_loop": "CUDA graph of the step, replayed once per step",
