@@ -2,23 +2,24 @@
 //
 // Both are HBM-bound row moves ("Poor HybridEP performance on dual-node 16x
 // B300 GPUs": dispatch_with_permute / combine_with_unpermute), so they are
-// written for bytes in flight, not for arithmetic.  Two families:
+// written for bytes in flight, not for arithmetic.
 //
-//  * bulk kernels (the default where they apply): the Blackwell copy engine
-//    (cp.async.bulk, "TMA") moves the rows.  Each warp runs its own pipeline
-//    of shared-memory stages guarded by mbarriers.  Combine gathers the k rows
-//    of one (token, column chunk) unit into a stage with k bulk copies and
-//    reduces it from shared memory; dispatch loads one x chunk and writes it
-//    to its k receive rows with k bulk stores.  Bytes in flight are bounded by
-//    shared memory (about 190 KB per SM), not by registers.  Every barrier
-//    wait has a wall-time limit; a kernel that gives up records a fault bit,
-//    drains its own copies and returns.
-//  * LSU kernels (fallback: k > 8, or buffers a bulk copy cannot address):
-//    one warp per (token, column chunk) unit with 16-byte vector loads and
-//    stores, every load of a unit issued before any is used.
+//  * bulk pipelines (every dispatch; combine with at most 8 partners): the
+//    Blackwell bulk-copy engine (cp.async.bulk, "TMA") moves the rows.  Each
+//    warp runs its own pipeline of shared-memory stages guarded by mbarriers.
+//    Combine gathers the partner pieces of one unit into a stage and reduces
+//    it from shared memory (combine_bulk_kernel; combine_packed_kernel packs
+//    several column pieces per partner into a stage when a unit has few
+//    partners); dispatch loads one source chunk and writes it to its partner
+//    rows with bulk stores.  Bytes in flight are bounded by shared memory
+//    (about 190 KB per SM), not by registers.  Every barrier wait has a
+//    wall-time limit; a kernel that gives up records a fault bit, drains its
+//    own copies and returns.
+//  * LSU combine (more than 8 partners): one warp per (unit, column chunk)
+//    with 16-byte vector loads, every load of a round issued before any is
+//    used.  Quantise-in-dispatch also uses plain vector loads and stores.
 //
-// Both walk a persistent grid over units x chunks with a tail of at most one
-// unit per warp.  Which rows a unit touches is a route (below): the flat path
+// All walk a persistent grid over units x chunks.  Which rows a unit touches is a route (below): the flat path
 // pairs a token with its k receive rows; the two hops of the Mode 2 relay pair
 // a token with its relay rows, and a relay row with the receive rows it feeds.
 // A partner row outside its buffer is skipped (dispatch) or contributes
