@@ -567,44 +567,88 @@ def run_ours(args, w):
     comb_gbs = c_bytes / (combine_us * 1e-6) / 1e9
     traffic = read_traffic("combine_kernel", w.name)
 
-    # End to end through the public API with host buffers: H2D of the step's
-    # inputs from pinned memory, the four calls, D2H of the combined output
-    # and the statistics record.
+    # End to end through the public API with host buffers: every step uploads
+    # its inputs from pinned host memory, runs the calls and downloads the
+    # combined output and the statistics record.  Steps are pipelined over two
+    # sets of device buffers and three streams (uploads, calls, downloads), as
+    # a serving loop would: the host link is full duplex, so step i's download
+    # runs beside step i+1's upload, and step i's kernels beside it too.
     e2e_steps = min(args.steps, 30)
     h_ids = torch.from_numpy(ids).pin_memory()
     h_gates = torch.from_numpy(gates).pin_memory()
     h_x = x_d.cpu().pin_memory()
     h_xs = xs_d.cpu().pin_memory() if xs_d is not None else None
     h_y = y_d.cpu().pin_memory() if fp8 else None
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_stats = torch.empty(stats.shape, dtype=stats.dtype).pin_memory()
+    h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h_stats = [torch.empty(stats.shape, dtype=stats.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_gates, h_x, h_xs, h_y) if t is not None)
-    d2h = h_out.numel() * h_out.element_size() + h_stats.numel() * h_stats.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size() + h_stats[0].numel() * h_stats[0].element_size()
 
-    def e2e_step():
-        ids_d.copy_(h_ids, non_blocking=True)
-        gates_d.copy_(h_gates, non_blocking=True)
-        x_d.copy_(h_x, non_blocking=True)
-        if h_xs is not None:
-            xs_d.copy_(h_xs, non_blocking=True)
-        if h_y is not None:
-            y_d.copy_(h_y, non_blocking=True)
-        step()
-        h_out.copy_(out, non_blocking=True)
-        h_stats.copy_(stats, non_blocking=True)
+    def device_set():
+        d = {"ids": torch.empty_like(ids_d), "gates": torch.empty_like(gates_d), "x": torch.empty_like(x_d),
+             "xs": torch.empty_like(xs_d) if xs_d is not None else None,
+             "recv": torch.empty_like(recv), "recv_s": torch.empty_like(recv_s) if recv_s is not None else None,
+             "out": torch.empty_like(out), "lay": moe.Layout(prob, dev, with_stats=True),
+             "ws": moe.alloc_workspace(prob, dev)}
+        d["y"] = torch.empty_like(y_d) if fp8 else d["recv"]
+        return d
 
-    for _ in range(2):
-        e2e_step()
+    sets = [{"ids": ids_d, "gates": gates_d, "x": x_d, "xs": xs_d, "recv": recv, "recv_s": recv_s, "out": out,
+             "lay": lay, "ws": ws, "y": y_d}, device_set()]
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of set b uploaded
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # calls on set b finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # outputs of set b downloaded
+
+    def e2e_step(i):
+        b = i % 2
+        d = sets[b]
+        s_up.wait_event(ev_done[b])  # the previous calls on set b have read its inputs
+        with torch.cuda.stream(s_up):
+            d["ids"].copy_(h_ids, non_blocking=True)
+            d["gates"].copy_(h_gates, non_blocking=True)
+            d["x"].copy_(h_x, non_blocking=True)
+            if h_xs is not None:
+                d["xs"].copy_(h_xs, non_blocking=True)
+            if h_y is not None:
+                d["y"].copy_(h_y, non_blocking=True)
+        ev_in[b].record(s_up)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])  # set b's previous outputs are on the host
+        moe.moe_layout(prob, d["ids"], d["ws"], d["lay"], stream)
+        if w.quantize:
+            moe.moe_dispatch_quant(prob, d["lay"], d["x"], d["recv"], d["recv_s"], stream)
+        else:
+            moe.moe_dispatch(prob, d["lay"], d["x"], d["xs"], d["recv"], d["recv_s"], stream)
+        moe.moe_combine(prob, d["lay"], d["y"], d["gates"], d["out"], stream)
+        ev_done[b].record(stream)
+        s_down.wait_event(ev_done[b])
+        with torch.cuda.stream(s_down):
+            h_out[b].copy_(d["out"], non_blocking=True)
+            h_stats[b].copy_(d["lay"].stats, non_blocking=True)
+        ev_out[b].record(s_down)
+
+    def e2e_run(n):
+        s_up.wait_stream(stream)
+        s_down.wait_stream(stream)
+        for i in range(n):
+            e2e_step(i)
+        stream.wait_stream(s_up)
+        stream.wait_stream(s_down)
+
+    e2e_run(2)
     barrier(world)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    if not torch.equal(sets[1]["out"].view(torch.int16), out.view(torch.int16)):
+        raise RuntimeError("the two device sets of the end-to-end loop disagree")
+    h_stats = h_stats[(e2e_steps - 1) % 2]
     st = moe.decode_stats(prob, h_stats.numpy())
 
     if rank != 0:
@@ -630,7 +674,9 @@ def run_ours(args, w):
                      "traffic": traffic, "peak_source": peak_src},
         "e2e": {"value": round(world * (d_bytes + c_bytes) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_link_gbs": round(h2d / (e2e_ms * 1e-3) / 1e9, 1),
+                "schedule": "two device buffer sets; uploads, calls and downloads on three streams"},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "mode2_relay": dict(relay, frac_of_peak=round(relay["gbs"] / peak, 4)) if relay else None,
         "per_expert_groups": [p for p in peo if p],
