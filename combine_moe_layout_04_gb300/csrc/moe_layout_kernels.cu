@@ -151,25 +151,34 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
         const unsigned long long nkey = ~((c << 32) | (unsigned)e);          // minimum via complement
         v[RMAX_EXPERT_MIN] = nkey > v[RMAX_EXPERT_MIN] ? nkey : v[RMAX_EXPERT_MIN];
     }
+    // The record goes to the workspace and, when the caller asked for it, to
+    // a.out.stats as well: every word is stored to both from registers.
     int64_t* rec = reinterpret_cast<int64_t*>(a.ws + a.wl.stats);
-    int64_t* src = rec + MOE_STATS_HEADER_WORDS;
-    int64_t* dst = src + (size_t)MOE_SRC_FIELDS * a.Rs;
+    int64_t* const copy = a.out.stats;
+    auto put = [&](size_t i, int64_t val) {
+        rec[i] = val;
+        if (copy != nullptr) copy[i] = val;
+    };
+    const size_t src = MOE_STATS_HEADER_WORDS;
+    const size_t dst = src + (size_t)MOE_SRC_FIELDS * a.Rs;
+    __shared__ int64_t s_hdr[MOE_STATS_HEADER_WORDS];
+    for (int i = tid; i < MOE_STATS_HEADER_WORDS; i += blockDim.x) s_hdr[i] = 0;
     for (int r = tid; r < a.Rs; r += blockDim.x) {
         const int64_t tok = __ldcg(ws32(a.wl.src_tokens) + r);
         const int64_t m0 = __ldcg(ws32(a.wl.src_mode0) + r);
         const int64_t m1 = __ldcg(ws32(a.wl.src_mode1) + r);
         const int64_t m2 = __ldcg(ws32(a.wl.src_mode2) + r);
-        src[MOE_SRC_TOKENS * a.Rs + r] = tok;
-        src[MOE_SRC_COPIES * a.Rs + r] = tok * a.k;
-        src[MOE_SRC_MODE0 * a.Rs + r] = m0;
-        src[MOE_SRC_MODE1 * a.Rs + r] = m1;
-        src[MOE_SRC_MODE2 * a.Rs + r] = m2;
+        put(src + MOE_SRC_TOKENS * a.Rs + r, tok);
+        put(src + MOE_SRC_COPIES * a.Rs + r, tok * a.k);
+        put(src + MOE_SRC_MODE0 * a.Rs + r, m0);
+        put(src + MOE_SRC_MODE1 * a.Rs + r, m1);
+        put(src + MOE_SRC_MODE2 * a.Rs + r, m2);
         // "tokens x k x h x 2 B" per rank and direction ("Balancing and
         // Beyond", section 1); copies x row bytes per mode (section 3.2).
-        src[MOE_SRC_NAIVE_BYTES * a.Rs + r] = tok * a.k * (int64_t)a.h * 2;
-        src[MOE_SRC_MODE0_BYTES * a.Rs + r] = m0 * a.row_bytes;
-        src[MOE_SRC_MODE1_BYTES * a.Rs + r] = m1 * a.row_bytes;
-        src[MOE_SRC_MODE2_BYTES * a.Rs + r] = m2 * a.row_bytes;
+        put(src + MOE_SRC_NAIVE_BYTES * a.Rs + r, tok * a.k * (int64_t)a.h * 2);
+        put(src + MOE_SRC_MODE0_BYTES * a.Rs + r, m0 * a.row_bytes);
+        put(src + MOE_SRC_MODE1_BYTES * a.Rs + r, m1 * a.row_bytes);
+        put(src + MOE_SRC_MODE2_BYTES * a.Rs + r, m2 * a.row_bytes);
         v[RSUM_TOK] += tok;
         v[RSUM_M0] += m0;
         v[RSUM_M1] += m1;
@@ -182,12 +191,12 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
         const int64_t tok = __ldcg(ws32(a.wl.dst_tokens) + r);
         const int64_t rem = __ldcg(ws32(a.wl.dst_remote) + r);
         const int64_t rel = __ldcg(ws32(a.wl.dst_relay) + r);
-        dst[MOE_DST_SLOTS * a.R + r] = slots;
-        dst[MOE_DST_TOKENS * a.R + r] = tok;
-        dst[MOE_DST_SELF * a.R + r] = __ldcg(ws32(a.wl.dst_self) + r);
-        dst[MOE_DST_LOCAL * a.R + r] = __ldcg(ws32(a.wl.dst_local) + r);
-        dst[MOE_DST_REMOTE * a.R + r] = rem;
-        dst[MOE_DST_RELAY * a.R + r] = rel;
+        put(dst + MOE_DST_SLOTS * a.R + r, slots);
+        put(dst + MOE_DST_TOKENS * a.R + r, tok);
+        put(dst + MOE_DST_SELF * a.R + r, __ldcg(ws32(a.wl.dst_self) + r));
+        put(dst + MOE_DST_LOCAL * a.R + r, __ldcg(ws32(a.wl.dst_local) + r));
+        put(dst + MOE_DST_REMOTE * a.R + r, rem);
+        put(dst + MOE_DST_RELAY * a.R + r, rel);
         v[RMAX_SLOTS] = max(v[RMAX_SLOTS], (unsigned long long)slots);
         v[RMAX_TOKENS] = max(v[RMAX_TOKENS], (unsigned long long)tok);
         v[RMAX_REMOTE] = max(v[RMAX_REMOTE], (unsigned long long)rem);
@@ -208,7 +217,7 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
     __syncthreads();
     if (tid == 0) {
         const unsigned long long* r = s_fin;
-        for (int i = 0; i < MOE_STATS_HEADER_WORDS; ++i) rec[i] = 0;
+        int64_t* rec = s_hdr;  // the header is built in shared memory
         const int64_t S = (int64_t)a.T * a.k;
         const int64_t emax = (int64_t)(r[RMAX_EXPERT] >> 32);
         const unsigned long long minkey = ~r[RMAX_EXPERT_MIN];
@@ -240,11 +249,8 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
         rec[MOE_ST_RANK_IMBALANCE] = __double_as_longlong(rratio);
         rec[MOE_ST_NUM_HOSTS] = a.H;
     }
-    if (a.out.stats != nullptr) {
-        // The caller asked for the record with the layout as well.
-        __syncthreads();
-        for (size_t i = tid; i < a.wl.stats_words; i += blockDim.x) a.out.stats[i] = rec[i];
-    }
+    __syncthreads();
+    for (int i = tid; i < MOE_STATS_HEADER_WORDS; i += blockDim.x) put(i, s_hdr[i]);
 }
 
 // ---- count phase -----------------------------------------------------------
@@ -663,15 +669,28 @@ __device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b) {
         if (tid == 0) {
             a.out.expert_offset[a.E] = total;
             a.out.rank_offset[a.R] = total;
+        }
+        if (warp == 0) {
+            // host counts and their exclusive scan: lane L holds hosts L and L + 32
             const int32_t* g_hcount = reinterpret_cast<const int32_t*>(a.ws + a.wl.hcount);
-            int run = 0;
-            for (int hh = 0; hh < a.H; ++hh) {
-                const int c = __ldcg(g_hcount + hh);
-                a.out.host_count[hh] = c;
-                a.out.host_offset[hh] = run;
-                run += c;
+            const int c0 = lane < a.H ? __ldcg(g_hcount + lane) : 0;
+            const int c1 = lane + 32 < a.H ? __ldcg(g_hcount + lane + 32) : 0;
+            int x0 = c0, x1 = c1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u0 = __shfl_up_sync(kFull, x0, off), u1 = __shfl_up_sync(kFull, x1, off);
+                if (lane >= off) { x0 += u0; x1 += u1; }
             }
-            a.out.host_offset[a.H] = run;
+            const int low_total = __shfl_sync(kFull, x0, 31);
+            if (lane < a.H) {
+                a.out.host_count[lane] = c0;
+                a.out.host_offset[lane] = x0 - c0;
+            }
+            if (lane + 32 < a.H) {
+                a.out.host_count[lane + 32] = c1;
+                a.out.host_offset[lane + 32] = low_total + x1 - c1;
+            }
+            if (lane == 31) a.out.host_offset[a.H] = low_total + x1;
         }
         __syncthreads();
         write_stats(a, sm.tot, sm.rfill);
