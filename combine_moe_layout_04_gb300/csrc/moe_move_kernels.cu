@@ -38,7 +38,10 @@ constexpr int kMoveThreads = 256;
 constexpr int kMoveWarps = kMoveThreads / 32;
 constexpr unsigned kAll = 0xffffffffu;
 
-// How a combine pipeline treats an fp32 chain carried across launches.
+// How a combine carries an fp32 chain across launches through an fp32 row per
+// unit (h floats): kAccFirst starts the sum from 0 and stores the chain,
+// kAccMid adds to the stored chain (and skips units with no partner),
+// kAccLast adds to it and writes the bf16 row; kAccNone is a plain combine.
 constexpr int kAccNone = 0, kAccFirst = 1, kAccMid = 2, kAccLast = 3;
 
 // ---- routes ------------------------------------------------------------------
@@ -371,16 +374,11 @@ __device__ __forceinline__ void drain_stages(uint32_t bar0, const bool (&pending
 // Plain: the partners are summed into the unit's own row.  GROUPED: partners
 // with the same key are summed into output row `key` (one sum per key, each
 // in ascending lane order).
-//
-// ACC chains the sum across launches through an fp32 row per unit (acc, h
-// floats): kAccFirst starts from 0 and writes acc, kAccMid adds to acc (and
-// skips units with no partner), kAccLast adds to acc and writes the bf16 row.
-template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, int ACC, class Route>
+template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, class Route>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y,
-                    uint8_t* __restrict__ out, int row_bytes, float* __restrict__ acc_rows) {
+                    uint8_t* __restrict__ out, int row_bytes) {
     constexpr int STAGE_BYTES = KMAX * CHUNK;
-    static_assert(ACC == kAccNone || !GROUPED, "an fp32 chain has one output row per unit");
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -478,35 +476,15 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
                     orow_i = __shfl_sync(0xffffffffu, kr[s], lead);
                 }
                 rem &= ~grp;
-                if (ACC == kAccMid && grp == 0u) break;  // nothing to add: acc stays
                 uint4* orow = reinterpret_cast<uint4*>(out + (size_t)orow_i * row_bytes + (size_t)c * CHUNK);
-                float* arow = ACC == kAccNone ? nullptr
-                                              : acc_rows + (size_t)orow_i * (row_bytes / 2) + (size_t)c * (CHUNK / 2);
                 for (int v = lane; v < cb / 16; v += 32) {
                     float acc[8];
-                    if constexpr (ACC == kAccMid || ACC == kAccLast) {
-                        const uint4 a0 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v));
-                        const uint4 a1 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v + 4));
-                        acc[0] = __uint_as_float(a0.x); acc[1] = __uint_as_float(a0.y);
-                        acc[2] = __uint_as_float(a0.z); acc[3] = __uint_as_float(a0.w);
-                        acc[4] = __uint_as_float(a1.x); acc[5] = __uint_as_float(a1.y);
-                        acc[6] = __uint_as_float(a1.z); acc[7] = __uint_as_float(a1.w);
-                    } else {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-                    }
+                    for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
 #pragma unroll
                     for (int j = 0; j < KMAX; ++j)
                         if ((grp >> j) & 1u) fma_bf16x8(acc, wj[j], lds_v4(st + j * CHUNK + v * 16));
-                    if constexpr (ACC == kAccFirst || ACC == kAccMid) {
-                        uint4* a4 = reinterpret_cast<uint4*>(arow + 8 * v);
-                        st_v4(a4, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                                             __float_as_uint(acc[2]), __float_as_uint(acc[3])));
-                        st_v4(a4 + 1, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
-                                                 __float_as_uint(acc[6]), __float_as_uint(acc[7])));
-                    } else {
-                        st_v4(orow + v, pack_bf16x8(acc));
-                    }
+                    st_v4(orow + v, pack_bf16x8(acc));
                 }
             }
             __syncwarp();
@@ -534,9 +512,9 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
 // floor(kPackSlots / n) pieces of every partner (a round), so a unit with one
 // or two partners fills its stages as fully as one with eight.  Rounds are
 // issued in order through the warp's stages; the partners of the next unit
-// are looked up while the current unit's rounds are in flight.  ACC as for
-// combine_bulk_kernel (a round that continues an fp32 chain reads the chain's
-// values directly; bringing them through the stage left fewer slots for the
+// are looked up while the current unit's rounds are in flight.  ACC carries an
+// fp32 chain across launches (kAcc*); a round reads and writes the chain's
+// values directly (bringing them through the stage left fewer slots for the
 // partners and measured slower).  At most kPackSlots partners (compacted,
 // ascending lane order, so each sum keeps the route's partner order).
 constexpr int kPiece = 512, kPackSlots = 8;
@@ -678,6 +656,10 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
                 uint4* o = reinterpret_cast<uint4*>(out + (size_t)orow * row_bytes + (size_t)piece * kPiece);
                 float* arow = ACC == kAccNone ? nullptr
                                               : acc_rows + (size_t)orow * (row_bytes / 2) + (size_t)piece * (kPiece / 2);
+                // Lane v's 8 chain values are two 16-byte halves 32 bytes apart, so a
+                // warp request fills half of each sector it touches; L2 merges the
+                // halves.  Exchanging values between lanes for fully packed requests
+                // measured slower (the shuffles sit between the wait and the refill).
                 if (lane < pb / 16) {
                     const int v = lane;
                     float acc[8];
@@ -847,14 +829,14 @@ int grid_for(K kernel, long long units) {
 constexpr int kCombWarps = 8, kCombStages = 2, kCombChunk = 512, kCombCtasPerSm = 3;
 constexpr int kDispWarps = 4, kDispStages = 4, kDispChunk = 7168, kDispCtasPerSm = 1;
 
-template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, int PER_SM, class Route, int ACC = kAccNone>
+template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, int PER_SM, class Route>
 cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, const void* y, void* out,
-                                cudaStream_t stream, float* acc = nullptr) {
+                                cudaStream_t stream) {
     const int row_bytes = nvec * 16;
     const int nch = (row_bytes + CHUNK - 1) / CHUNK;
     const long long units = max_units * nch;
     if (units == 0) return cudaSuccess;
-    auto kern = combine_bulk_kernel<WARPS, STAGES, CHUNK, KMAX, GROUPED, ACC, Route>;
+    auto kern = combine_bulk_kernel<WARPS, STAGES, CHUNK, KMAX, GROUPED, Route>;
     const size_t smem = (size_t)WARPS * STAGES * KMAX * CHUNK;
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -863,7 +845,7 @@ cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, 
     const long long cap = (long long)sms * PER_SM;
     const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
     kern<<<grid, WARPS * 32, smem, stream>>>(rt, nch, static_cast<const uint8_t*>(y), static_cast<uint8_t*>(out),
-                                             row_bytes, acc);
+                                             row_bytes);
     return cudaGetLastError();
 }
 
@@ -907,16 +889,14 @@ cudaError_t launch_combine_t(const Route& rt, long long max_units, int nvec, int
 // the LSU kernel.
 constexpr int kCombStageBytes = 8 * kCombChunk;
 
-template <class Route, int ACC = kAccNone>
+template <class Route>
 cudaError_t launch_combine_route(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
-                                 cudaStream_t stream, float* acc = nullptr) {
+                                 cudaStream_t stream) {
     constexpr int W = kCombWarps, S = kCombStages, B = kCombStageBytes, C = kCombCtasPerSm;
-    if constexpr (ACC == kAccNone) {
-        if (nl <= 2) return launch_combine_bulk<W, S, B / 2, 2, false, C, Route>(rt, max_units, nvec, y, out, stream);
-        if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C, Route>(rt, max_units, nvec, y, out, stream);
-    }
-    if (nl <= 8) return launch_combine_bulk<W, S, B / 8, 8, false, C, Route, ACC>(rt, max_units, nvec, y, out, stream, acc);
-    return launch_combine_t<8, 1, Route, ACC>(rt, max_units, nvec, nl, y, out, stream, acc);
+    if (nl <= 2) return launch_combine_bulk<W, S, B / 2, 2, false, C, Route>(rt, max_units, nvec, y, out, stream);
+    if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C, Route>(rt, max_units, nvec, y, out, stream);
+    if (nl <= 8) return launch_combine_bulk<W, S, B / 8, 8, false, C, Route>(rt, max_units, nvec, y, out, stream);
+    return launch_combine_t<8, 1, Route>(rt, max_units, nvec, nl, y, out, stream);
 }
 
 template <int ACC, class Route>
@@ -975,10 +955,11 @@ cudaError_t launch_combine_group(const MoveArgs& m, const GroupArgs& ga, const v
         if (ga.g == ga.G - 1) return launch_combine_packed<kAccLast>(rt, m.T, m.nvec, y, out, stream, acc);
         return launch_combine_packed<kAccMid>(rt, m.T, m.nvec, y, out, stream, acc);
     }
-    if (ga.g == 0) return launch_combine_route<GroupSlotRoute, kAccFirst>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
+    // more than 8 slots per token: the LSU kernel carries the chain
+    if (ga.g == 0) return launch_combine_t<8, 1, GroupSlotRoute, kAccFirst>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
     if (ga.g == ga.G - 1)
-        return launch_combine_route<GroupSlotRoute, kAccLast>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
-    return launch_combine_route<GroupSlotRoute, kAccMid>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
+        return launch_combine_t<8, 1, GroupSlotRoute, kAccLast>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
+    return launch_combine_t<8, 1, GroupSlotRoute, kAccMid>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
 }
 
 cudaError_t launch_relay_dispatch(const MoveArgs& m, const RelayArgs& r, const void* x, const float* xs, void* relay,
