@@ -142,6 +142,28 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "note": note}
 
 
+def bind_near_gpu(dev):
+    """Runs this process on the CPUs that the system lists as local to the GPU,
+    so that the pinned host buffers of the end-to-end loop are allocated in the
+    memory nearest it.  Returns the CPU list used, or None where it cannot be
+    found."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        path = f"/sys/bus/pci/devices/{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0/local_cpulist"
+        text = open(path).read().strip()
+        cpus = set()
+        for part in text.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+            return text
+    except (AttributeError, OSError, ValueError):
+        pass
+    return None
+
+
 def dist_setup(backend="nccl"):
     """Rank of this replica from the torchrun environment.  Each rank works on
     its own GPU (LOCAL_RANK); the process group only carries the barrier and
@@ -443,6 +465,7 @@ def run_ours(args, w):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    host_cpus = bind_near_gpu(dev)
     fp8 = w.dtype == "fp8"
     ids = mw.gen_ids(w)
     gates = mw.gen_gates(w)
@@ -676,7 +699,8 @@ def run_ours(args, w):
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "h2d_link_gbs": round(h2d / (e2e_ms * 1e-3) / 1e9, 1),
-                "schedule": "two device buffer sets; uploads, calls and downloads on three streams"},
+                "schedule": "two device buffer sets; uploads, calls and downloads on three streams",
+                "host_cpus": host_cpus},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "mode2_relay": dict(relay, frac_of_peak=round(relay["gbs"] / peak, 4)) if relay else None,
         "per_expert_groups": [p for p in peo if p],
