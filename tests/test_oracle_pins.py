@@ -15,6 +15,14 @@ import pytest
 import moe_workloads as mw
 
 
+def golden(name):
+    """A worked example the pages print (tests/golden/page_values.json)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "page_values.json")
+    return json.load(open(path))[name]
+
+
 def _prob(oracle, T, E, R, P, k, h=8, R_src=1, elem_bytes=2, e2r=None, src_off=None):
     return oracle.make_problem(T, h, k, E, R, P, R_src, elem_bytes, 128, e2r, src_off)
 
@@ -159,18 +167,20 @@ def test_copy_counts_tiny_value(oracle_mod):
 def test_copy_counts_deepseek_shape(oracle_mod):
     """E=256, k=8, EP32 on four hosts: c1 = 6, c2 ~ 2.7, 55 % fewer network
     copies ("Balancing and Beyond", section 3.2); uniform sample, 4 sigma."""
-    w = mw.Workload("u", T=20000, h=8, k=8, E=256, R=32, P=8, R_src=1, seed=11)
+    g = golden("dedup_deepseek")
+    E, k, R, H = g["experts"], g["topk"], g["ranks"], g["hosts"]
+    w = mw.Workload("u", T=20000, h=8, k=k, E=E, R=R, P=R // H, R_src=1, seed=11)
     ids = mw.gen_ids(w)
     prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, R_src=1)
     st = oracle_mod.stats(prob, ids)
     c1 = st["src_mode1"][0] / w.T
     c2 = st["src_mode2"][0] / w.T
-    c2_exact = float(_c2(256, 8, 4))
-    assert abs(c2_exact - 2.7107) < 1e-4
+    c2_exact = float(_c2(E, k, H))
+    assert abs(c2_exact - 2.7107) < 1e-4 and round(c2_exact, 1) == g["c2_approx"]
     # per-token variances are at most k p (1 - p) = 1.5 (c1) and 0.75 (c2)
-    assert abs(c1 - 6.0) < 4 * math.sqrt(1.5 / w.T)
+    assert abs(c1 - g["c1"]) < 4 * math.sqrt(1.5 / w.T)
     assert abs(c2 - c2_exact) < 4 * math.sqrt(0.75 / w.T)
-    assert round(1 - c2_exact / 6.0, 2) == 0.55
+    assert round(1 - c2_exact / g["c1"], 2) == g["fewer_network_bytes"]
 
 
 def test_hybridep_rdma_send_bytes(oracle_mod):
@@ -178,7 +188,10 @@ def test_hybridep_rdma_send_bytes(oracle_mod):
     local experts, top-8) prints rdma_send_bytes 117.11 MB (bf16) and 60.40 MB
     (fp8 with scales): one copy per (token, host) over all hosts.  Uniform
     routing; tolerance 3.5 sampling sigmas (0.25 MB)."""
+    g = golden("hybridep_rdma_send_bytes")
     w = mw.WORKLOADS["prefill"]
+    assert (w.T, w.h, w.R, w.R // w.P, w.E // w.R, w.k) == (g["tokens"], g["hidden"], g["ranks"], g["hosts"],
+                                                           g["local_experts"], g["topk"])
     ids = mw.gen_ids(w)
     prob, keep = _prob(oracle_mod, w.T, w.E, w.R, w.P, w.k, h=w.h, R_src=1)
     lay = oracle_mod.layout(prob, ids)
@@ -187,8 +200,8 @@ def test_hybridep_rdma_send_bytes(oracle_mod):
     st_fp8 = oracle_mod.stats(probf, ids)
     assert st_bf16["row_bytes"] == 14336 and st_fp8["row_bytes"] == 7168 + 4 * 56
     copies = int(lay["host_count"].sum())
-    assert abs(copies * st_bf16["row_bytes"] - 117.11e6) < 0.25e6
-    assert abs(copies * st_fp8["row_bytes"] - 60.40e6) < 0.13e6
+    assert abs(copies * st_bf16["row_bytes"] - g["bf16_MB"] * 1e6) < 0.25e6
+    assert abs(copies * st_fp8["row_bytes"] - g["fp8_MB"] * 1e6) < 0.13e6
 
 
 # --------------------------------------------- "Profiling when rank unbalance"
@@ -207,23 +220,25 @@ def test_p1_unbalanced_receive_counts(oracle_mod):
     """Host-0 ranks hold 384 tokens, host-1 ranks 64: a host-1 rank receives
     (384/16)*8 = 192 from host 0 and (64/16)*7 = 28 from its own host, 220 in
     all; each host-0 GPU sends 192 tokens over the network."""
-    st = _p1_case(oracle_mod, [384] * 8 + [64] * 8)
+    g = golden("unbalanced_batch")
+    st = _p1_case(oracle_mod, [g["tokens_per_rank_host0"]] * 8 + [g["tokens_per_rank_host1"]] * 8)
     for r in range(8, 16):
-        assert st["recv_remote"][r] == 192
-        assert st["recv_local"][r] == 28
-        assert st["recv_remote"][r] + st["recv_local"][r] == 220
+        assert st["recv_remote"][r] == g["host1_rank_recv_from_host0"]
+        assert st["recv_local"][r] == g["host1_rank_recv_from_own_host"]
+        assert st["recv_remote"][r] + st["recv_local"][r] == g["host1_rank_recv_total"]
     for r in range(8):
-        assert st["src_mode1"][r] == 192
+        assert st["src_mode1"][r] == g["host0_gpu_sends_unbalanced"]
 
 
 def test_p1_balanced_receive_counts(oracle_mod):
     """224 tokens per rank: (224/16)*15 = 210 received from other ranks, 112 of
     them over the network; each GPU sends 112 over the network."""
-    st = _p1_case(oracle_mod, [224] * 16)
+    g = golden("unbalanced_batch")
+    st = _p1_case(oracle_mod, [g["balanced_tokens_per_rank"]] * 16)
     for r in range(16):
-        assert st["recv_remote"][r] + st["recv_local"][r] == 210
-        assert st["recv_remote"][r] == 112
-        assert st["src_mode1"][r] == 112
+        assert st["recv_remote"][r] + st["recv_local"][r] == g["balanced_recv_from_other_ranks"]
+        assert st["recv_remote"][r] == g["balanced_recv_over_network"]
+        assert st["src_mode1"][r] == g["gpu_sends_balanced"]
 
 
 # ------------------------------------------------------------- imbalance ratio
@@ -415,15 +430,17 @@ def test_swap_plan_worked_example(oracle_mod):
     more, G1 holds e1 (30) and 70 more; swapping e0 and e1 turns 160 / 100 into
     130 / 130.  The swap is taken when tau <= 30 and refused when tau = 31."""
     # G0 = rank 0: e0 = 60, e2 = 50, e4 = 50;  G1 = rank 1: e1 = 30, e3 = 35, e5 = 35
+    g = golden("swap_example")
     e2r = np.array([0, 1, 0, 1, 0, 1], np.int32)
-    cnt = np.array([60, 30, 50, 35, 50, 35], np.int32)
+    cnt = np.array([g["e0_tokens"], g["e1_tokens"], 50, 35, 50, 35], np.int32)
+    assert list(np.bincount(e2r, weights=cnt)) == g["loads_before"]
     prob, keep = _prob(oracle_mod, 1, 6, 2, 2, 1, e2r=e2r)
     new, swaps = oracle_mod.swap_plan(prob, cnt, 30)
     a, b, x, y, old, best = swaps[0, 0]
-    assert (a, b, x, y, old, best) == (0, 1, 0, 1, 160, 130)
+    assert (a, b, x, y, old, best) == (0, 1, 0, 1, max(g["loads_before"]), max(g["loads_after"]))
     assert list(new) == [1, 0, 0, 1, 0, 1]
     loads = np.bincount(new, weights=cnt, minlength=2)
-    assert list(loads) == [130, 130]
+    assert list(loads) == g["loads_after"]
     new31, _ = oracle_mod.swap_plan(prob, cnt, 31)
     assert np.array_equal(new31, e2r)
 
