@@ -496,11 +496,17 @@ def run_ours(args, w):
     out = torch.empty((w.T, w.h), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(ev=None, s=stream):
+    # A workload whose routing is re-drawn every step (the skew sweep) cycles
+    # through all its steps' ids and gates.
+    n_route = max(1, w.steps)
+    ids_bank = [ids_d] + [torch.from_numpy(mw.gen_ids(w, step=j)).to(dev) for j in range(1, n_route)]
+    gates_bank = [gates_d] + [torch.from_numpy(mw.gen_gates(w, step=j)).to(dev) for j in range(1, n_route)]
+
+    def step(ev=None, s=stream, j=0):
         # Events bracket the two row movers: before dispatch, between dispatch
         # and combine, after combine.  Layout and statistics (written by the
         # layout call into lay.stats) take the rest of the step.
-        moe.moe_layout(prob, ids_d, ws, lay, s)
+        moe.moe_layout(prob, ids_bank[j], ws, lay, s)
         if ev is not None:
             ev[0].record(s)
         if w.quantize:
@@ -509,12 +515,12 @@ def run_ours(args, w):
             moe.moe_dispatch(prob, lay, x_d, xs_d, recv, recv_s, s)
         if ev is not None:
             ev[1].record(s)
-        moe.moe_combine(prob, lay, y_d, gates_d, out, s)
+        moe.moe_combine(prob, lay, y_d, gates_bank[j], out, s)
         if ev is not None:
             ev[2].record(s)
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(j=i % n_route)
     rc, bits = moe.moe_status(ws, stream)
     if rc != moe.MOE_OK:
         raise RuntimeError(f"device status {bits:#x}")
@@ -523,20 +529,24 @@ def run_ours(args, w):
     # layout kernel, dispatch, combine) captured once and replayed once per
     # step -- the same launches without the host's launch gaps.  The calls
     # allocate nothing and never synchronise, so they capture as they are.
-    graph = torch.cuda.CUDAGraph()
+    graphs = []
     cap = torch.cuda.Stream(dev)
     cap.wait_stream(stream)
     with torch.cuda.stream(cap):
-        graph.capture_begin()
-        step(s=cap)
-        graph.capture_end()
+        for j in range(n_route):  # one graph per routing of the cycle
+            g = torch.cuda.CUDAGraph()
+            g.capture_begin()
+            step(s=cap, j=j)
+            g.capture_end()
+            graphs.append(g)
     stream.wait_stream(cap)
-    for _ in range(args.warmup):
-        graph.replay()
+    for i in range(args.warmup):
+        graphs[i % n_route].replay()
     rc, bits = moe.moe_status(ws, stream)
     if rc != moe.MOE_OK:
         raise RuntimeError(f"device status {bits:#x} after graph replays")
     out_graph = out.clone()  # the replayed step must give what the calls give
+    j_graph = (args.warmup - 1) % n_route
 
     sampler = ClockSampler(local)
     time.sleep(0.5)
@@ -545,8 +555,8 @@ def run_ours(args, w):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     h0 = time.time()
     start.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
+    for i in range(args.steps):
+        graphs[i % n_route].replay()
     end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -563,7 +573,7 @@ def run_ours(args, w):
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     p0.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step(evs[i], j=i % n_route)
     p1.record(stream)
     torch.cuda.synchronize(dev)
     ms_step_eager = max_over_ranks(p0.elapsed_time(p1), world) / args.steps
@@ -572,9 +582,15 @@ def run_ours(args, w):
     pct = {name: [round(float(v), 2) for v in np.percentile(per[:, i] * 1e3, [10, 50, 90])]
            for i, name in enumerate(("dispatch", "combine"))}
     layout_stats_us = ms_step_eager * 1e3 - dispatch_us - combine_us
+    step(j=j_graph)
     if not torch.equal(out.view(torch.int16), out_graph.view(torch.int16)):
         raise RuntimeError("the replayed step and the eager calls disagree")
     del out_graph
+
+    ratios = []
+    for j in range(n_route):
+        moe.moe_layout(prob, ids_bank[j], ws, lay, stream)
+        ratios.append(moe.decode_stats(prob, lay.stats.cpu().numpy())["imbalance_ratio"])
 
     relay = relay_measure(args, w, moe, prob, lay, ws, ids_d, x_d, xs_d, recv, recv_s, y_d, gates_d, out,
                           stream, world, dev)
@@ -687,11 +703,13 @@ def run_ours(args, w):
         "tokens_per_s_dc": round(w.T / ((dispatch_us + combine_us) * 1e-6), 1),
         "layout_stats_us": round(layout_stats_us, 2), "dc_us": round(dc_us, 2),
         "ms_per_step_eager": round(ms_step_eager, 5),
-        "timed_loop": "CUDA graph of the step, replayed once per step",
+        "timed_loop": "CUDA graph of the step (one per routing of a re-drawn cycle), replayed once per step",
         "dc_gbs": round(dc_gbs, 1), "dc_frac_of_peak": round(dc_gbs / peak, 4),
         "step_frac_of_peak": round(value / world / peak, 4),
         "algorithmic_bytes": {"dispatch": d_bytes, "combine": c_bytes},
         "imbalance_ratio": round(st["imbalance_ratio"], 4),
+        "routing_steps": n_route,
+        "imbalance_ratio_range": [round(min(ratios), 3), round(max(ratios), 3)],
         "roofline": {"bound": "hbm", "kernel": "combine_kernel", "achieved": round(comb_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(comb_gbs / peak, 4),
                      "traffic": traffic, "peak_source": peak_src},
