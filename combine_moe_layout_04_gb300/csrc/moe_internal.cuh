@@ -316,8 +316,11 @@ inline int device_sm_count() {
 
 // Allows `kernel` at least `bytes` of dynamic shared memory on the current
 // device (the attribute is set only when it has to grow).
+// Raises the kernel's dynamic shared-memory limit to `bytes` (cached per
+// device).  Set whatever the size: a kernel's static shared memory counts
+// against the same 48 KB default, so a dynamic size below 48 KB can still need
+// the opt-in.
 inline cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
     static std::mutex mu;
     static std::unordered_map<const void*, std::unordered_map<int, size_t>> done;
     int dev = 0;
@@ -331,20 +334,23 @@ inline cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
     return e;
 }
 
-// Resident blocks per SM of `kernel` at the given block size (cached).
+// Resident blocks per SM of `kernel` at the given block size and dynamic
+// shared memory (cached per device, block size and shared-memory size).
 inline int blocks_per_sm(const void* kernel, int threads, size_t smem) {
     static std::mutex mu;
-    static std::unordered_map<const void*, std::unordered_map<int, int>> cache;
+    static std::unordered_map<const void*, std::unordered_map<unsigned long long, int>> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const unsigned long long key = ((unsigned long long)(unsigned)dev << 48) |
+                                   ((unsigned long long)(unsigned)threads << 32) | (unsigned long long)smem;
     std::lock_guard<std::mutex> lock(mu);
-    auto& per_dev = cache[kernel];
-    auto it = per_dev.find(dev);
-    if (it != per_dev.end()) return it->second;
+    auto& per_kernel = cache[kernel];
+    auto it = per_kernel.find(key);
+    if (it != per_kernel.end()) return it->second;
     int n = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) n = 0;
     n = n > 0 ? n : 1;
-    per_dev[dev] = n;
+    per_kernel[key] = n;
     return n;
 }
 

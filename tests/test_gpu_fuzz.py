@@ -13,7 +13,7 @@ from harness import Case, dev_to_bits, oracle_problem
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 40
+N_CASES = 160
 
 
 @pytest.fixture(scope="module")
