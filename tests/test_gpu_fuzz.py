@@ -50,8 +50,12 @@ def _draw(seed):
 
 @pytest.mark.parametrize("seed", range(N_CASES))
 def test_fuzz_all_calls(dev, oracle_mod, seed):
-    import torch
     w, e2r, G = _draw(seed)
+    _check_all_calls(dev, oracle_mod, w, e2r, G)
+
+
+def _check_all_calls(dev, oracle_mod, w, e2r, G):
+    import torch
     c = Case(w, dev, expert_to_rank=e2r, y_on_device=False)
     m = c.moe
     lay = m.Layout(c.prob, dev, with_stats=True)
@@ -122,3 +126,17 @@ def test_fuzz_all_calls(dev, oracle_mod, seed):
     _, out = oracle_mod.combine_groups(prob, c.ids, ref["pos"], grp_ref, G, c.y_host, c.gates)
     assert np.array_equal(dev_to_bits(c.out), out)
     assert m.moe_move_faults() == 0
+
+
+LARGE = [
+    # grids too large to be co-resident: the two-kernel layout path; relay tiles of 1024 tokens
+    (mw.Workload("large-bf16", T=150000, h=16, k=8, E=64, R=16, P=4, R_src=16, routing="zipf", zipf_s=0.8,
+                 seed=7), 2),
+    (mw.Workload("large-fp8", T=100000, h=128, k=6, E=32, R=8, P=2, R_src=1, dtype="fp8", seed=8), 4),
+]
+
+
+@pytest.mark.parametrize("w,G", LARGE, ids=[w.name for w, _ in LARGE])
+def test_large_batch_all_calls(dev, oracle_mod, w, G):
+    """Every call at 100K-150K tokens (small rows keep the oracle quick)."""
+    _check_all_calls(dev, oracle_mod, w, None, G)
