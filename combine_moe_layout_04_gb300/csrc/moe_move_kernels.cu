@@ -705,17 +705,21 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
 
 // Dispatch: each warp owns STAGES stages of CHUNK bytes of source rows; a stage
 // holds one (unit, column chunk), written to the unit's partner rows by one
-// bulk store each.  SKIP_EMPTY (routes where many units have no partner, such
-// as one expert group): partners are looked up before the load, and a unit
-// without any is not loaded.
+// bulk store each.  fp8 scale rows (`groups` floats) travel with the first
+// chunk: through the stage as one more bulk load and a bulk store per partner
+// when sbytes = 4 * groups > 0 (a multiple of 16 bytes, both arrays 16-byte
+// aligned), otherwise by plain 4-byte copies.  SKIP_EMPTY (routes where many
+// units have no partner, such as one expert group): partners are looked up
+// before the load, and a unit without any is not loaded.
 template <int WARPS, int STAGES, int CHUNK, class Route, bool SKIP_EMPTY = false>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ x, const float* __restrict__ xs,
-                     uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups) {
+                     uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups, int sbytes) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t stage0 = smem_u32(smem + (size_t)warp * STAGES * CHUNK);
+    const int stride = CHUNK + sbytes;  // a stage: the chunk, then the scale row
+    const uint32_t stage0 = smem_u32(smem + (size_t)warp * STAGES * stride);
     const uint32_t bar0 = smem_u32(&s_bar[warp][0]);
     if (lane == 0) {
 #pragma unroll
@@ -744,9 +748,12 @@ dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ 
         if (lane == 0) {
             const int c = (int)(u - ui * nch);
             const int cb = min(CHUNK, row_bytes - c * CHUNK);
-            mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)cb);
-            bulk_g2s(stage0 + s * CHUNK, x + (size_t)rt.self_row(ui) * row_bytes + (size_t)c * CHUNK, (uint32_t)cb,
-                     bar0 + 8 * s);
+            const bool with_scales = sbytes > 0 && c == 0;
+            const size_t src = (size_t)rt.self_row(ui);
+            mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(cb + (with_scales ? sbytes : 0)));
+            bulk_g2s(stage0 + s * stride, x + src * row_bytes + (size_t)c * CHUNK, (uint32_t)cb, bar0 + 8 * s);
+            if (with_scales)
+                bulk_g2s(stage0 + s * stride + CHUNK, xs + src * groups, (uint32_t)sbytes, bar0 + 8 * s);
         }
         return true;
     };
@@ -785,10 +792,14 @@ dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ 
             ph[s] += 1;
             pending[s] = false;
             fence_proxy_async_smem();
-            if (p >= 0) bulk_s2g(recv + (size_t)p * row_bytes + (size_t)c * CHUNK, stage0 + s * CHUNK, (uint32_t)cb);
+            if (p >= 0) {
+                bulk_s2g(recv + (size_t)p * row_bytes + (size_t)c * CHUNK, stage0 + s * stride, (uint32_t)cb);
+                if (sbytes > 0 && c == 0)
+                    bulk_s2g(rs + (size_t)p * groups, stage0 + s * stride + CHUNK, (uint32_t)sbytes);
+            }
             bulk_commit();
-            if (groups > 0 && c == 0) {
-                // fp8 scales: h/128 floats per row, moved with the first chunk.
+            if (groups > 0 && sbytes == 0 && c == 0) {
+                // fp8 scales that a bulk copy cannot move: plain copies with the first chunk.
                 const size_t src = (size_t)rt.self_row(ui) * groups;
                 for (unsigned mm = __ballot_sync(0xffffffffu, p >= 0); mm; mm &= mm - 1) {
                     const int pj = __shfl_sync(0xffffffffu, p, __ffs(mm) - 1);
@@ -828,6 +839,9 @@ int grid_for(K kernel, long long units) {
 // prefill-fp8 shape: warps per CTA, stages per warp, chunk bytes, CTAs per SM.
 constexpr int kCombWarps = 8, kCombStages = 2, kCombChunk = 512, kCombCtasPerSm = 3;
 constexpr int kDispWarps = 4, kDispStages = 4, kDispChunk = 7168, kDispCtasPerSm = 1;
+// Largest scale row (floats) moved through the dispatch stages: 4 x 4 stages
+// x (7168 + 4 x 1024) bytes stay within an SM's shared memory.
+constexpr int kMaxStagedScales = 1024;
 
 template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, int PER_SM, class Route>
 cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, const void* y, void* out,
@@ -856,7 +870,12 @@ cudaError_t launch_dispatch_bulk(const Route& rt, long long max_units, int row_b
     const long long units = max_units * nch;
     if (units == 0) return cudaSuccess;
     auto kern = dispatch_bulk_kernel<WARPS, STAGES, CHUNK, Route, SKIP_EMPTY>;
-    const size_t smem = (size_t)WARPS * STAGES * CHUNK;
+    // scale rows through the stages when a bulk copy can move them
+    const int sbytes = (groups > 0 && groups % 4 == 0 && groups <= kMaxStagedScales &&
+                        (reinterpret_cast<uintptr_t>(xs) & 15) == 0 && (reinterpret_cast<uintptr_t>(ds) & 15) == 0)
+                           ? 4 * groups
+                           : 0;
+    const size_t smem = (size_t)WARPS * STAGES * (CHUNK + sbytes);
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
@@ -864,7 +883,7 @@ cudaError_t launch_dispatch_bulk(const Route& rt, long long max_units, int row_b
     const long long cap = (long long)sms * PER_SM;
     const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
     kern<<<grid, WARPS * 32, smem, stream>>>(rt, nch, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(dst),
-                                             ds, row_bytes, groups);
+                                             ds, row_bytes, groups, sbytes);
     return cudaGetLastError();
 }
 
