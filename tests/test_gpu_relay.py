@@ -234,3 +234,23 @@ def test_relay_full_size(dev, oracle_mod, name):
     assert np.array_equal(dev_to_bits(case.out[torch.from_numpy(sel).to(dev)]), out_sub)
     got_part = dev_to_bits(rc.partial[torch.from_numpy(rp[sel][rp[sel] >= 0].astype(np.int64)).to(dev)])
     assert np.array_equal(got_part, part_sub[rp_sub[rp_sub >= 0]])
+
+
+def test_relay_layout_twice_after_one_layout(dev, oracle_mod):
+    """A second relay layout after the same moe_layout gives the same rows
+    (many tiles: 70000 tokens in 512-token tiles)."""
+    import torch
+    w = _small(T=70000, h=64, k=4, E=16, R=8, P=2)
+    case = Case(w, dev, y_on_device=False)
+    rc = RelayCase(case)
+    m = case.moe
+    m.moe_layout(case.prob, case.ids_d, case.ws, case.lay)
+    m.moe_relay_layout(case.prob, case.lay, case.ws, rc.rel)
+    first = rc.rel.relay_pos.clone()
+    rc.rel.relay_pos.fill_(-9)
+    m.moe_relay_layout(case.prob, case.lay, case.ws, rc.rel)
+    code, bits = m.moe_status(case.ws)
+    assert code == 0 and bits == 0
+    assert torch.equal(rc.rel.relay_pos, first)
+    prob, keep = oracle_problem(oracle_mod, w)
+    assert np.array_equal(first.cpu().numpy(), oracle_mod.relay_layout(prob, case.ids))
