@@ -321,6 +321,8 @@ def peo_bytes(w, ids, group, G):
     tg = group[ids]                                              # [T, k]
     has = np.stack([(tg == g).any(axis=1) for g in range(G)])    # [G, T]
     dispatch = rho * (int(has.sum()) + w.T * w.k)
+    if G == 1:  # one group: a plain combine, no fp32 chain
+        return dispatch, 2 * w.h * w.T * w.k + 2 * w.h * w.T
     mids = int(has[1:G - 1].sum()) if G > 2 else 0
     combine = 2 * w.h * w.T * w.k + 4 * w.h * w.T + 8 * w.h * mids + (4 * w.h + 2 * w.h) * w.T
     return dispatch, combine
