@@ -59,8 +59,8 @@ bool make_sources(const oracle_problem* p, std::vector<int32_t>* src_of_token) {
     return true;
 }
 
-// Top-k ids must be k distinct experts in [0, E) ("k distinct experts",
-// "Balancing and Beyond" section 3.2).
+// Top-k ids must be k distinct experts in [0, E): the routing model of
+// "Balancing and Beyond", section 3.2 draws distinct experts per token.
 bool ids_valid(const oracle_problem* p, const int32_t* ids) {
     for (int t = 0; t < p->T; ++t) {
         for (int j = 0; j < p->k; ++j) {
