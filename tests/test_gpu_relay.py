@@ -131,6 +131,7 @@ RELAY_CASES = [
     _small(T=333, h=1024, k=8, E=256, R=128, P=2, dtype="fp8"),       # 64 hosts (two host words per lane)
     _small(T=200, k=16, E=64, R=32, P=2),                             # k > 8: the LSU combine, 16 hosts
     _small(T=96, k=32, E=64, R=64, P=1),                              # largest top-k, 32+ hosts per token
+    _small(T=128, k=32, E=1024, R=1024, P=16, R_src=64),             # the largest E, R, hosts and top-k together
     _small(T=5000, h=64, k=2, E=8, R=4, P=2),                         # several relay tiles, ragged tail
     _small(T=70000, h=64, k=2, E=8, R=4, P=2),                        # 512-token relay tiles
 ]
