@@ -1,6 +1,6 @@
 """Benchmark: one MoE layer's layout + stats + dispatch + combine on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--tokens T] [--impl ours|reference]
 
 A step is one pass of the whole hot path over one batch: moe_layout (which
 also writes the statistics record), moe_dispatch and moe_combine, inputs
@@ -739,10 +739,17 @@ def main():
     ap.add_argument("--workload", default="prefill-fp8")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="run the workload with this many tokens instead (a smaller case of the same kernels, "
+                         "for profiling); the line names it <workload>@T<tokens>")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     import moe_workloads as mw
     w = mw.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        if args.tokens <= 0 or args.tokens % w.R_src:
+            ap.error(f"--tokens must be a positive multiple of the {w.R_src} source ranks of {w.name}")
+        w = mw.scaled(w, T=args.tokens, name=f"{w.name}@T{args.tokens}")
     if args.impl == "reference":
         run_reference(args, w)
     else:

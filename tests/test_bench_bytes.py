@@ -1,6 +1,8 @@
 """The bench's algorithmic byte counts, checked on CPU against the sizes the
 workloads imply (no GPU)."""
+import json
 import os
+import subprocess
 import sys
 
 import numpy as np
@@ -47,3 +49,18 @@ def test_group_bytes():
     rows_read = sum(int((group2[ids] == g).any(axis=1).sum()) for g in range(2))
     assert d == rho * (rows_read + w.T * w.k)
     assert c == 2 * w.h * w.T * w.k + 10 * w.h * w.T
+
+
+def test_tokens_option_runs_a_smaller_case():
+    """--tokens runs the same workload with fewer tokens and names it so (the
+    oracle arm, which needs no GPU); a count the source ranks do not divide
+    is refused."""
+    bench = os.path.join(ROOT, "bench.py")
+    p = subprocess.run([sys.executable, bench, "--impl", "reference", "--workload", "prefill-fp8", "--tokens", "256",
+                        "--steps", "2", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    d = json.loads(p.stdout.strip().splitlines()[-1])
+    assert d["config"]["workload"] == "prefill-fp8@T256" and d["config"]["T"] == 256
+    p = subprocess.run([sys.executable, bench, "--impl", "reference", "--workload", "decode-EP32-r8", "--tokens", "100"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert p.returncode != 0 and "multiple of the 32 source ranks" in p.stderr
