@@ -32,6 +32,7 @@ MOE_STATUS_TIMEOUT = 16
 MOE_STATUS_RELAY_CAPACITY = 32
 MOE_FP8_GROUP = 128
 MOE_MAX_GROUPS = 64
+MOE_MAX_HIDDEN = 1 << 20
 MOE_STATS_HEADER_WORDS = 32
 MOE_FAULT_WAIT_TIMEOUT = 1
 

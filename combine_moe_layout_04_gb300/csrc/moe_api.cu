@@ -24,7 +24,7 @@ int check_problem(const moe_problem* p, Dims* d) {
     d->R = p->num_ranks; d->P = p->ranks_per_host; d->Rs = p->num_src_ranks;
     d->fp8 = p->dtype == MOE_DTYPE_FP8_E4M3;
     if (p->dtype != MOE_DTYPE_BF16 && p->dtype != MOE_DTYPE_FP8_E4M3) return MOE_ERR_INVALID;
-    if (d->T < 0 || d->h <= 0) return MOE_ERR_INVALID;
+    if (d->T < 0 || d->h <= 0 || d->h > MOE_MAX_HIDDEN) return MOE_ERR_INVALID;
     if (d->k < 1 || d->k > MOE_MAX_TOPK) return MOE_ERR_INVALID;
     if (d->E < 1 || d->E > MOE_MAX_EXPERTS) return MOE_ERR_INVALID;
     if (d->R < 1 || d->R > MOE_MAX_RANKS || d->P < 1 || d->R % d->P != 0) return MOE_ERR_INVALID;

@@ -79,10 +79,11 @@ typedef enum {
 #define MOE_MAX_EXPERTS  1024
 #define MOE_MAX_RANKS    1024
 #define MOE_MAX_HOSTS    64
+#define MOE_MAX_HIDDEN   (1 << 20)  /* columns of a row: row bytes stay far inside int32 */
 #define MOE_FP8_GROUP    128   /* columns per fp32 scale */
 
 /* The problem, fixed for one layer.  Sizes:
- *   num_tokens T >= 0, hidden h > 0 (bf16: h % 8 == 0; fp8: h % 128 == 0),
+ *   num_tokens T >= 0, hidden h in [1, 2^20] (bf16: h % 8 == 0; fp8: h % 128 == 0),
  *   topk k in [1, 32], num_experts E in [1, 1024], num_ranks R in [1, 1024],
  *   ranks_per_host P with R % P == 0 and R / P <= 64,
  *   num_src_ranks R_src in [1, R], T * k < 2^31.

@@ -56,7 +56,8 @@ def _p(moe, **kw):
     dict(topk=0), dict(topk=33), dict(num_experts=1025), dict(num_ranks=3, ranks_per_host=2),
     dict(num_ranks=1024, ranks_per_host=8), dict(num_src_ranks=5), dict(num_experts=18),
     dict(num_tokens=250), dict(hidden=1020), dict(dtype=1, hidden=1000), dict(dtype=7),
-    dict(num_tokens=1 << 28, topk=8, num_src_ranks=1), dict(num_tokens=-1)])
+    dict(num_tokens=1 << 28, topk=8, num_src_ranks=1), dict(num_tokens=-1),
+    dict(hidden=(1 << 20) + 8), dict(hidden=1 << 30), dict(dtype=1, hidden=(1 << 20) + 128)])
 def test_host_rejects_bad_problems(moe, bad):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_workspace_bytes(_p(moe, **bad))
