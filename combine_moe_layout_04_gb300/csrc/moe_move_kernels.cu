@@ -224,6 +224,7 @@ combine_kernel(const Route rt, const MoveArgs m, int nl, const uint4* __restrict
     const int gwarp = blockIdx.x * kMoveWarps + (threadIdx.x >> 5);
     const int nwarps = gridDim.x * kMoveWarps;
     const long long units = rt.units() * m.nchunks;
+    const uint64_t ypol = l2_evict_first_policy();  // y rows are read once
     for (long long u = gwarp; u < units; u += nwarps) {
         const long long ui = u / m.nchunks;
         const int c = (int)(u - ui * m.nchunks);
@@ -258,7 +259,7 @@ combine_kernel(const Route rt, const MoveArgs m, int nl, const uint4* __restrict
 #pragma unroll
                 for (int i = 0; i < U; ++i) {
                     v[j][i] = make_uint4(0u, 0u, 0u, 0u);
-                    if (use && v0 + 32 * i < vend) v[j][i] = ld_stream_v4(src + v0 + 32 * i);
+                    if (use && v0 + 32 * i < vend) v[j][i] = ld_stream_v4_hint(src + v0 + 32 * i, ypol);
                 }
                 if (!use) wj[j] = 0.0f;
             }
@@ -384,6 +385,7 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t stage0 = smem_u32(smem + (size_t)warp * STAGES * STAGE_BYTES);
     const uint32_t bar0 = smem_u32(&s_bar[warp][0]);
+    const uint64_t ypol = l2_evict_first_policy();  // y rows are read once
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -420,8 +422,8 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
         if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(__popc(mask) * cb));
         __syncwarp();
         if (p >= 0)
-            bulk_g2s(stage0 + s * STAGE_BYTES + lane * CHUNK,
-                     y + (size_t)p * row_bytes + (size_t)c * CHUNK, (uint32_t)cb, bar0 + 8 * s);
+            bulk_g2s_hint(stage0 + s * STAGE_BYTES + lane * CHUNK,
+                          y + (size_t)p * row_bytes + (size_t)c * CHUNK, (uint32_t)cb, bar0 + 8 * s, ypol);
         return mask;
     };
 
@@ -544,6 +546,7 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t stage0 = smem_u32(smem + (size_t)warp * STAGES * STAGE_BYTES);
     const uint32_t bar0 = smem_u32(&s_bar[warp][0]);
+    const uint64_t ypol = l2_evict_first_policy();  // y rows are read once
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -620,8 +623,8 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
         if (lane < cnt * cur.n) {
             const int piece = first + lane / cur.n;
             const int pb = min(kPiece, row_bytes - piece * kPiece);
-            bulk_g2s(stage0 + s * STAGE_BYTES + lane * kPiece, y + (size_t)pj * row_bytes + (size_t)piece * kPiece,
-                     (uint32_t)pb, bar0 + 8 * s);
+            bulk_g2s_hint(stage0 + s * STAGE_BYTES + lane * kPiece,
+                          y + (size_t)pj * row_bytes + (size_t)piece * kPiece, (uint32_t)pb, bar0 + 8 * s, ypol);
         }
         cround += 1;
     };
