@@ -421,9 +421,16 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
         const unsigned mask = __ballot_sync(0xffffffffu, p >= 0);
         if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(__popc(mask) * cb));
         __syncwarp();
-        if (p >= 0)
-            bulk_g2s_hint(stage0 + s * STAGE_BYTES + lane * CHUNK,
-                          y + (size_t)p * row_bytes + (size_t)c * CHUNK, (uint32_t)cb, bar0 + 8 * s, ypol);
+        if (p >= 0) {
+            const uint8_t* src = y + (size_t)p * row_bytes + (size_t)c * CHUNK;
+            // The grouped pass (relay hop 1) loads plainly: the partial rows it
+            // writes are read back by the next pass, and they stay in L2 more
+            // often that way (1 % faster relay step on GB300).
+            if constexpr (GROUPED)
+                bulk_g2s(stage0 + s * STAGE_BYTES + lane * CHUNK, src, (uint32_t)cb, bar0 + 8 * s);
+            else
+                bulk_g2s_hint(stage0 + s * STAGE_BYTES + lane * CHUNK, src, (uint32_t)cb, bar0 + 8 * s, ypol);
+        }
         return mask;
     };
 
