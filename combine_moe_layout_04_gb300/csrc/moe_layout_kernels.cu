@@ -132,10 +132,34 @@ enum { RMAX_EXPERT = 0, RMAX_EXPERT_MIN, RMAX_SRC_M1, RMAX_SRC_M2, RMAX_SLOTS, R
        RMAX_REMOTE, RMAX_RELAY, RSUM_TOK, RSUM_M0, RSUM_M1, RSUM_M2, R_COUNT };
 constexpr int kMaxStatWarps = 32;
 
+// Counters of the statistics record that thread tid reads from the workspace
+// (source rank tid, destination rank tid, and for warp 0 the host counts of
+// lanes L and L + 32).  The statistics block loads them as soon as they are
+// complete, so that their latency overlaps its other loads; counters of
+// ranks past the block size are read where they are used.
+struct StatIn {
+    int32_t src[4];  // tokens, mode 0, 1, 2 copies of source rank tid
+    int32_t dst[5];  // tokens, self, local, remote, relay of destination rank tid
+    int32_t hc0, hc1;
+};
+
+__device__ __forceinline__ void load_stat_inputs(const LayoutArgs& a, StatIn& in) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int32_t* src = reinterpret_cast<const int32_t*>(a.ws + a.wl.src_tokens);  // 4 blocks of R_src
+    const int32_t* dst = reinterpret_cast<const int32_t*>(a.ws + a.wl.dst_tokens);  // 5 blocks of R
+    const int32_t* hc = reinterpret_cast<const int32_t*>(a.ws + a.wl.hcount);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) in.src[i] = tid < a.Rs ? __ldcg(src + (size_t)i * a.Rs + tid) : 0;
+#pragma unroll
+    for (int i = 0; i < 5; ++i) in.dst[i] = tid < a.R ? __ldcg(dst + (size_t)i * a.R + tid) : 0;
+    in.hc0 = tid < 32 && lane < a.H ? __ldcg(hc + lane) : 0;
+    in.hc1 = tid < 32 && lane + 32 < a.H ? __ldcg(hc + lane + 32) : 0;
+}
+
 // The statistics record of a layout, written into the workspace by one whole
 // block once the counters are complete.  ecount / rcount: expert and rank
-// slot counts (any memory the block can read).
-__device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const int32_t* rcount) {
+// slot counts (any memory the block can read); in: load_stat_inputs.
+__device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const int32_t* rcount, const StatIn& in) {
     __shared__ unsigned long long s_red[R_COUNT][kMaxStatWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = (blockDim.x + 31) >> 5;
@@ -164,10 +188,11 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
     __shared__ int64_t s_hdr[MOE_STATS_HEADER_WORDS];
     for (int i = tid; i < MOE_STATS_HEADER_WORDS; i += blockDim.x) s_hdr[i] = 0;
     for (int r = tid; r < a.Rs; r += blockDim.x) {
-        const int64_t tok = __ldcg(ws32(a.wl.src_tokens) + r);
-        const int64_t m0 = __ldcg(ws32(a.wl.src_mode0) + r);
-        const int64_t m1 = __ldcg(ws32(a.wl.src_mode1) + r);
-        const int64_t m2 = __ldcg(ws32(a.wl.src_mode2) + r);
+        const bool mine = r == tid;  // loaded by load_stat_inputs
+        const int64_t tok = mine ? in.src[0] : __ldcg(ws32(a.wl.src_tokens) + r);
+        const int64_t m0 = mine ? in.src[1] : __ldcg(ws32(a.wl.src_mode0) + r);
+        const int64_t m1 = mine ? in.src[2] : __ldcg(ws32(a.wl.src_mode1) + r);
+        const int64_t m2 = mine ? in.src[3] : __ldcg(ws32(a.wl.src_mode2) + r);
         put(src + MOE_SRC_TOKENS * a.Rs + r, tok);
         put(src + MOE_SRC_COPIES * a.Rs + r, tok * a.k);
         put(src + MOE_SRC_MODE0 * a.Rs + r, m0);
@@ -187,14 +212,17 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
         v[RMAX_SRC_M2] = max(v[RMAX_SRC_M2], (unsigned long long)m2);
     }
     for (int r = tid; r < a.R; r += blockDim.x) {
+        const bool mine = r == tid;  // loaded by load_stat_inputs
         const int64_t slots = rcount[r];
-        const int64_t tok = __ldcg(ws32(a.wl.dst_tokens) + r);
-        const int64_t rem = __ldcg(ws32(a.wl.dst_remote) + r);
-        const int64_t rel = __ldcg(ws32(a.wl.dst_relay) + r);
+        const int64_t tok = mine ? in.dst[0] : __ldcg(ws32(a.wl.dst_tokens) + r);
+        const int64_t self = mine ? in.dst[1] : __ldcg(ws32(a.wl.dst_self) + r);
+        const int64_t local = mine ? in.dst[2] : __ldcg(ws32(a.wl.dst_local) + r);
+        const int64_t rem = mine ? in.dst[3] : __ldcg(ws32(a.wl.dst_remote) + r);
+        const int64_t rel = mine ? in.dst[4] : __ldcg(ws32(a.wl.dst_relay) + r);
         put(dst + MOE_DST_SLOTS * a.R + r, slots);
         put(dst + MOE_DST_TOKENS * a.R + r, tok);
-        put(dst + MOE_DST_SELF * a.R + r, __ldcg(ws32(a.wl.dst_self) + r));
-        put(dst + MOE_DST_LOCAL * a.R + r, __ldcg(ws32(a.wl.dst_local) + r));
+        put(dst + MOE_DST_SELF * a.R + r, self);
+        put(dst + MOE_DST_LOCAL * a.R + r, local);
         put(dst + MOE_DST_REMOTE * a.R + r, rem);
         put(dst + MOE_DST_RELAY * a.R + r, rel);
         v[RMAX_SLOTS] = max(v[RMAX_SLOTS], (unsigned long long)slots);
@@ -561,6 +589,8 @@ __device__ void rank_prologue(const LayoutArgs& a, const RankSmem& sm, int b) {
 __device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b) {
     __shared__ int32_t s_warp[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    StatIn stat_in = {};
+    if (b == a.wl.blocks) load_stat_inputs(a, stat_in);  // complete: every block's counts are published
     const int S = a.T * a.k;
     const SlotRange sr = slot_range(a, b);
     const int32_t* g_group = reinterpret_cast<const int32_t*>(a.ws + a.wl.group);
@@ -672,9 +702,7 @@ __device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b) {
         }
         if (warp == 0) {
             // host counts and their exclusive scan: lane L holds hosts L and L + 32
-            const int32_t* g_hcount = reinterpret_cast<const int32_t*>(a.ws + a.wl.hcount);
-            const int c0 = lane < a.H ? __ldcg(g_hcount + lane) : 0;
-            const int c1 = lane + 32 < a.H ? __ldcg(g_hcount + lane + 32) : 0;
+            const int c0 = stat_in.hc0, c1 = stat_in.hc1;
             int x0 = c0, x1 = c1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -693,7 +721,7 @@ __device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b) {
             if (lane == 31) a.out.host_offset[a.H] = low_total + x1;
         }
         __syncthreads();
-        write_stats(a, sm.tot, sm.rfill);
+        write_stats(a, sm.tot, sm.rfill, stat_in);
         return;
     }
 
@@ -760,8 +788,10 @@ __global__ void layout_empty_kernel(const LayoutArgs a) {
         if (hh < a.H) a.out.host_count[hh] = 0;
         a.out.host_offset[hh] = 0;
     }
+    StatIn in;
+    load_stat_inputs(a, in);
     __syncthreads();
-    write_stats(a, a.out.expert_count, a.out.rank_count);
+    write_stats(a, a.out.expert_count, a.out.rank_count, in);
 }
 
 // Copies the statistics record out of the workspace (one small block; it
