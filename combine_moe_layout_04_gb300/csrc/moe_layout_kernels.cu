@@ -112,19 +112,19 @@ __device__ __forceinline__ void warp_count(int32_t* counters, int key) {
 
 // ---- statistics ----------------------------------------------------------
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(kFull, v, off);
-        v = o > v ? o : v;
-    }
-    return v;
+// Warp maximum of 64-bit keys by two 32-bit hardware reductions: the largest
+// high word, then the largest low word among the lanes that hold it.
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long v) {
+    const unsigned hi = (unsigned)(v >> 32), lo = (unsigned)v;
+    const unsigned mh = __reduce_max_sync(kFull, hi);
+    const unsigned ml = __reduce_max_sync(kFull, hi == mh ? lo : 0u);
+    return ((unsigned long long)mh << 32) | ml;
 }
 
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-    return v;
+// Warp sum of per-lane partial sums that, like their total, stay below 2^32
+// (every statistic summed is at most T * k < 2^31).
+__device__ __forceinline__ unsigned long long warp_sum_small(unsigned long long v) {
+    return __reduce_add_sync(kFull, (unsigned)v);
 }
 
 // Reductions of the statistics: maxima (of key values) and sums.
@@ -167,6 +167,8 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
 #pragma unroll
     for (int i = 0; i < R_COUNT; ++i) v[i] = 0ull;
     auto ws32 = [&](size_t off) { return reinterpret_cast<const int32_t*>(a.ws + off); };
+    // The status word for the record: its load overlaps the work below.
+    const unsigned status = tid == 0 ? __ldcg(reinterpret_cast<const unsigned*>(a.ws + a.wl.status)) : 0u;
 
     for (int e = tid; e < a.E; e += blockDim.x) {
         const unsigned long long c = (unsigned)ecount[e];
@@ -232,7 +234,7 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
     }
 #pragma unroll
     for (int i = 0; i < R_COUNT; ++i) {
-        const unsigned long long w = i < RSUM_TOK ? warp_max_u64(v[i]) : warp_sum_u64(v[i]);
+        const unsigned long long w = i < RSUM_TOK ? warp_max_key(v[i]) : warp_sum_small(v[i]);
         if (lane == 0) s_red[i][warp] = w;
     }
     __syncthreads();
@@ -243,13 +245,21 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
         s_fin[tid] = x;
     }
     __syncthreads();
+    const int64_t S = (int64_t)a.T * a.k;
+    if (tid < 2) {
+        // Imbalance ratios, one per thread: busiest expert over the layer mean
+        // T*k/E ("Balancing and Beyond", section 2), and the same for ranks.
+        const double top = tid == 0 ? (double)(int64_t)(s_fin[RMAX_EXPERT] >> 32) : (double)s_fin[RMAX_SLOTS];
+        const double parts = tid == 0 ? (double)a.E : (double)a.R;
+        const double ratio = S > 0 ? top / ((double)S / parts) : 0.0;
+        s_hdr[tid == 0 ? MOE_ST_IMBALANCE_RATIO : MOE_ST_RANK_IMBALANCE] = __double_as_longlong(ratio);
+    }
     if (tid == 0) {
         const unsigned long long* r = s_fin;
         int64_t* rec = s_hdr;  // the header is built in shared memory
-        const int64_t S = (int64_t)a.T * a.k;
         const int64_t emax = (int64_t)(r[RMAX_EXPERT] >> 32);
         const unsigned long long minkey = ~r[RMAX_EXPERT_MIN];
-        rec[MOE_ST_STATUS] = (int64_t)__ldcg(reinterpret_cast<const unsigned*>(a.ws + a.wl.status));
+        rec[MOE_ST_STATUS] = (int64_t)status;
         rec[MOE_ST_TOKENS] = a.T;
         rec[MOE_ST_SLOTS] = S;
         rec[MOE_ST_ROW_BYTES] = a.row_bytes;
@@ -269,12 +279,6 @@ __device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const in
         rec[MOE_ST_SUM_MODE0_BYTES] = (int64_t)r[RSUM_M0] * a.row_bytes;
         rec[MOE_ST_SUM_MODE1_BYTES] = (int64_t)r[RSUM_M1] * a.row_bytes;
         rec[MOE_ST_SUM_MODE2_BYTES] = (int64_t)r[RSUM_M2] * a.row_bytes;
-        // Imbalance ratio: busiest expert over the layer mean T*k/E
-        // ("Balancing and Beyond", section 2); the same for ranks.
-        const double ratio = S > 0 ? (double)emax / ((double)S / (double)a.E) : 0.0;
-        const double rratio = S > 0 ? (double)r[RMAX_SLOTS] / ((double)S / (double)a.R) : 0.0;
-        rec[MOE_ST_IMBALANCE_RATIO] = __double_as_longlong(ratio);
-        rec[MOE_ST_RANK_IMBALANCE] = __double_as_longlong(rratio);
         rec[MOE_ST_NUM_HOSTS] = a.H;
     }
     __syncthreads();
