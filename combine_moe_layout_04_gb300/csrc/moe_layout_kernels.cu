@@ -80,11 +80,8 @@ __device__ int block_exclusive_scan(int32_t* data, int n, int32_t* s_warp) {
     return total;
 }
 
-__device__ __forceinline__ int warp_sum(int v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-    return v;
-}
+// Sum over a converged warp (one hardware reduction).
+__device__ __forceinline__ int warp_sum(int v) { return __reduce_add_sync(kFull, v); }
 
 __device__ __forceinline__ int rank_of_expert(const LayoutArgs& a, int e, uint32_t* st) {
     int r = a.expert_to_rank ? a.expert_to_rank[e] : e / (a.E / a.R);
