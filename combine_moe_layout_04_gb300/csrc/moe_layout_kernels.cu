@@ -8,8 +8,8 @@
 //  count  one thread per token, 128 tokens per block.  A token's k ids stay in
 //         registers.  Every counter is aggregated across the warp before it
 //         touches shared memory: __match_any_sync groups equal expert ids,
-//         ballots count the tokens per rank and per host, shuffles reduce
-//         the per-source-rank counts.  Each block publishes its expert
+//         ballots count the tokens per rank and per host, one hardware warp
+//         reduction each sums the per-source-rank counts.  Each block publishes its expert
 //         histogram to a [B][E] table and adds it to the totals of its group
 //         of 16 blocks (16 atomics per counter instead of B).
 //  rank   256 threads per 128-token block.  Each warp ranks a contiguous run
@@ -19,9 +19,9 @@
 //         before its group and of at most 15 single-block counts, loaded in
 //         parallel: no block waits on another.  Every block derives the
 //         expert totals (the sum of the group rows) and the expert and rank
-//         offsets itself (cheap: O(E + R)); block 0 writes them out and also
-//         writes the statistics record into the workspace, so moe_stats is a
-//         plain copy.
+//         offsets itself (cheap: O(E + R)).  One extra block writes the counts
+//         and offsets out, and the statistics record into the workspace (so
+//         moe_stats is a plain copy), while the others write positions.
 //
 // Where the whole grid fits on the GPU at once, both phases run in one
 // cooperative kernel: each block counts, ranks its own slots (ids only),
