@@ -121,6 +121,7 @@ GROUP_CASES = [
     (_small(T=96, k=32, E=64, R=8), 2),                                # largest top-k
     (_small(T=400, k=8, E=64, R=8), 1),                                # one group: plain combine
     (_small(T=150, k=4, E=16, R=8), 8),                                # more groups than experts per rank
+    (_small(T=24, h=76800, k=4, E=16, R=8, P=2, dtype="fp8"), 2),      # 600 scale groups: plain copies
     (_small(T=200, k=8, E=1024, R=16, P=4), 64),                       # the largest E and group count
     (_small(T=128, k=32, E=1024, R=16, P=4), 64),                      # ... with the largest top-k (LSU chain)
 ]

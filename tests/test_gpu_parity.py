@@ -157,6 +157,7 @@ def _small(**kw):
     _small(T=96, k=32, E=64, R=8, P=2),            # largest top-k
     _small(T=512, k=8, E=1024, R=1024, P=16, R_src=512),  # largest E and R, 64 hosts
     _small(T=645, h=200, k=8, E=512, R=64, P=8, R_src=43),  # 45.9 KB dynamic + static > 48 KB: needs the opt-in
+    _small(T=24, h=76800, k=4, E=16, R=8, P=2, dtype="fp8"),  # 600 scale groups, staged with their chunk
 ], ids=lambda w: f"T{w.T}_h{w.h}_k{w.k}_E{w.E}_R{w.R}_{w.dtype}")
 def test_parity_edge_shapes(dev, oracle_mod, w):
     _full_check(oracle_mod, Case(w, dev, y_on_device=False))

@@ -133,6 +133,7 @@ RELAY_CASES = [
     _small(T=96, k=32, E=64, R=64, P=1),                              # largest top-k, 32+ hosts per token
     _small(T=128, k=32, E=1024, R=1024, P=16, R_src=64),             # the largest E, R, hosts and top-k together
     _small(T=5000, h=64, k=2, E=8, R=4, P=2),                         # several relay tiles, ragged tail
+    _small(T=24, h=76800, dtype="fp8"),                               # 600 scale groups: too many to stage, plain copies
     _small(T=70000, h=64, k=2, E=8, R=4, P=2),                        # 512-token relay tiles
 ]
 
