@@ -505,21 +505,23 @@ def run_ours(args, w):
     gates_bank = [gates_d] + [torch.from_numpy(mw.gen_gates(w, step=j)).to(dev) for j in range(1, n_route)]
 
     def step(ev=None, s=stream, j=0):
-        # Events bracket the two row movers: before dispatch, between dispatch
-        # and combine, after combine.  Layout and statistics (written by the
-        # layout call into lay.stats) take the rest of the step.
-        moe.moe_layout(prob, ids_bank[j], ws, lay, s)
+        # Events bracket each call: before the layout (which also writes the
+        # statistics record into lay.stats), before and after dispatch, after
+        # combine.
         if ev is not None:
             ev[0].record(s)
+        moe.moe_layout(prob, ids_bank[j], ws, lay, s)
+        if ev is not None:
+            ev[1].record(s)
         if w.quantize:
             moe.moe_dispatch_quant(prob, lay, x_d, recv, recv_s, s)
         else:
             moe.moe_dispatch(prob, lay, x_d, xs_d, recv, recv_s, s)
         if ev is not None:
-            ev[1].record(s)
+            ev[2].record(s)
         moe.moe_combine(prob, lay, y_d, gates_bank[j], out, s)
         if ev is not None:
-            ev[2].record(s)
+            ev[3].record(s)
 
     for i in range(args.warmup):
         step(j=i % n_route)
@@ -567,9 +569,11 @@ def run_ours(args, w):
     sampler.stop()
     ms_step = max_over_ranks(start.elapsed_time(end), world) / args.steps
 
-    # Per-kernel breakdown: the same steps issued one call at a time, with
-    # events between the kernels.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # Per-call breakdown, warm: the same steps issued one call at a time, back
+    # to back, with events before the layout, between the calls and after the
+    # combine.  Each call starts with what the previous one left in L2 (for
+    # bf16, the combine reads the receive rows the dispatch has just written).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -579,11 +583,43 @@ def run_ours(args, w):
     p1.record(stream)
     torch.cuda.synchronize(dev)
     ms_step_eager = max_over_ranks(p0.elapsed_time(p1), world) / args.steps
-    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(2)] for e in evs])  # ms
-    dispatch_us, combine_us = (per.mean(axis=0) * 1e3).tolist()
-    pct = {name: [round(float(v), 2) for v in np.percentile(per[:, i] * 1e3, [10, 50, 90])]
-           for i, name in enumerate(("dispatch", "combine"))}
+    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs]) * 1e3  # µs
+    layout_us, dispatch_us, combine_us = [max_over_ranks(v, world) for v in per.mean(axis=0).tolist()]
+    pct = {name: [round(float(v), 2) for v in np.percentile(per[:, i], [10, 50, 90])]
+           for i, name in enumerate(("layout", "dispatch", "combine"))}
     layout_stats_us = ms_step_eager * 1e3 - dispatch_us - combine_us
+
+    # Per-call breakdown, cold: before every call, outside its event pair, a
+    # write of twice the L2 size evicts whatever the previous call left there.
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (129 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    n_cold = min(args.steps, 200)
+    cold_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_cold)]
+    calls = (lambda s, j: moe.moe_layout(prob, ids_bank[j], ws, lay, s),
+             (lambda s, j: moe.moe_dispatch_quant(prob, lay, x_d, recv, recv_s, s)) if w.quantize else
+             (lambda s, j: moe.moe_dispatch(prob, lay, x_d, xs_d, recv, recv_s, s)),
+             lambda s, j: moe.moe_combine(prob, lay, y_d, gates_bank[j], out, s))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(n_cold):
+        for c, call in enumerate(calls):
+            flush.fill_(i & 0xFF)
+            cold_evs[i][2 * c].record(stream)
+            call(stream, i % n_route)
+            cold_evs[i][2 * c + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    cold = np.array([[e[2 * c].elapsed_time(e[2 * c + 1]) for c in range(3)] for e in cold_evs]) * 1e3
+    cold_mean = [max_over_ranks(v, world) for v in cold.mean(axis=0).tolist()]
+    del flush
+    per_call = {
+        "warm": {name: {"mean": round(layout_us if i == 0 else dispatch_us if i == 1 else combine_us, 2),
+                        "p10_p50_p90": pct[name]} for i, name in enumerate(("layout", "dispatch", "combine"))},
+        "cold": {name: {"mean": round(cold_mean[i], 2),
+                        "p10_p50_p90": [round(float(v), 2) for v in np.percentile(cold[:, i], [10, 50, 90])]}
+                 for i, name in enumerate(("layout", "dispatch", "combine"))},
+        "warm_steps": args.steps, "cold_steps": n_cold, "l2_flush_bytes": 2 * l2,
+        "note": "warm: calls back to back; cold: a write of 2x L2 before each call, outside its events",
+    }
     step(j=j_graph)
     if not torch.equal(out.view(torch.int16), out_graph.view(torch.int16)):
         raise RuntimeError("the replayed step and the eager calls disagree")
@@ -700,7 +736,7 @@ def run_ours(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_config(w),
         "dispatch_us": round(dispatch_us, 2), "combine_us": round(combine_us, 2),
-        "p10_p50_p90_us": pct,
+        "p10_p50_p90_us": pct, "per_call_us": per_call,
         "tokens_per_s": round(world * w.T / (ms_step * 1e-3), 1),
         "tokens_per_s_dc": round(w.T / ((dispatch_us + combine_us) * 1e-6), 1),
         "layout_stats_us": round(layout_stats_us, 2), "dc_us": round(dc_us, 2),

@@ -4,8 +4,9 @@ Argument marshalling only.  Every step runs in the library's CUDA kernels
 (``csrc/``); PyTorch provides device memory and streams.  The entry points
 mirror the C-ABI declared in ``include/moe_layout.h``:
 
-    moe_workspace_bytes, moe_layout, moe_stats_words, moe_stats,
-    moe_dispatch, moe_combine, moe_status, moe_status_string,
+    moe_workspace_bytes, moe_layout, moe_stats_words, moe_stats (host record,
+    synchronises), moe_stats_device, moe_dispatch, moe_combine, moe_status,
+    moe_status_string, moe_layout_noalloc,
     moe_relay_layout, moe_dispatch_relay, moe_combine_relay (the Mode 2 relay),
     moe_expert_groups, moe_dispatch_group, moe_combine_group (per-expert groups)
 
@@ -34,6 +35,7 @@ MOE_FP8_GROUP = 128
 MOE_MAX_GROUPS = 64
 MOE_MAX_HIDDEN = 1 << 20
 MOE_STATS_HEADER_WORDS = 32
+MOE_ST_STATUS = 0  # header word holding the device status bits
 MOE_FAULT_WAIT_TIMEOUT = 1
 
 # Header word names in index order (include/moe_layout.h, MOE_ST_*).
@@ -46,7 +48,8 @@ STATS_HEADER = ("status", "T", "slots", "row_bytes", "max_expert_count", "argmax
 STATS_SRC = ("src_tokens", "src_copies", "src_mode0", "src_mode1", "src_mode2",
              "src_naive_bytes", "src_mode0_bytes", "src_mode1_bytes", "src_mode2_bytes")
 STATS_DST = ("recv_slots", "recv_tokens", "recv_self", "recv_local", "recv_remote", "recv_relay")
-EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_dispatch",
+EXPORTED = ("moe_workspace_bytes", "moe_layout", "moe_stats_words", "moe_stats", "moe_stats_device",
+            "moe_dispatch",
             "moe_combine", "moe_status", "moe_status_string", "moe_layout_noalloc",
             "moe_move_faults", "moe_selftest_bounded_waits", "moe_dispatch_quant", "moe_swap_plan",
             "moe_relay_layout", "moe_dispatch_relay", "moe_combine_relay",
@@ -103,8 +106,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_layout.restype = i
     lib.moe_stats_words.argtypes = [P]
     lib.moe_stats_words.restype = ctypes.c_size_t
-    lib.moe_stats.argtypes = [P, L, vp, vp, vp]
+    lib.moe_stats.argtypes = [P, L, vp, ctypes.POINTER(ctypes.c_int64), vp]
     lib.moe_stats.restype = i
+    lib.moe_stats_device.argtypes = [P, vp, vp, vp]
+    lib.moe_stats_device.restype = i
     lib.moe_dispatch.argtypes = [P, L, vp, vp, vp, vp, vp]
     lib.moe_dispatch.restype = i
     lib.moe_swap_plan.argtypes = [P, L, ctypes.c_int32, vp, vp, vp]
@@ -270,9 +275,29 @@ def moe_stats_words(problem: Problem) -> int:
     return int(load_library().moe_stats_words(ctypes.byref(problem.c())))
 
 
-def moe_stats(problem: Problem, layout: Layout, workspace, stats, stream=None):
-    _check(load_library().moe_stats(ctypes.byref(problem.c()), ctypes.byref(layout.c()),
-                                    _ptr(workspace), _ptr(stats), _stream(stream)), "moe_stats")
+def moe_stats(problem: Problem, layout: Layout, workspace=None, stream=None):
+    """The statistics record copied to host memory; synchronises the stream.
+    Returns (code, record): code is what moe_status would return for the
+    record's status word, record a numpy int64 array (decode_stats names its
+    words).  With layout.stats set the record comes from there and the
+    workspace may be None."""
+    import numpy as np
+    rec = np.zeros(moe_stats_words(problem), dtype=np.int64)
+    rc = load_library().moe_stats(ctypes.byref(problem.c()), ctypes.byref(layout.c()), _ptr(workspace),
+                                  rec.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _stream(stream))
+    # A code that the record's status word explains came from the device; any
+    # other is a host-side rejection or a failed copy, and the record is empty.
+    from_record = rc in (MOE_OK, MOE_ERR_BAD_IDS, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT) or (
+        rc == MOE_ERR_INVALID and int(rec[0]) & (MOE_STATUS_PLACEMENT | MOE_STATUS_SRC_OFFSET))
+    if not from_record:
+        raise MoeError(rc, "moe_stats")
+    return rc, rec
+
+
+def moe_stats_device(problem: Problem, workspace, stats, stream=None):
+    """The statistics record copied to a device int64 tensor, asynchronously."""
+    _check(load_library().moe_stats_device(ctypes.byref(problem.c()), _ptr(workspace), _ptr(stats),
+                                           _stream(stream)), "moe_stats_device")
 
 
 def moe_dispatch(problem: Problem, layout: Layout, x, x_scales, recv, recv_scales, stream=None):

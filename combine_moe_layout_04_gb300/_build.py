@@ -70,7 +70,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             for _, log in results:
                 f.write(log)
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [cc, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results]
+        cmd = [cc, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results] + ["-ldl"]  # NVTX 3 loads a profiler's hook with dlopen
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -1,6 +1,7 @@
 // moe_api.cu -- the extern "C" entry points of libmoe_layout.so: argument
-// checks on the host, then kernel launches on the caller's stream.  The
-// library allocates no memory and keeps no state between calls.
+// checks on the host, then kernel launches on the caller's stream, each call
+// inside an NVTX range of its own name.  The library allocates no memory and
+// keeps no state between calls (moe_noalloc.cu's fixed scratch array aside).
 
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -72,6 +73,15 @@ WsLayout ws_layout(const Dims& d) { return moe::make_ws_layout(d.T, d.E, d.R, d.
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// The code a set of device status bits stands for (timeouts first).
+int code_of_status(uint32_t bits) {
+    if (bits & MOE_STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
+    if (bits & (MOE_STATUS_ID_RANGE | MOE_STATUS_ID_REPEAT)) return MOE_ERR_BAD_IDS;
+    if (bits & (MOE_STATUS_PLACEMENT | MOE_STATUS_SRC_OFFSET)) return MOE_ERR_INVALID;
+    if (bits & MOE_STATUS_RELAY_CAPACITY) return MOE_ERR_CAPACITY;
+    return MOE_OK;
+}
+
 int64_t row_bytes(const Dims& d) {
     return d.fp8 ? (int64_t)d.h + 4LL * (d.h / MOE_FP8_GROUP) : 2LL * d.h;
 }
@@ -81,6 +91,7 @@ int64_t row_bytes(const Dims& d) {
 extern "C" {
 
 int moe_workspace_bytes(const moe_problem* problem, size_t* bytes) {
+    MOE_NVTX("moe_workspace_bytes");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -90,6 +101,7 @@ int moe_workspace_bytes(const moe_problem* problem, size_t* bytes) {
 }
 
 size_t moe_stats_words(const moe_problem* problem) {
+    MOE_NVTX("moe_stats_words");
     Dims d;
     if (check_problem(problem, &d) != MOE_OK) return 0;
     return MOE_STATS_HEADER_WORDS + (size_t)MOE_SRC_FIELDS * d.Rs + (size_t)MOE_DST_FIELDS * d.R;
@@ -97,6 +109,7 @@ size_t moe_stats_words(const moe_problem* problem) {
 
 int moe_layout(const moe_problem* problem, const int32_t* ids, void* workspace,
                const moe_layout_t* layout, moe_stream_t stream) {
+    MOE_NVTX("moe_layout");
     Dims d;
     int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -120,20 +133,46 @@ int moe_layout(const moe_problem* problem, const int32_t* ids, void* workspace,
 }
 
 int moe_stats(const moe_problem* problem, const moe_layout_t* layout, const void* workspace,
-              int64_t* stats, moe_stream_t stream) {
+              int64_t* host_stats, moe_stream_t stream) {
+    MOE_NVTX("moe_stats");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
-    if (!layout_complete(layout, d.T) || workspace == nullptr || stats == nullptr) return MOE_ERR_INVALID;
-    if (!aligned(workspace, 256) || !aligned(stats, 8)) return MOE_ERR_ALIGN;
+    if (layout == nullptr || host_stats == nullptr) return MOE_ERR_INVALID;
+    const WsLayout wl = ws_layout(d);
+    // The layout call left the finished record in the workspace and, when
+    // asked, in layout->stats as well.
+    const void* src = layout->stats;
+    if (src == nullptr) {
+        if (workspace == nullptr) return MOE_ERR_INVALID;
+        if (!aligned(workspace, 256)) return MOE_ERR_ALIGN;
+        src = static_cast<const uint8_t*>(workspace) + wl.stats;
+    }
+    if (!aligned(src, 8) || !aligned(host_stats, 8)) return MOE_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(host_stats, src, 8 * wl.stats_words, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return code_of_status(static_cast<uint32_t>(host_stats[MOE_ST_STATUS]));
+}
+
+int moe_stats_device(const moe_problem* problem, const void* workspace, int64_t* device_stats,
+                     moe_stream_t stream) {
+    MOE_NVTX("moe_stats_device");
+    Dims d;
+    const int rc = check_problem(problem, &d);
+    if (rc != MOE_OK) return rc;
+    if (workspace == nullptr || device_stats == nullptr) return MOE_ERR_INVALID;
+    if (!aligned(workspace, 256) || !aligned(device_stats, 8)) return MOE_ERR_ALIGN;
     // The layout kernels leave the finished record in the workspace.
     const WsLayout wl = ws_layout(d);
-    return cuda_status(moe::launch_stats_copy(static_cast<const uint8_t*>(workspace), wl, stats,
+    return cuda_status(moe::launch_stats_copy(static_cast<const uint8_t*>(workspace), wl, device_stats,
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_dispatch(const moe_problem* problem, const moe_layout_t* layout, const void* x,
                  const float* x_scales, void* recv, float* recv_scales, moe_stream_t stream) {
+    MOE_NVTX("moe_dispatch");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -155,6 +194,7 @@ int moe_dispatch(const moe_problem* problem, const moe_layout_t* layout, const v
 
 int moe_dispatch_quant(const moe_problem* problem, const moe_layout_t* layout, const void* x_bf16,
                        void* recv, float* recv_scales, moe_stream_t stream) {
+    MOE_NVTX("moe_dispatch_quant");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -174,6 +214,7 @@ int moe_dispatch_quant(const moe_problem* problem, const moe_layout_t* layout, c
 
 int moe_combine(const moe_problem* problem, const moe_layout_t* layout, const void* y,
                 const float* weights, void* out, moe_stream_t stream) {
+    MOE_NVTX("moe_combine");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -192,6 +233,7 @@ int moe_combine(const moe_problem* problem, const moe_layout_t* layout, const vo
 
 int moe_relay_layout(const moe_problem* problem, const moe_layout_t* layout, void* workspace,
                      const moe_relay_t* relay, moe_stream_t stream) {
+    MOE_NVTX("moe_relay_layout");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -221,6 +263,7 @@ int moe_relay_layout(const moe_problem* problem, const moe_layout_t* layout, voi
 int moe_dispatch_relay(const moe_problem* problem, const moe_layout_t* layout, const moe_relay_t* relay,
                        const void* x, const float* x_scales, void* relay_rows, float* relay_scales,
                        void* recv, float* recv_scales, moe_stream_t stream) {
+    MOE_NVTX("moe_dispatch_relay");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -248,6 +291,7 @@ int moe_dispatch_relay(const moe_problem* problem, const moe_layout_t* layout, c
 
 int moe_combine_relay(const moe_problem* problem, const moe_layout_t* layout, const moe_relay_t* relay,
                       const void* y, const float* weights, void* partial, void* out, moe_stream_t stream) {
+    MOE_NVTX("moe_combine_relay");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -272,6 +316,7 @@ int moe_combine_relay(const moe_problem* problem, const moe_layout_t* layout, co
 
 int moe_expert_groups(const moe_problem* problem, int32_t num_groups, int32_t* expert_group,
                       moe_stream_t stream) {
+    MOE_NVTX("moe_expert_groups");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -284,6 +329,7 @@ int moe_expert_groups(const moe_problem* problem, int32_t num_groups, int32_t* e
 int moe_dispatch_group(const moe_problem* problem, const moe_layout_t* layout, const int32_t* ids,
                        const int32_t* expert_group, int32_t group, const void* x, const float* x_scales,
                        void* recv, float* recv_scales, moe_stream_t stream) {
+    MOE_NVTX("moe_dispatch_group");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -309,6 +355,7 @@ int moe_dispatch_group(const moe_problem* problem, const moe_layout_t* layout, c
 int moe_combine_group(const moe_problem* problem, const moe_layout_t* layout, const int32_t* ids,
                       const int32_t* expert_group, int32_t group, int32_t num_groups, const void* y,
                       const float* weights, float* acc, void* out, moe_stream_t stream) {
+    MOE_NVTX("moe_combine_group");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -333,6 +380,7 @@ int moe_combine_group(const moe_problem* problem, const moe_layout_t* layout, co
 }
 
 int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream) {
+    MOE_NVTX("moe_status");
     if (workspace == nullptr || status_bits == nullptr) return MOE_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint32_t bits = 0;
@@ -341,15 +389,12 @@ int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     *status_bits = bits;
-    if (bits & MOE_STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
-    if (bits & (MOE_STATUS_ID_RANGE | MOE_STATUS_ID_REPEAT)) return MOE_ERR_BAD_IDS;
-    if (bits & (MOE_STATUS_PLACEMENT | MOE_STATUS_SRC_OFFSET)) return MOE_ERR_INVALID;
-    if (bits & MOE_STATUS_RELAY_CAPACITY) return MOE_ERR_CAPACITY;
-    return MOE_OK;
+    return code_of_status(bits);
 }
 
 int moe_swap_plan(const moe_problem* problem, const moe_layout_t* layout, int32_t tau,
                   int32_t* new_expert_to_rank, int32_t* swaps, moe_stream_t stream) {
+    MOE_NVTX("moe_swap_plan");
     Dims d;
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
@@ -363,11 +408,13 @@ int moe_swap_plan(const moe_problem* problem, const moe_layout_t* layout, int32_
 }
 
 int moe_move_faults(uint32_t* bits, moe_stream_t stream) {
+    MOE_NVTX("moe_move_faults");
     if (bits == nullptr) return MOE_ERR_INVALID;
     return cuda_status(moe::read_move_faults(bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_selftest_bounded_waits(uint32_t* bits, moe_stream_t stream) {
+    MOE_NVTX("moe_selftest_bounded_waits");
     if (bits == nullptr) return MOE_ERR_INVALID;
     return cuda_status(moe::run_wait_selftest(bits, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -8,10 +8,21 @@
 #include <mutex>
 #include <unordered_map>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/moe_layout.h"
 
 namespace moe {
+
+// An NVTX range around one entry point (header-only NVTX 3: a push and a pop
+// that cost nothing unless a profiler is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define MOE_NVTX(name) ::moe::NvtxRange moe_nvtx_range_(name)
 
 // Layout kernels work on fixed token blocks: the counting pass runs one thread
 // per token, the ranking pass splits the block's T_B * k slots over 8 warps.

@@ -9,7 +9,6 @@
 // of the library's own device memory, declared below.  Every GPU that loads
 // the library holds this array until the process exits.
 
-#include <atomic>
 #include <cuda_runtime.h>
 
 #include "moe_internal.cuh"
@@ -17,29 +16,19 @@
 namespace {
 
 // The scratch itself.  In host code this name is only a host-side stand-in:
-// its device address comes from cudaGetSymbolAddress, once per device.
+// its device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_layout_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kCachedDevices = 64;
-std::atomic<void*> g_scratch_addr[kCachedDevices];
-
-// Device address of the scratch on the current device.  The first call on a
-// device looks it up (with that device current) and caches it.
+// Device address of the scratch in the current device's context.  It is
+// looked up on every call rather than cached: the lookup allocates nothing
+// and costs far less than a launch, and a cached address would go stale when
+// the module is loaded again at another address (after cudaDeviceReset, or
+// in another context on the same device).  The first lookup on a device
+// loads the library's device code there.
 cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kCachedDevices) {
-        void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-        if (p != nullptr) {
-            *out = p;
-            return cudaSuccess;
-        }
-    }
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_layout_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_layout_scratch);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kCachedDevices) g_scratch_addr[dev].store(p, std::memory_order_release);
     *out = p;
     return cudaSuccess;
 }
@@ -48,6 +37,7 @@ cudaError_t scratch_address(void** out) {
 
 extern "C" int moe_layout_noalloc(const moe_problem* problem, const int32_t* ids,
                                   const moe_layout_t* layout, moe_stream_t stream) {
+    MOE_NVTX("moe_layout_noalloc");
     size_t need = 0;
     const int rc = moe_workspace_bytes(problem, &need);
     if (rc != MOE_OK) return rc;

@@ -16,13 +16,18 @@
  *
  * Call order per MoE layer: moe_layout -> (moe_stats) -> moe_dispatch ->
  * [experts] -> moe_combine.  All calls are asynchronous on the given stream;
- * only moe_status synchronises it.
+ * only moe_stats, moe_status, moe_move_faults and moe_selftest_bounded_waits
+ * synchronise it.  Every entry
+ * point opens an NVTX range of its own name (header-only NVTX 3: free when no
+ * profiler is attached).
  *
  * Memory.  The caller allocates every buffer (device memory unless stated)
- * and the workspace; the library allocates nothing, keeps no state between
- * calls and never frees.  Inputs must stay valid until the stream has run the
- * work.  A workspace may be reused by later calls on the same stream; two
- * calls that may run concurrently need two workspaces.
+ * and the workspace; the library allocates nothing and never frees.  It keeps
+ * no state between calls, with one exception: moe_layout_noalloc's fixed
+ * scratch array (see there), which every call of that entry point shares.
+ * Inputs must stay valid until the stream has run the work.  A workspace may
+ * be reused by later calls on the same stream; two calls that may run
+ * concurrently need two workspaces.
  *
  * Errors.  Every entry point returns a moe_status code.  Arguments that the
  * host can check (sizes, NULL or misaligned pointers) are rejected before any
@@ -145,8 +150,7 @@ int moe_layout(const moe_problem* problem, const int32_t* ids, void* workspace,
  * MOE_STATS_HEADER_WORDS + 9 * R_src + 6 * R. */
 size_t moe_stats_words(const moe_problem* problem);
 
-/* Statistics of the last moe_layout run with this workspace, written to a
- * device int64 array of moe_stats_words() words (copy it to the host to read).
+/* The statistics record of a layout: int64 words, moe_stats_words() of them.
  * Header word indices are MOE_ST_*; the two ratios are IEEE doubles stored in
  * int64 words.  Then nine per-source-rank blocks of R_src words
  * (MOE_SRC_*), then six per-destination-rank blocks of R words (MOE_DST_*).
@@ -193,11 +197,39 @@ enum { MOE_SRC_TOKENS = 0, MOE_SRC_COPIES, MOE_SRC_MODE0, MOE_SRC_MODE1, MOE_SRC
 enum { MOE_DST_SLOTS = 0, MOE_DST_TOKENS, MOE_DST_SELF, MOE_DST_LOCAL, MOE_DST_REMOTE,
        MOE_DST_RELAY, MOE_DST_FIELDS };
 
+/* Statistics of a layout, copied to HOST memory; synchronises the stream.
+ * The quantities are those of "Balancing and Beyond", sections 1 (bytes that
+ * leave each rank: tokens x k x h x 2 B) and 2 (imbalance ratio), with the
+ * Mode 0/1/2 copy counts of section 3.2; the record format is above.
+ *   layout: the layout made by moe_layout; when layout->stats is set, the
+ *     record is read from there (so a moe_layout_noalloc caller, which has no
+ *     workspace, passes workspace = NULL), otherwise from the workspace.
+ *   workspace: the workspace that moe_layout used, or NULL (see layout).
+ *   host_stats: host int64 [moe_stats_words()] (pageable or pinned).
+ * Returns, after the copy, what moe_status would return for the record's
+ * status word (MOE_ST_STATUS): MOE_OK, MOE_ERR_BAD_IDS, MOE_ERR_INVALID,
+ * MOE_ERR_CAPACITY or MOE_ERR_TIMEOUT; MOE_ERR_CUDA when the copy fails.  The
+ * record is written to host_stats in every case but MOE_ERR_CUDA.  Not for
+ * use inside a stream capture (it synchronises): capture moe_stats_device. */
 int moe_stats(const moe_problem* problem, const moe_layout_t* layout,
-              const void* workspace, int64_t* stats, moe_stream_t stream);
+              const void* workspace, int64_t* host_stats, moe_stream_t stream);
+
+/* The record of "Balancing and Beyond", sections 1 and 2, as for moe_stats,
+ * copied to DEVICE memory, asynchronously (one small kernel
+ * on the stream; it can be captured in a CUDA graph).  The layout's own
+ * layout->stats pointer gives the same record without this call.
+ *   workspace: the workspace of the moe_layout call; device_stats: device
+ *   int64 [moe_stats_words()], 8-byte aligned. */
+int moe_stats_device(const moe_problem* problem, const void* workspace, int64_t* device_stats,
+                     moe_stream_t stream);
 
 /* Dispatch-permute: for every slot, recv[pos[t, j]] = x[t] (a byte-exact row
- * copy); for fp8 also recv_scales[pos[t, j]] = x_scales[t].
+ * copy); for fp8 also recv_scales[pos[t, j]] = x_scales[t].  This is the
+ * dispatch of "Balancing and Beyond", section 1 (each token to its top-k
+ * experts, one row per chosen expert), with the receive rows expert-contiguous
+ * as the permute half of "Poor HybridEP performance on dual-node 16x B300
+ * GPUs" (dispatch_with_permute) leaves them; FP8 rows travel with their
+ * scales as in that page's FP8 run.
  *   x: [T, h] bf16 or e4m3 bytes; x_scales: fp32 [T, h/128] (fp8) or NULL;
  *   recv: [T*k, h]; recv_scales: fp32 [T*k, h/128] (fp8) or NULL.
  * x and recv must be 16-byte aligned (MOE_ERR_ALIGN otherwise); scale arrays
@@ -222,6 +254,10 @@ int moe_dispatch_quant(const moe_problem* problem, const moe_layout_t* layout,
 
 /* Combine-unpermute: out[t] = bf16_rne(sum over j = 0..k-1, in ascending j,
  * of w[t, j] * y[pos[t, j]]) with one fp32 fma per term starting from 0.0f.
+ * This is the combine of "Balancing and Beyond", section 1 (the k expert
+ * outputs of a token brought back as their gate-weighted sum) and the
+ * unpermute half of "Poor HybridEP performance on dual-node 16x B300 GPUs"
+ * (combine_with_unpermute); the fixed slot order makes it deterministic.
  *   y: bf16 [T*k, h] expert outputs in receive order; weights: fp32 [T, k];
  *   out: bf16 [T, h].  y and out 16-byte aligned.  Only pos is read from the
  * layout. */
@@ -253,7 +289,9 @@ typedef struct moe_relay_t {
     int64_t capacity;   /* rows the relay buffers hold; T * min(k, H) always fits */
 } moe_relay_t;
 
-/* Relay rows of a layout made by moe_layout with this workspace.  Reads the
+/* Relay rows of a layout made by moe_layout with this workspace: the
+ * per-(token, host) copies of "Balancing and Beyond", section 3.2 (Figure 3:
+ * one copy per token and remote host, relayed by the same-index GPU).  Reads the
  * layout's host_mask, host_offset, rank_offset and pos.  Sets
  * MOE_STATUS_RELAY_CAPACITY in the workspace's status word when host_offset[H]
  * exceeds capacity (moe_status then returns MOE_ERR_CAPACITY).  All arrays
@@ -261,7 +299,9 @@ typedef struct moe_relay_t {
 int moe_relay_layout(const moe_problem* problem, const moe_layout_t* layout, void* workspace,
                      const moe_relay_t* relay, moe_stream_t stream);
 
-/* Two-hop dispatch: relay[relay_pos[t][H]] = x[t] for every (t, H) with the
+/* Two-hop dispatch of "Balancing and Beyond", section 3.2 (Figure 3): the
+ * token crosses to each host once, then fans out there.
+ * relay[relay_pos[t][H]] = x[t] for every (t, H) with the
  * mask bit (hop 1), then recv[pos[t, j]] = relay[slot_relay[t*k + j]] for every
  * slot (hop 2); fp8 scales travel with their rows.  recv equals what
  * moe_dispatch writes, byte for byte.
@@ -272,7 +312,9 @@ int moe_dispatch_relay(const moe_problem* problem, const moe_layout_t* layout, c
                        const void* x, const float* x_scales, void* relay_rows, float* relay_scales,
                        void* recv, float* recv_scales, moe_stream_t stream);
 
-/* Two-hop combine, bf16 in and out:
+/* Two-hop combine of "Balancing and Beyond", section 3.2 (Figure 3): the
+ * relay GPU sums its host's expert outputs for a token before the way back.
+ * bf16 in and out:
  *   hop 1: partial[r] = bf16_rne(sum over the slots j of token t = relay_src[r]
  *          with slot_relay[t*k + j] = r, in ascending j, of w[t, j] *
  *          y[pos[t, j]]), one fp32 fma per term from 0.0f;
@@ -302,7 +344,8 @@ int moe_combine_relay(const moe_problem* problem, const moe_layout_t* layout, co
 int moe_expert_groups(const moe_problem* problem, int32_t num_groups, int32_t* expert_group,
                       moe_stream_t stream);
 
-/* Dispatch of one expert group: recv[pos[t, j]] = x[t] (scales with it) for
+/* Dispatch of one expert group ("Balancing and Beyond", section 3.3 and
+ * Figure 4: per-expert overlap).  recv[pos[t, j]] = x[t] (scales with it) for
  * the slots whose expert ids[t, j] has expert_group = group; no other receive
  * row is written.  The G groups together write what moe_dispatch writes.
  *   ids: the [T, k] ids the layout was made from; other arguments as for
@@ -311,7 +354,9 @@ int moe_dispatch_group(const moe_problem* problem, const moe_layout_t* layout, c
                        const int32_t* expert_group, int32_t group, const void* x, const float* x_scales,
                        void* recv, float* recv_scales, moe_stream_t stream);
 
-/* Combine of one expert group.  One fp32 fma chain per token runs through the
+/* Combine of one expert group ("Balancing and Beyond", section 3.3 and
+ * Figure 4: a group's combine runs while the next group's dispatch does).
+ * One fp32 fma chain per token runs through the
  * groups in ascending order and, inside a group, through the token's slots of
  * that group in ascending j: group 0 starts it from 0.0f; every later group
  * continues it from acc[t]; every group but the last stores it to acc[t]
@@ -323,7 +368,9 @@ int moe_combine_group(const moe_problem* problem, const moe_layout_t* layout, co
                       const int32_t* expert_group, int32_t group, int32_t num_groups, const void* y,
                       const float* weights, float* acc, void* out, moe_stream_t stream);
 
-/* Waits for the stream, then reads the device status bits of the workspace
+/* The pages have no counterpart: the status word is this library's way to
+ * report data-dependent faults without faulting the GPU.
+ * Waits for the stream, then reads the device status bits of the workspace
  * (the faults found by the last moe_layout and moe_relay_layout).
  * *status_bits receives them; returns MOE_OK, MOE_ERR_BAD_IDS,
  * MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT or MOE_ERR_CUDA. */
@@ -340,19 +387,24 @@ int moe_status(const void* workspace, uint32_t* status_bits, moe_stream_t stream
  * which every GPU that loads the library holds until the process exits.  It
  * allocates nothing and frees nothing.
  *   - Returns MOE_ERR_CAPACITY, before any work is enqueued, when the
- *     problem's moe_workspace_bytes() exceeds MOE_NOALLOC_SCRATCH_BYTES
- *     (2 MiB: enough for T = 65536 tokens with E = 256 experts).
- *   - The first call on a device looks up the array's device address with
- *     that device current and caches it; make that first call before any
- *     stream capture.
+ *     problem's moe_workspace_bytes() exceeds MOE_NOALLOC_SCRATCH_BYTES.  The
+ *     workspace grows with T * E (about 4 bytes per expert per 128 tokens,
+ *     plus the statistics record), so 2 MiB holds about 245,000 tokens with
+ *     E = 256 experts and about 57,000 with E = 1024.
+ *   - Each call looks up the array's address on the current device (no
+ *     allocation, no synchronisation).  The first call on a device also loads
+ *     the library's device code there: make that first call before any stream
+ *     capture.
  *   - All calls in the process share the one array per device.  Two calls
  *     that may overlap on the GPU (different streams, or different host
  *     threads) race on it and corrupt each other's layout; serialise them.
  *     Each call clears the counters it needs, so stale contents from an
  *     earlier call do no harm.
- *   - This variant does not report the device status bits (an id out of
- *     range or repeated still cannot write out of bounds); validate the ids
- *     upstream, or use moe_layout with a workspace and moe_status. */
+ *   - There is no caller workspace, so moe_status cannot read this variant's
+ *     device status bits.  They reach the caller through the statistics
+ *     record: set layout->stats, and word MOE_ST_STATUS holds the bits (or
+ *     call moe_stats with that layout and workspace = NULL).  An id out of
+ *     range or repeated still cannot write out of bounds. */
 #define MOE_NOALLOC_SCRATCH_BYTES (2u << 20)
 int moe_layout_noalloc(const moe_problem* problem, const int32_t* ids,
                        const moe_layout_t* layout, moe_stream_t stream);
@@ -374,7 +426,8 @@ int moe_layout_noalloc(const moe_problem* problem, const int32_t* ids,
 int moe_swap_plan(const moe_problem* problem, const moe_layout_t* layout, int32_t tau,
                   int32_t* new_expert_to_rank, int32_t* swaps, moe_stream_t stream);
 
-/* Device faults of the row movers since the last call: bit
+/* The pages have no counterpart (bounded waits of this library's movers).
+ * Device faults of the row movers since the last call: bit
  * MOE_FAULT_WAIT_TIMEOUT is set when a bulk-copy pipeline of moe_dispatch or
  * moe_combine waited more than one second for its own copies, gave up, drained
  * them and returned (its output is then incomplete).  Waits for the stream,
@@ -382,7 +435,8 @@ int moe_swap_plan(const moe_problem* problem, const moe_layout_t* layout, int32_
 #define MOE_FAULT_WAIT_TIMEOUT 0x1u
 int moe_move_faults(uint32_t* bits, moe_stream_t stream);
 
-/* Self-test of the library's bounded device waits (the bulk-copy barrier
+/* The pages have no counterpart.
+ * Self-test of the library's bounded device waits (the bulk-copy barrier
  * waits of moe_dispatch / moe_combine and the grid barrier of moe_layout):
  * runs them, with a 10 ms limit, on barriers that can never complete and on
  * barriers that do, without faulting or hanging the GPU.  Allocates nothing;

@@ -83,7 +83,7 @@ class Case:
         if layout:
             m.moe_layout(self.prob, self.ids_d, self.ws, self.lay)
         if stats:
-            m.moe_stats(self.prob, self.lay, self.ws, self.stats)
+            m.moe_stats_device(self.prob, self.ws, self.stats)
         if dispatch:
             m.moe_dispatch(self.prob, self.lay, self.x_d, self.xs_d, self.recv, self.recv_s)
         if combine:

@@ -157,3 +157,51 @@ def test_host_rejects_bad_group_calls(moe):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_dispatch_group(p, lay, ids, grp, 0, odd, None, good, None, stream=0)
     assert ei.value.code == moe.MOE_ERR_ALIGN
+
+
+def test_stats_call_shapes():
+    """moe_stats hands a host record over and synchronises; moe_stats_device
+    is the asynchronous device copy (the header says which is which)."""
+    text = open(HEADER).read()
+    flat = re.sub(r"\s+", " ", text)
+    assert ("int moe_stats(const moe_problem* problem, const moe_layout_t* layout, "
+            "const void* workspace, int64_t* host_stats, moe_stream_t stream);") in flat
+    assert ("int moe_stats_device(const moe_problem* problem, const void* workspace, int64_t* device_stats, "
+            "moe_stream_t stream);") in flat
+    decl = flat[flat.index("/* Statistics of a layout, copied to HOST memory"):flat.index("int moe_stats(")]
+    assert "synchronises the stream" in decl
+
+
+def test_every_call_cites_its_passage():
+    """Each exported call's declaration comment names the page that defines
+    it, or says that the pages have no counterpart."""
+    text = open(HEADER).read()
+    pages = ("Balancing and Beyond", "Poor HybridEP", "Profiling when rank unbalance", "no counterpart")
+    cited_elsewhere = {"moe_stats_words", "moe_status_string"}   # sizes and names, no operation
+    for name in _declared():
+        if name in cited_elsewhere:
+            continue
+        at = re.search(r"^\s*int " + name + r"\(", text, flags=re.M).start()
+        comment = text[text.rindex("/*", 0, at):at]
+        assert any(p in comment for p in pages), name
+
+
+def test_host_stats_rejected_on_host(moe):
+    p = _p(moe)
+    lay = moe.Layout.__new__(moe.Layout)
+    for n in moe._LAYOUT_FIELDS:
+        setattr(lay, n, _Fake(0x10000))
+    lay.stats = None
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_stats(p, lay, None, stream=0)           # neither layout.stats nor a workspace
+    assert ei.value.code == moe.MOE_ERR_INVALID
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_stats(p, lay, _Fake(0x50010), stream=0)  # workspace not 256-byte aligned
+    assert ei.value.code == moe.MOE_ERR_ALIGN
+    lay.stats = _Fake(0x40004)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_stats(p, lay, None, stream=0)            # device record not 8-byte aligned
+    assert ei.value.code == moe.MOE_ERR_ALIGN
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_stats_device(p, _Fake(0x50000), _Fake(0x40004), stream=0)
+    assert ei.value.code == moe.MOE_ERR_ALIGN

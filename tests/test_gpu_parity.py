@@ -278,7 +278,7 @@ def test_layout_two_kernel_path_large_batch(dev, oracle_mod):
 
 def test_stats_delivered_with_the_layout(dev):
     """moe_layout can write the statistics record itself (layout.stats); it
-    equals what moe_stats copies out of the workspace."""
+    equals what moe_stats_device copies out of the workspace."""
     import torch
     import combine_moe_layout_04_gb300 as moe
     w = mw.scaled(mw.WORKLOADS["decode-EP32-r8"], T=1024, R_src=8)
@@ -286,7 +286,43 @@ def test_stats_delivered_with_the_layout(dev):
     lay = moe.Layout(case.prob, dev, with_stats=True)
     lay.stats.fill_(-1)
     moe.moe_layout(case.prob, case.ids_d, case.ws, lay)
-    moe.moe_stats(case.prob, lay, case.ws, case.stats)
+    moe.moe_stats_device(case.prob, case.ws, case.stats)
     torch.cuda.synchronize()
     assert torch.equal(lay.stats, case.stats)
     assert moe.moe_move_faults() == 0
+
+
+@pytest.mark.parametrize("name", ["prefill-fp8", "decode-EP32-r8", "decode-EP32-alt", "tiny"])
+def test_host_stats_record_matches_oracle(dev, oracle_mod, name):
+    """moe_stats, the call that synchronises and hands the record to the host
+    ("Balancing and Beyond", sections 1 and 2: bytes leaving each rank and the
+    imbalance ratio), read from the workspace and from layout.stats: every
+    field equals the oracle's at the workload's full size."""
+    import combine_moe_layout_04_gb300 as moe
+    w = mw.WORKLOADS[name]
+    step = w.steps - 1
+    case = Case(w, dev, step=step, y_on_device=True)
+    case.run(dispatch=False, combine=False, stats=False)
+    prob, keep = oracle_problem(oracle_mod, w)
+    ref = oracle_mod.stats(prob, case.ids)
+    for lay, ws in ((case.lay, case.ws), (moe.Layout(case.prob, dev, with_stats=True), None)):
+        if ws is None:
+            moe.moe_layout(case.prob, case.ids_d, case.ws, lay)
+        rc, rec = moe.moe_stats(case.prob, lay, ws)
+        assert rc == moe.MOE_OK
+        got = moe.decode_stats(case.prob, rec)
+        assert got["status"] == 0 and got["num_hosts"] == w.H
+        for field, val in ref.items():
+            assert np.array_equal(np.asarray(got[field]), np.asarray(val)), f"stats {field} differs"
+
+
+def test_host_stats_reports_bad_ids(dev):
+    """The syncing moe_stats returns the status of the record it hands over."""
+    import combine_moe_layout_04_gb300 as moe
+    w = _small(T=300, k=4, E=16)
+    ids = mw.gen_ids(w)
+    ids[5, 1] = -2
+    case = Case(w, dev, ids=ids, y_on_device=False)
+    case.run(dispatch=False, combine=False, stats=False)
+    rc, rec = moe.moe_stats(case.prob, case.lay, case.ws)
+    assert rc == moe.MOE_ERR_BAD_IDS and rec[moe.MOE_ST_STATUS] == moe.MOE_STATUS_ID_RANGE

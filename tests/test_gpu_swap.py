@@ -44,14 +44,25 @@ def test_swap_worked_example(dev):
     assert list(new) == [1, 0, 0, 1, 0, 1]
 
 
+def _oracle_counts(oracle_mod, w, ids, e2r=None):
+    """Expert counts from the oracle's own layout of the same ids: the swap
+    plan's expected values never take an input from the CUDA path."""
+    prob, keep = oracle_mod.make_problem(w.T, w.h, w.k, w.E, w.R, w.P, w.R_src,
+                                         expert_to_rank=None if e2r is None else np.asarray(e2r, np.int32))
+    return prob, keep, oracle_mod.layout(prob, np.ascontiguousarray(ids, np.int32))["expert_count"]
+
+
 @pytest.mark.parametrize("name", ["decode-EP32-r8", "decode-EP32-s1.1", "prefill-fp8"])
 def test_swap_plan_parity(dev, oracle_mod, name):
+    """"Balancing and Beyond", section 3.1 and Figure 2(b): the plan from the
+    layout's expert counts, against the oracle's plan from the oracle's counts."""
     w = mw.WORKLOADS[name]
     ids = mw.gen_ids(w)
+    prob, keep, want_cnt = _oracle_counts(oracle_mod, w, ids)
     for tau in (0, 5, 200):
         cnt, new, swaps = _plan(dev, w, ids, tau)
-        prob, keep = oracle_mod.make_problem(w.T, w.h, w.k, w.E, w.R, w.P, w.R_src)
-        want_new, want_swaps = oracle_mod.swap_plan(prob, cnt, tau)
+        assert np.array_equal(cnt, want_cnt), "GPU expert counts differ from the oracle layout's"
+        want_new, want_swaps = oracle_mod.swap_plan(prob, want_cnt, tau)
         assert np.array_equal(new, want_new)
         assert np.array_equal(swaps, want_swaps)
 
@@ -63,13 +74,17 @@ def test_swap_plan_custom_placement_and_next_layout(dev, oracle_mod):
     rng = np.random.default_rng(12)
     e2r = rng.permutation(np.repeat(np.arange(w.R), w.E // w.R)).astype(np.int32)
     ids = mw.gen_ids(w)
+    prob, keep, want_cnt = _oracle_counts(oracle_mod, w, ids, e2r)
     cnt, new, swaps = _plan(dev, w, ids, 1, e2r)
-    prob, keep = oracle_mod.make_problem(w.T, w.h, w.k, w.E, w.R, w.P, w.R_src, expert_to_rank=e2r)
-    want_new, want_swaps = oracle_mod.swap_plan(prob, cnt, 1)
+    assert np.array_equal(cnt, want_cnt), "GPU expert counts differ from the oracle layout's"
+    want_new, want_swaps = oracle_mod.swap_plan(prob, want_cnt, 1)
     assert np.array_equal(new, want_new) and np.array_equal(swaps, want_swaps)
+    # the next step's layout under the new placement, against the oracle's
+    prob2, keep2, want_cnt2 = _oracle_counts(oracle_mod, w, ids, want_new)
     cnt2, _, _ = _plan(dev, w, ids, 1, new)
-    load_after = np.bincount(new, weights=cnt2, minlength=w.R)
+    assert np.array_equal(cnt2, want_cnt2)
+    load_after = np.bincount(want_new, weights=want_cnt2, minlength=w.R)
     for hh in range(w.H):
-        for a, b, x, y, old, best in swaps[hh]:
+        for a, b, x, y, old, best in want_swaps[hh]:
             if old - best >= 1:
                 assert max(load_after[a], load_after[b]) == best
