@@ -471,8 +471,11 @@ def run_ours(args, w):
     fp8 = w.dtype == "fp8"
     ids = mw.gen_ids(w)
     gates = mw.gen_gates(w)
+    # Launch shapes: the library's defaults unless MOE_* variables set some
+    # (moe_tuning; MOE_DISPATCH_KIND=bulk, MOE_DISPATCH_WARPS=6, ...).
+    tuning = moe.Tuning.from_env()
     prob = moe.Problem(w.T, w.h, w.k, w.E, w.R, w.P, w.R_src,
-                       moe.MOE_DTYPE_FP8_E4M3 if fp8 else moe.MOE_DTYPE_BF16)
+                       moe.MOE_DTYPE_FP8_E4M3 if fp8 else moe.MOE_DTYPE_BF16, tuning=tuning)
     lay = moe.Layout(prob, dev, with_stats=True)  # the layout call also writes the statistics
     ws = moe.alloc_workspace(prob, dev)
     stats = lay.stats
@@ -758,6 +761,7 @@ def run_ours(args, w):
                 "schedule": "two device buffer sets; uploads, calls and downloads on three streams",
                 "host_cpus": host_cpus},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "tuning": {k: v for k, v in tuning.as_dict().items() if v} or "library defaults",
         "mode2_relay": dict(relay, frac_of_peak=round(relay["gbs"] / peak, 4)) if relay else None,
         "per_expert_groups": [p for p in peo if p],
         "clocks": sampler.summary(h0, h1),

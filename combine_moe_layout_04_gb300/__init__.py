@@ -37,6 +37,7 @@ MOE_MAX_HIDDEN = 1 << 20
 MOE_STATS_HEADER_WORDS = 32
 MOE_ST_STATUS = 0  # header word holding the device status bits
 MOE_FAULT_WAIT_TIMEOUT = 1
+MOE_MOVE_AUTO, MOE_MOVE_VECTOR, MOE_MOVE_BULK = 0, 1, 2
 
 # Header word names in index order (include/moe_layout.h, MOE_ST_*).
 STATS_HEADER = ("status", "T", "slots", "row_bytes", "max_expert_count", "argmax_expert",
@@ -66,12 +67,54 @@ class MoeError(RuntimeError):
         self.code = code
 
 
+_TUNING_FIELDS = ("dispatch_kind", "dispatch_sms", "dispatch_ctas_per_sm", "dispatch_warps", "dispatch_stages",
+                  "dispatch_chunk_bytes", "combine_kind", "combine_sms", "combine_ctas_per_sm")
+
+
+class _TuningC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in _TUNING_FIELDS] + [("reserved", ctypes.c_int32 * 7)]
+
+
 class _ProblemC(ctypes.Structure):
     _fields_ = [("num_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32), ("topk", ctypes.c_int32),
                 ("num_experts", ctypes.c_int32), ("num_ranks", ctypes.c_int32),
                 ("ranks_per_host", ctypes.c_int32), ("num_src_ranks", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("expert_to_rank", ctypes.c_void_p),
-                ("src_rank_offsets", ctypes.c_void_p)]
+                ("src_rank_offsets", ctypes.c_void_p), ("tuning", ctypes.POINTER(_TuningC))]
+
+
+@dataclass
+class Tuning:
+    """Launch shapes of the row movers (moe_tuning in include/moe_layout.h);
+    0 keeps the library's default.  Shapes change speed only, never results."""
+    dispatch_kind: int = MOE_MOVE_AUTO
+    dispatch_sms: int = 0
+    dispatch_ctas_per_sm: int = 0
+    dispatch_warps: int = 0
+    dispatch_stages: int = 0
+    dispatch_chunk_bytes: int = 0
+    combine_kind: int = MOE_MOVE_AUTO
+    combine_sms: int = 0
+    combine_ctas_per_sm: int = 0
+
+    def c(self) -> _TuningC:
+        return _TuningC(*[int(getattr(self, n)) for n in _TUNING_FIELDS])
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n in _TUNING_FIELDS}
+
+    @classmethod
+    def from_env(cls, environ=None) -> "Tuning":
+        """MOE_DISPATCH_KIND, MOE_DISPATCH_SMS, ... (upper-case field names
+        with a MOE_ prefix; kinds also as "auto", "vector" or "bulk")."""
+        env = os.environ if environ is None else environ
+        kinds = {"auto": MOE_MOVE_AUTO, "vector": MOE_MOVE_VECTOR, "bulk": MOE_MOVE_BULK}
+        vals = {}
+        for n in _TUNING_FIELDS:
+            v = env.get("MOE_" + n.upper())
+            if v is not None and v != "":
+                vals[n] = kinds[v.lower()] if v.lower() in kinds else int(v)
+        return cls(**vals)
 
 
 _LAYOUT_FIELDS = ("expert_count", "expert_offset", "rank_count", "rank_offset", "host_count",
@@ -172,6 +215,7 @@ class Problem:
     dtype: int = MOE_DTYPE_BF16
     expert_to_rank: object = None      # device int32 tensor [E] or None
     src_rank_offsets: object = None    # device int32 tensor [R_src + 1] or None
+    tuning: Optional[Tuning] = None    # launch shapes, or None for the defaults
 
     @property
     def num_hosts(self) -> int:
@@ -184,9 +228,14 @@ class Problem:
         return 2 * self.hidden
 
     def c(self) -> _ProblemC:
-        return _ProblemC(self.num_tokens, self.hidden, self.topk, self.num_experts, self.num_ranks,
-                         self.ranks_per_host, self.num_src_ranks, self.dtype,
-                         _ptr(self.expert_to_rank), _ptr(self.src_rank_offsets))
+        # the struct keeps its tuning alive for as long as it is referenced
+        pc = _ProblemC(self.num_tokens, self.hidden, self.topk, self.num_experts, self.num_ranks,
+                       self.ranks_per_host, self.num_src_ranks, self.dtype,
+                       _ptr(self.expert_to_rank), _ptr(self.src_rank_offsets), None)
+        if self.tuning is not None:
+            pc._tuning = self.tuning.c()
+            pc.tuning = ctypes.pointer(pc._tuning)
+        return pc
 
 
 class Layout:

@@ -15,12 +15,46 @@ using moe::WsLayout;
 struct Dims {
     int T, h, k, E, R, P, H, Rs;
     bool fp8;
+    moe::MoveShape shape;
 };
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Launch shapes of a moe_tuning (NULL: every default), checked on the host.
+int check_tuning(const moe_tuning* t, moe::MoveShape* sh) {
+    *sh = moe::MoveShape{};
+    if (t == nullptr) return MOE_OK;
+    auto in = [](int v, int lo, int hi) { return v == 0 || (v >= lo && v <= hi); };
+    if (!in(t->dispatch_kind, MOE_MOVE_VECTOR, MOE_MOVE_BULK) || !in(t->combine_kind, MOE_MOVE_VECTOR, MOE_MOVE_BULK))
+        return MOE_ERR_INVALID;
+    if (!in(t->dispatch_sms, 1, 1 << 16) || !in(t->combine_sms, 1, 1 << 16)) return MOE_ERR_INVALID;
+    if (!in(t->dispatch_ctas_per_sm, 1, 8) || !in(t->dispatch_warps, 1, 16) || !in(t->dispatch_stages, 1, 8))
+        return MOE_ERR_INVALID;
+    if (!in(t->dispatch_chunk_bytes, 256, 32768) || t->dispatch_chunk_bytes % 16 != 0) return MOE_ERR_INVALID;
+    if (!in(t->combine_ctas_per_sm, 1, 3)) return MOE_ERR_INVALID;
+    for (int r : t->reserved)
+        if (r != 0) return MOE_ERR_INVALID;
+    // the bulk dispatch's stages must fit in shared memory (the larger of the
+    // two default warp counts stands in for a field left 0)
+    const long long warps = t->dispatch_warps ? t->dispatch_warps : 6;
+    const long long stages = t->dispatch_stages ? t->dispatch_stages : 4;
+    const long long chunk = t->dispatch_chunk_bytes ? t->dispatch_chunk_bytes : 7168;
+    if (warps * stages * chunk > 220 * 1024) return MOE_ERR_INVALID;
+    sh->dispatch_kind = t->dispatch_kind;
+    sh->dispatch_sms = t->dispatch_sms;
+    sh->dispatch_ctas = t->dispatch_ctas_per_sm;
+    sh->dispatch_warps = t->dispatch_warps;
+    sh->dispatch_stages = t->dispatch_stages;
+    sh->dispatch_chunk = t->dispatch_chunk_bytes;
+    sh->combine_kind = t->combine_kind;
+    sh->combine_sms = t->combine_sms;
+    sh->combine_ctas = t->combine_ctas_per_sm;
+    return MOE_OK;
+}
+
 int check_problem(const moe_problem* p, Dims* d) {
     if (p == nullptr) return MOE_ERR_INVALID;
+    if (check_tuning(p->tuning, &d->shape) != MOE_OK) return MOE_ERR_INVALID;
     d->T = p->num_tokens; d->h = p->hidden; d->k = p->topk; d->E = p->num_experts;
     d->R = p->num_ranks; d->P = p->ranks_per_host; d->Rs = p->num_src_ranks;
     d->fp8 = p->dtype == MOE_DTYPE_FP8_E4M3;
@@ -183,6 +217,7 @@ int moe_dispatch(const moe_problem* problem, const moe_layout_t* layout, const v
     if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(layout->pos, 4)) return MOE_ERR_ALIGN;
     if (d.fp8 && (!aligned(x_scales, 4) || !aligned(recv_scales, 4))) return MOE_ERR_ALIGN;
     moe::MoveArgs m{};
+    m.shape = d.shape;
     m.pos = layout->pos;
     m.T = d.T;
     m.k = d.k;
@@ -205,6 +240,7 @@ int moe_dispatch_quant(const moe_problem* problem, const moe_layout_t* layout, c
     if (!aligned(x_bf16, 16) || !aligned(recv, 16) || !aligned(recv_scales, 4) || !aligned(layout->pos, 4))
         return MOE_ERR_ALIGN;
     moe::MoveArgs m{};
+    m.shape = d.shape;
     m.pos = layout->pos;
     m.T = d.T;
     m.k = d.k;
@@ -224,6 +260,7 @@ int moe_combine(const moe_problem* problem, const moe_layout_t* layout, const vo
     if (!aligned(y, 16) || !aligned(out, 16) || !aligned(weights, 4) || !aligned(layout->pos, 4))
         return MOE_ERR_ALIGN;
     moe::MoveArgs m{};
+    m.shape = d.shape;
     m.pos = layout->pos;
     m.T = d.T;
     m.k = d.k;
@@ -279,6 +316,7 @@ int moe_dispatch_relay(const moe_problem* problem, const moe_layout_t* layout, c
     if (d.fp8 && (!aligned(x_scales, 4) || !aligned(relay_scales, 4) || !aligned(recv_scales, 4)))
         return MOE_ERR_ALIGN;
     moe::MoveArgs m{};
+    m.shape = d.shape;
     m.pos = layout->pos;
     m.T = d.T;
     m.k = d.k;
@@ -305,6 +343,7 @@ int moe_combine_relay(const moe_problem* problem, const moe_layout_t* layout, co
         !aligned(relay->slot_relay, 4))
         return MOE_ERR_ALIGN;
     moe::MoveArgs m{};
+    m.shape = d.shape;
     m.pos = layout->pos;
     m.T = d.T;
     m.k = d.k;
@@ -342,6 +381,7 @@ int moe_dispatch_group(const moe_problem* problem, const moe_layout_t* layout, c
         return MOE_ERR_ALIGN;
     if (d.fp8 && (!aligned(x_scales, 4) || !aligned(recv_scales, 4))) return MOE_ERR_ALIGN;
     moe::MoveArgs m{};
+    m.shape = d.shape;
     m.pos = layout->pos;
     m.T = d.T;
     m.k = d.k;
@@ -370,6 +410,7 @@ int moe_combine_group(const moe_problem* problem, const moe_layout_t* layout, co
         !aligned(layout->pos, 4) || !aligned(ids, 4) || !aligned(expert_group, 4))
         return MOE_ERR_ALIGN;
     moe::MoveArgs m{};
+    m.shape = d.shape;
     m.pos = layout->pos;
     m.T = d.T;
     m.k = d.k;

@@ -112,12 +112,19 @@ struct LayoutArgs {
     moe_layout_t out;
 };
 
+// Launch shapes of the row movers from a moe_tuning (0 = the default).
+struct MoveShape {
+    int dispatch_kind, dispatch_sms, dispatch_ctas, dispatch_warps, dispatch_stages, dispatch_chunk;
+    int combine_kind, combine_sms, combine_ctas;
+};
+
 struct MoveArgs {
     const int32_t* pos;
     int T, k;
     int nvec;        // 16-byte vectors per row
     int nchunks;     // column chunks per row (one warp per (token, chunk))
     int chunk_vecs;  // vectors per chunk
+    MoveShape shape;
 };
 
 // Mode 2 relay rows of one layout (moe_relay_t plus the device word that
@@ -192,6 +199,20 @@ __device__ __forceinline__ uint4 ld_stream_v4_hint(const uint4* p, uint64_t pol)
     asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
     return v;
+}
+
+// 32-byte accesses (256-bit global loads and stores of sm_100 and later): the
+// address must be 32-byte aligned.  A warp request of consecutive lanes then
+// covers 1 KB of whole sectors.
+__device__ __forceinline__ void ld_stream_v8f(const float* p, float (&v)[8]) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+                 : "l"(p));
+}
+__device__ __forceinline__ void st_v8f(float* p, const float (&v)[8]) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ void st_v4(uint4* p, uint4 v) {

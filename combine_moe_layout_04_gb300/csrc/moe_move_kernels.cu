@@ -546,7 +546,7 @@ __device__ __forceinline__ void compact_partners(int lane, int p, float w, int& 
 template <int WARPS, int STAGES, int ACC, class Route>
 __global__ void __launch_bounds__(WARPS * 32, kCombCtasPerSmPacked)
 combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __restrict__ out, int row_bytes,
-                      float* __restrict__ acc_rows) {
+                      float* __restrict__ acc_rows, bool acc_v8) {
     constexpr int STAGE_BYTES = kPackSlots * kPiece;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
@@ -666,20 +666,24 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
                 uint4* o = reinterpret_cast<uint4*>(out + (size_t)orow * row_bytes + (size_t)piece * kPiece);
                 float* arow = ACC == kAccNone ? nullptr
                                               : acc_rows + (size_t)orow * (row_bytes / 2) + (size_t)piece * (kPiece / 2);
-                // Lane v's 8 chain values are two 16-byte halves 32 bytes apart, so a
-                // warp request fills half of each sector it touches; L2 merges the
-                // halves.  Exchanging values between lanes for fully packed requests
-                // measured slower (the shuffles sit between the wait and the refill).
+                // Lane v's 8 chain values are 32 contiguous bytes.  With a 32-byte
+                // aligned chain they move as one 256-bit access, so a warp request
+                // covers 1 KB of whole sectors; otherwise as two 16-byte halves 32
+                // bytes apart (each request then half-fills the sectors it touches).
                 if (lane < pb / 16) {
                     const int v = lane;
                     float acc[8];
                     if constexpr (ACC == kAccMid || ACC == kAccLast) {
-                        const uint4 a0 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v));
-                        const uint4 a1 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v + 4));
-                        acc[0] = __uint_as_float(a0.x); acc[1] = __uint_as_float(a0.y);
-                        acc[2] = __uint_as_float(a0.z); acc[3] = __uint_as_float(a0.w);
-                        acc[4] = __uint_as_float(a1.x); acc[5] = __uint_as_float(a1.y);
-                        acc[6] = __uint_as_float(a1.z); acc[7] = __uint_as_float(a1.w);
+                        if (acc_v8) {
+                            ld_stream_v8f(arow + 8 * v, acc);
+                        } else {
+                            const uint4 a0 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v));
+                            const uint4 a1 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * v + 4));
+                            acc[0] = __uint_as_float(a0.x); acc[1] = __uint_as_float(a0.y);
+                            acc[2] = __uint_as_float(a0.z); acc[3] = __uint_as_float(a0.w);
+                            acc[4] = __uint_as_float(a1.x); acc[5] = __uint_as_float(a1.y);
+                            acc[6] = __uint_as_float(a1.z); acc[7] = __uint_as_float(a1.w);
+                        }
                     } else {
 #pragma unroll
                         for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
@@ -688,11 +692,15 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
                     for (int j = 0; j < kPackSlots; ++j)
                         if (j < n) fma_bf16x8(acc, wj[j], lds_v4(st + (i * n + j) * kPiece + v * 16));
                     if constexpr (ACC == kAccFirst || ACC == kAccMid) {
-                        uint4* a4 = reinterpret_cast<uint4*>(arow + 8 * v);
-                        st_v4(a4, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                                             __float_as_uint(acc[2]), __float_as_uint(acc[3])));
-                        st_v4(a4 + 1, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
-                                                 __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+                        if (acc_v8) {
+                            st_v8f(arow + 8 * v, acc);
+                        } else {
+                            uint4* a4 = reinterpret_cast<uint4*>(arow + 8 * v);
+                            st_v4(a4, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                                                 __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+                            st_v4(a4 + 1, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                                     __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+                        }
                     } else {
                         st_v4(o + v, pack_bf16x8(acc));
                     }
@@ -713,82 +721,92 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
     }
 }
 
-// Dispatch: each warp owns STAGES stages of CHUNK bytes of source rows; a stage
+// Dispatch through shared memory: each warp owns `stages` stages of `chunk`
+// bytes of source rows (warps, stages and chunk are launch values); a stage
 // holds one (unit, column chunk), written to the unit's partner rows by one
 // bulk store each.  fp8 scale rows (`groups` floats) travel with the first
 // chunk: through the stage as one more bulk load and a bulk store per partner
 // when sbytes = 4 * groups > 0 (a multiple of 16 bytes, both arrays 16-byte
 // aligned), otherwise by plain 4-byte copies.  SKIP_EMPTY (routes where many
 // units have no partner, such as one expert group): partners are looked up
-// before the load, and a unit without any is not loaded.
-template <int WARPS, int STAGES, int CHUNK, class Route, bool SKIP_EMPTY = false>
-__global__ void __launch_bounds__(WARPS * 32, 1)
-dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ x, const float* __restrict__ xs,
-                     uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups, int sbytes) {
+// before the load, and a unit without any is not loaded.  Dynamic shared
+// memory: the barriers (kDispBarBytes), then the warps' stages.
+constexpr int kMaxDispWarps = 16, kMaxDispStages = 8;
+constexpr int kDispBarBytes = kMaxDispWarps * kMaxDispStages * 8;
+
+template <class Route, bool SKIP_EMPTY = false>
+__global__ void __launch_bounds__(kMaxDispWarps * 32, 1)
+dispatch_bulk_kernel(const Route rt, const int nch, const int stages, const int chunk, const uint8_t* __restrict__ x,
+                     const float* __restrict__ xs, uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes,
+                     int groups, int sbytes) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int stride = CHUNK + sbytes;  // a stage: the chunk, then the scale row
-    const uint32_t stage0 = smem_u32(smem + (size_t)warp * STAGES * stride);
-    const uint32_t bar0 = smem_u32(&s_bar[warp][0]);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, warps = blockDim.x >> 5;
+    const int stride = chunk + sbytes;  // a stage: the chunk, then the scale row
+    const uint32_t stage0 = smem_u32(smem + kDispBarBytes + (size_t)warp * stages * stride);
+    const uint32_t bar0 = smem_u32(smem + 8 * kMaxDispStages * warp);
     if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
+        for (int s = 0; s < stages; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_mbar_init();
     }
     __syncwarp();
 
     const long long units = rt.units() * nch;
-    const long long nw = (long long)gridDim.x * WARPS;
-    const long long gw = (long long)blockIdx.x * WARPS + warp;
+    const long long nw = (long long)gridDim.x * warps;
+    const long long gw = (long long)blockIdx.x * warps + warp;
+    const long long step = (long long)stages * nw;  // a stage's stride through the units
 
-    long long su[STAGES];
-    bool pending[STAGES];
-    uint32_t ph[STAGES];
-    int pr[STAGES];  // SKIP_EMPTY: this lane's partner row of the stage's unit
+    long long su[kMaxDispStages];
+    bool pending[kMaxDispStages];
+    uint32_t ph[kMaxDispStages];
+    int pr[kMaxDispStages];  // SKIP_EMPTY: this lane's partner row of the stage's unit
     // Issues the bulk load of unit u into stage s (lane 0); with SKIP_EMPTY
     // (all lanes call it) returns false, loading nothing, when u has no partner.
-    auto issue = [&](int s, long long u) -> bool {
+    auto issue = [&](int s, long long u, int& p_out) -> bool {
         const long long ui = u / nch;
         if constexpr (SKIP_EMPTY) {
             float unused;
-            rt.partner(ui, true, lane, pr[s], unused);
-            if (__ballot_sync(0xffffffffu, pr[s] >= 0) == 0u) return false;
+            rt.partner(ui, true, lane, p_out, unused);
+            if (__ballot_sync(0xffffffffu, p_out >= 0) == 0u) return false;
         }
         if (lane == 0) {
             const int c = (int)(u - ui * nch);
-            const int cb = min(CHUNK, row_bytes - c * CHUNK);
+            const int cb = min(chunk, row_bytes - c * chunk);
             const bool with_scales = sbytes > 0 && c == 0;
             const size_t src = (size_t)rt.self_row(ui);
             mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(cb + (with_scales ? sbytes : 0)));
-            bulk_g2s(stage0 + s * stride, x + src * row_bytes + (size_t)c * CHUNK, (uint32_t)cb, bar0 + 8 * s);
+            bulk_g2s(stage0 + s * stride, x + src * row_bytes + (size_t)c * chunk, (uint32_t)cb, bar0 + 8 * s);
             if (with_scales)
-                bulk_g2s(stage0 + s * stride + CHUNK, xs + src * groups, (uint32_t)sbytes, bar0 + 8 * s);
+                bulk_g2s(stage0 + s * stride + chunk, xs + src * groups, (uint32_t)sbytes, bar0 + 8 * s);
         }
         return true;
     };
-    // First unit at or after u, in this warp's stride, that needs a load.
-    auto next_loaded = [&](int s, long long u) -> long long {
-        while (u < units && !issue(s, u)) u += STAGES * nw;
+    // First unit at or after u, in this stage's stride, that needs a load.
+    auto next_loaded = [&](int s, long long u, int& p_out) -> long long {
+        while (u < units && !issue(s, u, p_out)) u += step;
         return u;
     };
 
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < kMaxDispStages; ++s) {
+        pending[s] = false;
         ph[s] = 0;
-        su[s] = next_loaded(s, gw + s * nw);
-        pending[s] = su[s] < units;
+        pr[s] = -1;
+        su[s] = units;
+        if (s < stages) {
+            su[s] = next_loaded(s, gw + s * nw, pr[s]);
+            pending[s] = su[s] < units;
+        }
     }
     bool failed = false, busy = true;
     while (busy && !failed) {
         busy = false;
 #pragma unroll
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < kMaxDispStages; ++s) {
             if (!pending[s] || failed) continue;
             const long long u = su[s];
             const long long ui = u / nch;
             const int c = (int)(u - ui * nch);
-            const int cb = min(CHUNK, row_bytes - c * CHUNK);
+            const int cb = min(chunk, row_bytes - c * chunk);
             int p = pr[s];
             if constexpr (!SKIP_EMPTY) {
                 float unused;
@@ -803,9 +821,9 @@ dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ 
             pending[s] = false;
             fence_proxy_async_smem();
             if (p >= 0) {
-                bulk_s2g(recv + (size_t)p * row_bytes + (size_t)c * CHUNK, stage0 + s * stride, (uint32_t)cb);
+                bulk_s2g(recv + (size_t)p * row_bytes + (size_t)c * chunk, stage0 + s * stride, (uint32_t)cb);
                 if (sbytes > 0 && c == 0)
-                    bulk_s2g(rs + (size_t)p * groups, stage0 + s * stride + CHUNK, (uint32_t)sbytes);
+                    bulk_s2g(rs + (size_t)p * groups, stage0 + s * stride + chunk, (uint32_t)sbytes);
             }
             bulk_commit();
             if (groups > 0 && sbytes == 0 && c == 0) {
@@ -819,7 +837,7 @@ dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ 
             // The stage may be refilled once every lane's stores have read it.
             bulk_wait_read<0>();
             __syncwarp();
-            su[s] = next_loaded(s, u + STAGES * nw);
+            su[s] = next_loaded(s, u + step, pr[s]);
             if (su[s] < units) {
                 pending[s] = true;
                 busy = true;
@@ -829,7 +847,121 @@ dispatch_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ 
     bulk_wait_all();
     if (failed) {
         if (lane == 0) atomicOr(&g_move_faults, kFaultWaitTimeout);
-        drain_stages<STAGES>(bar0, pending, ph);
+#pragma unroll
+        for (int s = 0; s < kMaxDispStages; ++s)
+            if (pending[s]) mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs);
+    }
+}
+
+// ---- vector dispatch ---------------------------------------------------------
+//
+// Rows through registers: one warp per (unit, span of the source row).  Every
+// lane loads its V vectors of VB bytes of the span, all loads issued before
+// any store, then writes them to each partner row in ascending lane order.  A
+// span is 32 x V x VB = 7168 bytes (an fp8 row of h = 7168; half a bf16 one).
+// With VB = 32 the loads and stores are 256-bit (sm_100 and later), so a warp
+// request covers 1 KB of whole sectors.  On GB300 this moved a read-1 /
+// write-8 broadcast of 16384 fp8 rows (7168 B, random receive rows) in
+// 166-168 us against 182-184 us for the shared-memory bulk pipeline, and
+// 4096 bf16 rows in 86-88 us against 94 us: with the same bytes in flight per
+// SM, the register path keeps the DRAM write stream fuller.  fp8 scale rows travel
+// with the first span: lane L keeps words L + 32 q (rows of up to
+// 32 x kVecScaleWords groups; longer ones are copied word by word).  A unit
+// without partners loads nothing.
+constexpr int kVecThreads = 256;
+constexpr int kVecMinBlocks = 2;   // ~100 registers a thread: two 8-warp CTAs fill an SM's registers
+constexpr int kVecScaleWords = 4;
+// A grid of 8x the resident CTAs, each warp taking one or two units, moved
+// the fp8 broadcast above in 166-168 us on GB300; a persistent grid of
+// exactly the resident CTAs looping over the units took 185 us.
+constexpr int kVecOversubscribe = 8;
+
+template <int VB> struct VecT;
+template <> struct VecT<32> {
+    uint32_t w[8];
+    __device__ __forceinline__ void load(const uint8_t* p) {
+        asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                       "=r"(w[7])
+                     : "l"(p));
+    }
+    __device__ __forceinline__ void store(uint8_t* p) const {
+        asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                     :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                        "r"(w[7])
+                     : "memory");
+    }
+};
+template <> struct VecT<16> {
+    uint32_t w[4];
+    __device__ __forceinline__ void load(const uint8_t* p) {
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p));
+    }
+    __device__ __forceinline__ void store(uint8_t* p) const {
+        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                     :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+    }
+};
+
+template <int VB> struct VecSpan { static constexpr int V = 7168 / (32 * VB); };
+
+template <int VB, class Route>
+__global__ void __launch_bounds__(kVecThreads, kVecMinBlocks)
+dispatch_vec_kernel(const Route rt, const int nspan, const uint8_t* __restrict__ x, const float* __restrict__ xs,
+                    uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups) {
+    constexpr int V = VecSpan<VB>::V;
+    constexpr int SPAN = 32 * V * VB;
+    constexpr int WPB = kVecThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const long long units = rt.units() * nspan;
+    const long long nw = (long long)gridDim.x * WPB;
+    long long u = (long long)blockIdx.x * WPB + (threadIdx.x >> 5);
+    float unused;
+    int pnext;  // partners of the warp's next unit, looked up one unit ahead
+    rt.partner(u / nspan, u < units, lane, pnext, unused);
+    for (; u < units; u += nw) {
+        const long long ui = u / nspan;
+        const int c = (int)(u - ui * nspan);
+        const int p = pnext;
+        // the next unit's lookup goes out now; its loads overlap this unit's stores
+        rt.partner((u + nw) / nspan, u + nw < units, lane, pnext, unused);
+        const unsigned pm = __ballot_sync(kAll, p >= 0);
+        if (pm == 0u) continue;  // nothing to write
+        const size_t srow = (size_t)rt.self_row(ui);
+        const uint8_t* src = x + srow * row_bytes + (size_t)c * SPAN;
+        const int lim = row_bytes - c * SPAN;  // bytes of the row from this span on
+        VecT<VB> v[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int off = (i * 32 + lane) * VB;
+            if (off < lim) v[i].load(src + off);
+        }
+        const bool scales = groups > 0 && c == 0;
+        const bool keep = groups <= 32 * kVecScaleWords;
+        float sv[kVecScaleWords];
+#pragma unroll
+        for (int q = 0; q < kVecScaleWords; ++q)
+            sv[q] = (scales && keep && lane + 32 * q < groups) ? xs[srow * groups + lane + 32 * q] : 0.0f;
+        for (unsigned m = pm; m; m &= m - 1) {
+            const int pj = __shfl_sync(kAll, p, __ffs(m) - 1);
+            uint8_t* dst = recv + (size_t)pj * row_bytes + (size_t)c * SPAN;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int off = (i * 32 + lane) * VB;
+                if (off < lim) v[i].store(dst + off);
+            }
+            if (scales) {
+                float* srow_out = rs + (size_t)pj * groups;
+                if (keep) {
+#pragma unroll
+                    for (int q = 0; q < kVecScaleWords; ++q)
+                        if (lane + 32 * q < groups) srow_out[lane + 32 * q] = sv[q];
+                } else {
+                    for (int g = lane; g < groups; g += 32) srow_out[g] = xs[srow * groups + g];
+                }
+            }
+        }
     }
 }
 
@@ -845,10 +977,23 @@ int grid_for(K kernel, long long units) {
     return (int)max(1LL, min(need, cap));
 }
 
+// SMs a mover's grid may cover: the tuning's count, at most the GPU's.
+int mover_sms(int want) {
+    const int sms = device_sm_count();
+    return want > 0 && want < sms ? want : sms;
+}
+
+// Grid of `per_sm` CTAs on each of `sms` SMs, no larger than the work needs.
+int capped_grid(long long units, int warps_per_cta, int sms, int per_sm) {
+    const long long need = (units + warps_per_cta - 1) / warps_per_cta;
+    const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
+    return (int)(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
 // Default shapes of the bulk pipelines, chosen by a sweep on GB300 at the
 // prefill-fp8 shape: warps per CTA, stages per warp, chunk bytes, CTAs per SM.
 constexpr int kCombWarps = 8, kCombStages = 2, kCombChunk = 512, kCombCtasPerSm = 3;
-constexpr int kDispWarps = 4, kDispStages = 4, kDispChunk = 7168, kDispCtasPerSm = 1;
+constexpr int kDispWarps = 4, kDispStages = 4, kDispChunk = 7168;
 // Dispatch routes whose units have few partners (the relay hops: 2-4 rows a
 // unit at the decode and prefill shapes; one expert group: about k/G) issue
 // fewer stores per load, so more warps keep more loads in flight: 6 warps of
@@ -856,13 +1001,13 @@ constexpr int kDispWarps = 4, kDispStages = 4, kDispChunk = 7168, kDispCtasPerSm
 // 334.5 us) and the G = 4 group schedule 2.6-3.5 % faster, while the flat
 // dispatch (8 partners) was 0.4-0.7 % slower with them.
 constexpr int kFewWarps = 6, kFewStages = 4;
-// Shared memory a dispatch CTA may take: scale rows go through the stages
-// only while every stage, chunk and scale row, fits in it.
+// Shared memory a dispatch CTA's stages may take: scale rows go through the
+// stages only while every stage, chunk and scale row, fits in it.
 constexpr size_t kDispSmemMax = 220 * 1024;
 
 template <int WARPS, int STAGES, int CHUNK, int KMAX, bool GROUPED, int PER_SM, class Route>
 cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, const void* y, void* out,
-                                cudaStream_t stream) {
+                                const MoveShape& sh, cudaStream_t stream) {
     const int row_bytes = nvec * 16;
     const int nch = (row_bytes + CHUNK - 1) / CHUNK;
     const long long units = max_units * nch;
@@ -871,43 +1016,69 @@ cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, 
     const size_t smem = (size_t)WARPS * STAGES * KMAX * CHUNK;
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    const int sms = device_sm_count();
-    const long long need = (units + WARPS - 1) / WARPS;
-    const long long cap = (long long)sms * PER_SM;
-    const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
+    const int grid = capped_grid(units, WARPS, mover_sms(sh.combine_sms), sh.combine_ctas > 0 ? sh.combine_ctas : PER_SM);
     kern<<<grid, WARPS * 32, smem, stream>>>(rt, nch, static_cast<const uint8_t*>(y), static_cast<uint8_t*>(out),
                                              row_bytes);
     return cudaGetLastError();
 }
 
-template <int WARPS, int STAGES, int CHUNK, int PER_SM, class Route, bool SKIP_EMPTY = false>
-cudaError_t launch_dispatch_bulk(const Route& rt, long long max_units, int row_bytes, const void* x, const float* xs,
-                                 void* dst, float* ds, int groups, cudaStream_t stream) {
-    const int nch = (row_bytes + CHUNK - 1) / CHUNK;
+// The dispatch pipelines for one route.  kind: MOE_MOVE_VECTOR or
+// MOE_MOVE_BULK (the caller resolves MOE_MOVE_AUTO); few: the route's units
+// have few partners (bulk default: 6 warps per CTA instead of 4).
+template <class Route, bool SKIP_EMPTY>
+cudaError_t launch_dispatch_route(const Route& rt, long long max_units, int row_bytes, const void* x, const float* xs,
+                                  void* dst, float* ds, int groups, const MoveShape& sh, int kind, bool few,
+                                  cudaStream_t stream) {
+    if (max_units == 0) return cudaSuccess;
+    const int sms = mover_sms(sh.dispatch_sms);
+    if (kind == MOE_MOVE_VECTOR) {
+        // 32-byte vectors when every row and both bases allow them
+        const bool v32 = row_bytes % 32 == 0 && (reinterpret_cast<uintptr_t>(x) & 31) == 0 &&
+                         (reinterpret_cast<uintptr_t>(dst) & 31) == 0;
+        const int span = 7168;
+        const int nspan = (row_bytes + span - 1) / span;
+        const long long units = max_units * nspan;
+        // By default the grid holds up to kVecOversubscribe times the CTAs that
+        // fit at once (about one unit per warp at the workloads here); a tuning
+        // that sets SMs or CTAs per SM gets a persistent grid of that size.
+        const bool persistent = sh.dispatch_sms > 0 || sh.dispatch_ctas > 0;
+        auto launch = [&](auto kern) {
+            const int occ = blocks_per_sm(reinterpret_cast<const void*>(kern), kVecThreads, 0);
+            const int per_sm = persistent ? (sh.dispatch_ctas > 0 ? min(sh.dispatch_ctas, occ) : occ)
+                                          : occ * kVecOversubscribe;
+            kern<<<capped_grid(units, kVecThreads / 32, sms, per_sm), kVecThreads, 0, stream>>>(
+                rt, nspan, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(dst), ds, row_bytes, groups);
+        };
+        if (v32)
+            launch(dispatch_vec_kernel<32, Route>);
+        else
+            launch(dispatch_vec_kernel<16, Route>);
+        return cudaGetLastError();
+    }
+    const int warps = sh.dispatch_warps > 0 ? sh.dispatch_warps : (few ? kFewWarps : kDispWarps);
+    const int stages = sh.dispatch_stages > 0 ? sh.dispatch_stages : (few ? kFewStages : kDispStages);
+    const int chunk = sh.dispatch_chunk > 0 ? sh.dispatch_chunk : kDispChunk;
+    const int nch = (row_bytes + chunk - 1) / chunk;
     const long long units = max_units * nch;
-    if (units == 0) return cudaSuccess;
-    auto kern = dispatch_bulk_kernel<WARPS, STAGES, CHUNK, Route, SKIP_EMPTY>;
+    auto kern = dispatch_bulk_kernel<Route, SKIP_EMPTY>;
     // scale rows through the stages when a bulk copy can move them and they fit
     const int sbytes = (groups > 0 && groups % 4 == 0 &&
-                        (size_t)WARPS * STAGES * (CHUNK + 4 * (size_t)groups) <= kDispSmemMax &&
+                        (size_t)warps * stages * (chunk + 4 * (size_t)groups) <= kDispSmemMax &&
                         (reinterpret_cast<uintptr_t>(xs) & 15) == 0 && (reinterpret_cast<uintptr_t>(ds) & 15) == 0)
                            ? 4 * groups
                            : 0;
-    const size_t smem = (size_t)WARPS * STAGES * (CHUNK + sbytes);
+    const size_t smem = kDispBarBytes + (size_t)warps * stages * (chunk + sbytes);
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    const int sms = device_sm_count();
-    const long long need = (units + WARPS - 1) / WARPS;
-    const long long cap = (long long)sms * PER_SM;
-    const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
-    kern<<<grid, WARPS * 32, smem, stream>>>(rt, nch, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(dst),
-                                             ds, row_bytes, groups, sbytes);
+    kern<<<capped_grid(units, warps, sms, 1), warps * 32, smem, stream>>>(
+        rt, nch, stages, chunk, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(dst), ds, row_bytes, groups,
+        sbytes);
     return cudaGetLastError();
 }
 
 template <int KB, int U, class Route, int ACC = kAccNone>
 cudaError_t launch_combine_t(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
-                             cudaStream_t stream, float* acc = nullptr) {
+                             const MoveShape& sh, cudaStream_t stream, float* acc = nullptr) {
     MoveArgs m{};
     m.nvec = nvec;
     m.chunk_vecs = 32 * U;
@@ -915,30 +1086,33 @@ cudaError_t launch_combine_t(const Route& rt, long long max_units, int nvec, int
     const long long units = max_units * m.nchunks;
     if (units == 0) return cudaSuccess;
     auto kern = combine_kernel<KB, U, Route, ACC>;
-    kern<<<grid_for(kern, units), kMoveThreads, 0, stream>>>(rt, m, nl, static_cast<const uint4*>(y),
-                                                              static_cast<uint4*>(out), acc);
+    const int occ = blocks_per_sm(reinterpret_cast<const void*>(kern), kMoveThreads, 0);
+    kern<<<capped_grid(units, kMoveWarps, mover_sms(sh.combine_sms), occ), kMoveThreads, 0, stream>>>(
+        rt, m, nl, static_cast<const uint4*>(y), static_cast<uint4*>(out), acc);
     return cudaGetLastError();
 }
 
 // Sums at most nl partner rows per unit.  The bulk pipeline's stage holds
 // kCombStageBytes: 8 partners x 512 B, or fewer partners with longer pieces
-// so that a warp keeps the same bytes in flight; more than 8 partners go to
-// the LSU kernel.
+// so that a warp keeps the same bytes in flight; more than 8 partners, or a
+// vector combine asked for by the tuning, go to the LSU kernel.
 constexpr int kCombStageBytes = 8 * kCombChunk;
 
 template <class Route>
 cudaError_t launch_combine_route(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
-                                 cudaStream_t stream) {
+                                 const MoveShape& sh, cudaStream_t stream) {
     constexpr int W = kCombWarps, S = kCombStages, B = kCombStageBytes, C = kCombCtasPerSm;
-    if (nl <= 2) return launch_combine_bulk<W, S, B / 2, 2, false, C, Route>(rt, max_units, nvec, y, out, stream);
-    if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C, Route>(rt, max_units, nvec, y, out, stream);
-    if (nl <= 8) return launch_combine_bulk<W, S, B / 8, 8, false, C, Route>(rt, max_units, nvec, y, out, stream);
-    return launch_combine_t<8, 1, Route>(rt, max_units, nvec, nl, y, out, stream);
+    if (sh.combine_kind != MOE_MOVE_VECTOR) {
+        if (nl <= 2) return launch_combine_bulk<W, S, B / 2, 2, false, C, Route>(rt, max_units, nvec, y, out, sh, stream);
+        if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C, Route>(rt, max_units, nvec, y, out, sh, stream);
+        if (nl <= 8) return launch_combine_bulk<W, S, B / 8, 8, false, C, Route>(rt, max_units, nvec, y, out, sh, stream);
+    }
+    return launch_combine_t<8, 1, Route>(rt, max_units, nvec, nl, y, out, sh, stream);
 }
 
 template <int ACC, class Route>
 cudaError_t launch_combine_packed(const Route& rt, long long max_units, int nvec, const void* y, void* out,
-                                  cudaStream_t stream, float* acc = nullptr) {
+                                  const MoveShape& sh, cudaStream_t stream, float* acc = nullptr) {
     const int row_bytes = nvec * 16;
     const int nspan = ((row_bytes + kPiece - 1) / kPiece + kPackSlots - 1) / kPackSlots;
     const long long units = max_units * nspan;
@@ -948,12 +1122,19 @@ cudaError_t launch_combine_packed(const Route& rt, long long max_units, int nvec
     const size_t smem = (size_t)W * S * kPackSlots * kPiece;
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    const long long need = (units + W - 1) / W;
-    const long long cap = (long long)device_sm_count() * kCombCtasPerSmPacked;
-    const int grid = (int)(need < cap ? (need > 0 ? need : 1) : cap);
+    const int per_sm = sh.combine_ctas > 0 ? sh.combine_ctas : kCombCtasPerSmPacked;
+    const int grid = capped_grid(units, W, mover_sms(sh.combine_sms), per_sm);
+    // Every chain piece starts at a multiple of 1 KB from the row start and a
+    // row is 4h bytes (h % 8 == 0), so a 32-byte aligned base aligns them all.
+    const bool acc_v8 = (reinterpret_cast<uintptr_t>(acc) & 31) == 0;
     kern<<<grid, W * 32, smem, stream>>>(rt, static_cast<const uint8_t*>(y), static_cast<uint8_t*>(out), row_bytes,
-                                         acc);
+                                         acc, acc_v8);
     return cudaGetLastError();
+}
+
+// The dispatch kind a route runs when the tuning leaves it to the library.
+int dispatch_kind(const MoveShape& sh) {
+    return sh.dispatch_kind == MOE_MOVE_BULK ? MOE_MOVE_BULK : MOE_MOVE_VECTOR;
 }
 
 long long relay_units_bound(const MoveArgs& m, const RelayArgs& r) {
@@ -966,68 +1147,73 @@ long long relay_units_bound(const MoveArgs& m, const RelayArgs& r) {
 cudaError_t launch_dispatch(const MoveArgs& m, const void* x, const float* xs, void* recv,
                             float* rs, int groups, cudaStream_t stream) {
     const SlotRoute rt{m.pos, nullptr, m.T, m.k, m.T * m.k};
-    return launch_dispatch_bulk<kDispWarps, kDispStages, kDispChunk, kDispCtasPerSm>(rt, m.T, m.nvec * 16, x, xs, recv,
-                                                                                     rs, groups, stream);
+    return launch_dispatch_route<SlotRoute, false>(rt, m.T, m.nvec * 16, x, xs, recv, rs, groups, m.shape,
+                                                   dispatch_kind(m.shape), false, stream);
 }
 
 cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, void* out,
                            cudaStream_t stream) {
     const SlotRoute rt{m.pos, w, m.T, m.k, m.T * m.k};
-    return launch_combine_route(rt, m.T, m.nvec, m.k, y, out, stream);
+    return launch_combine_route(rt, m.T, m.nvec, m.k, y, out, m.shape, stream);
 }
 
 cudaError_t launch_dispatch_group(const MoveArgs& m, const GroupArgs& ga, const void* x, const float* xs, void* recv,
                                   float* rs, int groups, cudaStream_t stream) {
     const GroupSlotRoute rt{m.pos, nullptr, ga.ids, ga.group, ga.g, m.T, m.k, ga.E, m.T * m.k};
-    return launch_dispatch_bulk<kFewWarps, kFewStages, kDispChunk, kDispCtasPerSm, GroupSlotRoute, true>(
-        rt, m.T, m.nvec * 16, x, xs, recv, rs, groups, stream);
+    return launch_dispatch_route<GroupSlotRoute, true>(rt, m.T, m.nvec * 16, x, xs, recv, rs, groups, m.shape,
+                                                       dispatch_kind(m.shape), true, stream);
 }
 
 cudaError_t launch_combine_group(const MoveArgs& m, const GroupArgs& ga, const void* y, const float* w, float* acc,
                                  void* out, cudaStream_t stream) {
     const GroupSlotRoute rt{m.pos, w, ga.ids, ga.group, ga.g, m.T, m.k, ga.E, m.T * m.k};
-    if (ga.G == 1) return launch_combine_route(rt, m.T, m.nvec, m.k, y, out, stream);
-    if (m.k <= kPackSlots) {  // a group holds about k / G of a token's slots: pack the stages
-        if (ga.g == 0) return launch_combine_packed<kAccFirst>(rt, m.T, m.nvec, y, out, stream, acc);
-        if (ga.g == ga.G - 1) return launch_combine_packed<kAccLast>(rt, m.T, m.nvec, y, out, stream, acc);
-        return launch_combine_packed<kAccMid>(rt, m.T, m.nvec, y, out, stream, acc);
+    const MoveShape& sh = m.shape;
+    if (ga.G == 1) return launch_combine_route(rt, m.T, m.nvec, m.k, y, out, sh, stream);
+    if (m.k <= kPackSlots && sh.combine_kind != MOE_MOVE_VECTOR) {
+        // a group holds about k / G of a token's slots: pack the stages
+        if (ga.g == 0) return launch_combine_packed<kAccFirst>(rt, m.T, m.nvec, y, out, sh, stream, acc);
+        if (ga.g == ga.G - 1) return launch_combine_packed<kAccLast>(rt, m.T, m.nvec, y, out, sh, stream, acc);
+        return launch_combine_packed<kAccMid>(rt, m.T, m.nvec, y, out, sh, stream, acc);
     }
-    // more than 8 slots per token: the LSU kernel carries the chain
-    if (ga.g == 0) return launch_combine_t<8, 1, GroupSlotRoute, kAccFirst>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
+    // more than 8 slots per token (or a vector combine asked for): the LSU kernel carries the chain
+    if (ga.g == 0)
+        return launch_combine_t<8, 1, GroupSlotRoute, kAccFirst>(rt, m.T, m.nvec, m.k, y, out, sh, stream, acc);
     if (ga.g == ga.G - 1)
-        return launch_combine_t<8, 1, GroupSlotRoute, kAccLast>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
-    return launch_combine_t<8, 1, GroupSlotRoute, kAccMid>(rt, m.T, m.nvec, m.k, y, out, stream, acc);
+        return launch_combine_t<8, 1, GroupSlotRoute, kAccLast>(rt, m.T, m.nvec, m.k, y, out, sh, stream, acc);
+    return launch_combine_t<8, 1, GroupSlotRoute, kAccMid>(rt, m.T, m.nvec, m.k, y, out, sh, stream, acc);
 }
 
 cudaError_t launch_relay_dispatch(const MoveArgs& m, const RelayArgs& r, const void* x, const float* xs, void* relay,
                                   float* relay_s, void* recv, float* recv_s, int groups, cudaStream_t stream) {
+    const int kind = dispatch_kind(m.shape);
     // hop 1: each token to its relay rows, one per host it reaches
     const HostRoute hop1{r.relay_pos, m.T, r.H, r.cap};
-    cudaError_t e = launch_dispatch_bulk<kFewWarps, kFewStages, kDispChunk, kDispCtasPerSm>(
-        hop1, m.T, m.nvec * 16, x, xs, relay, relay_s, groups, stream);
+    cudaError_t e = launch_dispatch_route<HostRoute, false>(hop1, m.T, m.nvec * 16, x, xs, relay, relay_s, groups,
+                                                            m.shape, kind, true, stream);
     if (e != cudaSuccess) return e;
     // hop 2: each relay row to the receive rows of its host's slots
     const RelaySlotRoute hop2{r.relay_src, r.slot_relay, m.pos, nullptr, r.n_relay, m.T, m.k, m.T * m.k, r.cap};
-    return launch_dispatch_bulk<kFewWarps, kFewStages, kDispChunk, kDispCtasPerSm>(
-        hop2, relay_units_bound(m, r), m.nvec * 16, relay, relay_s, recv, recv_s, groups, stream);
+    return launch_dispatch_route<RelaySlotRoute, false>(hop2, relay_units_bound(m, r), m.nvec * 16, relay, relay_s,
+                                                        recv, recv_s, groups, m.shape, kind, true, stream);
 }
 
 cudaError_t launch_relay_combine(const MoveArgs& m, const RelayArgs& r, const void* y, const float* w, void* partial,
                                  void* out, cudaStream_t stream) {
+    const MoveShape& sh = m.shape;
     // hop 1: each token's k expert rows, summed per host into its relay rows
     cudaError_t e;
-    if (m.k <= 8) {
+    if (m.k <= 8 && sh.combine_kind != MOE_MOVE_VECTOR) {
         const TokenRelayRoute hop1{m.pos, w, r.slot_relay, m.T, m.k, m.T * m.k, r.cap};
         e = launch_combine_bulk<kCombWarps, kCombStages, kCombChunk, 8, true, kCombCtasPerSm>(hop1, m.T, m.nvec, y,
-                                                                                            partial, stream);
+                                                                                            partial, sh, stream);
     } else {
         const RelaySlotRoute hop1{r.relay_src, r.slot_relay, m.pos, w, r.n_relay, m.T, m.k, m.T * m.k, r.cap};
-        e = launch_combine_route(hop1, relay_units_bound(m, r), m.nvec, m.k, y, partial, stream);
+        e = launch_combine_route(hop1, relay_units_bound(m, r), m.nvec, m.k, y, partial, sh, stream);
     }
     if (e != cudaSuccess) return e;
     // hop 2: each token sums its relay rows in ascending host order
     const HostRoute hop2{r.relay_pos, m.T, r.H, r.cap};
-    return launch_combine_route(hop2, m.T, m.nvec, m.k < r.H ? m.k : r.H, partial, out, stream);
+    return launch_combine_route(hop2, m.T, m.nvec, m.k < r.H ? m.k : r.H, partial, out, sh, stream);
 }
 
 cudaError_t launch_dispatch_quant(const MoveArgs& m0, const void* x, void* recv, float* rs, int h,

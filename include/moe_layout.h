@@ -87,6 +87,44 @@ typedef enum {
 #define MOE_MAX_HIDDEN   (1 << 20)  /* columns of a row: row bytes stay far inside int32 */
 #define MOE_FP8_GROUP    128   /* columns per fp32 scale */
 
+/* Launch shapes of the row movers.  The pages' HybridEP issue lists the
+ * knobs of that library ("Poor HybridEP performance on dual-node 16x B300
+ * GPUs": NUM_OF_TOKENS_PER_CHUNK_*, NUM_SMS_DISPATCH / NUM_SMS_COMBINE,
+ * NUM_BLOCKS_PERMUTE / NUM_BLOCKS_UNPERMUTE); these are their counterparts on
+ * one GPU.  Any field left 0 keeps the library's default; the shapes change
+ * speed only, never a byte of the results.  Out-of-range values give
+ * MOE_ERR_INVALID before anything is enqueued.
+ *   dispatch_kind: MOE_MOVE_AUTO (default), MOE_MOVE_VECTOR (rows through
+ *     registers with 32- or 16-byte vector loads and stores) or MOE_MOVE_BULK
+ *     (rows through shared memory with bulk copies, cp.async.bulk).
+ *   dispatch_sms / combine_sms: SMs the mover's grid covers, 1 .. the GPU's
+ *     SM count (fewer leave SMs to work that overlaps the mover).
+ *   dispatch_ctas_per_sm: vector dispatch CTAs per SM, 1 .. 8 (capped by
+ *     occupancy).
+ *   dispatch_warps, dispatch_stages, dispatch_chunk_bytes: bulk dispatch
+ *     warps per CTA (1 .. 16), shared-memory stages per warp (1 .. 8) and
+ *     bytes of a source row per stage (a multiple of 16, 256 .. 32768); their
+ *     product must fit in 220 KB of shared memory.
+ *   combine_kind: MOE_MOVE_AUTO (default), MOE_MOVE_BULK (partner pieces
+ *     gathered into shared memory by bulk copies; at most 8 partners, more
+ *     fall back to vector) or MOE_MOVE_VECTOR (16-byte vector loads).
+ *   combine_ctas_per_sm: bulk combine CTAs per SM, 1 .. 3. */
+#define MOE_MOVE_AUTO   0
+#define MOE_MOVE_VECTOR 1
+#define MOE_MOVE_BULK   2
+typedef struct moe_tuning {
+    int32_t dispatch_kind;
+    int32_t dispatch_sms;
+    int32_t dispatch_ctas_per_sm;
+    int32_t dispatch_warps;
+    int32_t dispatch_stages;
+    int32_t dispatch_chunk_bytes;
+    int32_t combine_kind;
+    int32_t combine_sms;
+    int32_t combine_ctas_per_sm;
+    int32_t reserved[7];          /* must be 0 */
+} moe_tuning;
+
 /* The problem, fixed for one layer.  Sizes:
  *   num_tokens T >= 0, hidden h in [1, 2^20] (bf16: h % 8 == 0; fp8: h % 128 == 0),
  *   topk k in [1, 32], num_experts E in [1, 1024], num_ranks R in [1, 1024],
@@ -95,7 +133,8 @@ typedef enum {
  * expert_to_rank: device int32 [E] or NULL (then E % R == 0, contiguous
  *   blocks of E/R experts per rank).
  * src_rank_offsets: device int32 [R_src + 1], ascending, 0 .. T, or NULL
- *   (then T % R_src == 0 and each source rank owns T / R_src tokens). */
+ *   (then T % R_src == 0 and each source rank owns T / R_src tokens).
+ * tuning: host moe_tuning or NULL (the defaults); read during each call only. */
 typedef struct moe_problem {
     int32_t num_tokens;
     int32_t hidden;
@@ -107,6 +146,7 @@ typedef struct moe_problem {
     int32_t dtype;                      /* moe_dtype */
     const int32_t* expert_to_rank;      /* device [E] or NULL */
     const int32_t* src_rank_offsets;    /* device [R_src + 1] or NULL */
+    const moe_tuning* tuning;           /* host, or NULL for the defaults */
 } moe_problem;
 
 /* Layout outputs, all caller-allocated device arrays (int32 unless noted).

@@ -205,3 +205,38 @@ def test_host_stats_rejected_on_host(moe):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_stats_device(p, _Fake(0x50000), _Fake(0x40004), stream=0)
     assert ei.value.code == moe.MOE_ERR_ALIGN
+
+
+def test_tuning_checked_on_host(moe):
+    """moe_tuning (launch shapes of the movers): every out-of-range field is
+    rejected by every call before anything is enqueued; defaults pass."""
+    import ctypes
+    p = _p(moe)
+    base = moe.moe_workspace_bytes(p)
+    for good in (dict(), dict(dispatch_kind=moe.MOE_MOVE_BULK, dispatch_warps=16, dispatch_stages=3,
+                              dispatch_chunk_bytes=4096),
+                 dict(dispatch_kind=moe.MOE_MOVE_VECTOR, dispatch_sms=1, dispatch_ctas_per_sm=8),
+                 dict(combine_kind=moe.MOE_MOVE_VECTOR, combine_sms=152, combine_ctas_per_sm=3)):
+        p.tuning = moe.Tuning(**good)
+        assert moe.moe_workspace_bytes(p) == base
+    for bad in (dict(dispatch_kind=3), dict(combine_kind=-1), dict(dispatch_sms=-1), dict(combine_sms=-4),
+                dict(dispatch_ctas_per_sm=9), dict(dispatch_warps=17), dict(dispatch_stages=9),
+                dict(dispatch_chunk_bytes=100), dict(dispatch_chunk_bytes=1000), dict(dispatch_chunk_bytes=32784),
+                dict(dispatch_warps=16, dispatch_stages=8, dispatch_chunk_bytes=7168), dict(combine_ctas_per_sm=4)):
+        p.tuning = moe.Tuning(**bad)
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_workspace_bytes(p)
+        assert ei.value.code == moe.MOE_ERR_INVALID, bad
+    # reserved words must stay zero
+    p.tuning = moe.Tuning()
+    pc = p.c()
+    pc._tuning.reserved[3] = 1
+    n = ctypes.c_size_t(0)
+    assert moe.load_library().moe_workspace_bytes(ctypes.byref(pc), ctypes.byref(n)) == moe.MOE_ERR_INVALID
+
+
+def test_tuning_from_environment(moe):
+    t = moe.Tuning.from_env({"MOE_DISPATCH_KIND": "bulk", "MOE_DISPATCH_WARPS": "6", "MOE_COMBINE_SMS": "76",
+                             "MOE_COMBINE_KIND": "vector", "UNRELATED": "1"})
+    assert t.dispatch_kind == moe.MOE_MOVE_BULK and t.dispatch_warps == 6
+    assert t.combine_kind == moe.MOE_MOVE_VECTOR and t.combine_sms == 76 and t.dispatch_sms == 0

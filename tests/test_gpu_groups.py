@@ -31,13 +31,18 @@ def _groups(case, G):
     return grp
 
 
-def _run_groups(case, G, grp, check=None, streams=None):
+def _run_groups(case, G, grp, check=None, streams=None, acc_offset=0):
     """Layout, then per group: dispatch, combine.  `check(g, acc)` runs after
     each group's combine when given.  With `streams` = (a, b), dispatches run
-    on a and combines on b, each combine after its group's dispatch."""
+    on a and combines on b, each combine after its group's dispatch.  The fp32
+    chain starts acc_offset floats into its allocation (4: 16-byte but not
+    32-byte aligned, the smallest alignment the call accepts)."""
     import torch
     m, c, w = case.moe, case, case.w
-    acc = torch.empty((w.T, w.h), dtype=torch.float32, device=case.dev) if G > 1 else None
+    acc = None
+    if G > 1:
+        buf = torch.empty(w.T * w.h + acc_offset, dtype=torch.float32, device=case.dev)
+        acc = buf[acc_offset:].view(w.T, w.h)
     m.moe_layout(c.prob, c.ids_d, c.ws, c.lay)
     if streams is not None:
         sa, sb = streams
@@ -62,7 +67,7 @@ def _run_groups(case, G, grp, check=None, streams=None):
     return m.moe_status(c.ws)
 
 
-def _group_parity(oracle, case, G, e2r=None, streams=None):
+def _group_parity(oracle, case, G, e2r=None, streams=None, acc_offset=0):
     import torch
     w = case.w
     prob, keep = oracle_problem(oracle, w, case.src_off, e2r)
@@ -93,7 +98,7 @@ def _group_parity(oracle, case, G, e2r=None, streams=None):
                 f"group {g}: fp32 accumulator differs"
 
     case.poison()
-    code, bits = _run_groups(case, G, grp, check, streams)
+    code, bits = _run_groups(case, G, grp, check, streams, acc_offset)
     assert code == 0 and bits == 0
     got = case.recv.view(torch.uint8).cpu().numpy()
     assert np.array_equal(got.reshape(-1), np.ascontiguousarray(want_recv).view(np.uint8).reshape(-1))
@@ -139,6 +144,15 @@ def test_group_custom_placement(dev, oracle_mod):
     rng = np.random.default_rng(21)
     e2r = rng.integers(0, w.R - 2, size=w.E).astype(np.int32)
     _group_parity(oracle_mod, Case(w, dev, expert_to_rank=e2r, y_on_device=False), 3, e2r=e2r)
+
+
+@pytest.mark.parametrize("acc_offset", [4, 8])
+def test_group_chain_alignment(dev, oracle_mod, acc_offset):
+    """The fp32 chain moves as 32-byte accesses when its rows are 32-byte
+    aligned and as 16-byte halves otherwise: a chain 16 bytes (and 32 bytes)
+    into its allocation gives the same accumulators and output."""
+    w = mw.scaled(mw.WORKLOADS["decode-EP32-r8"], T=640, R_src=8)
+    _group_parity(oracle_mod, Case(w, dev, y_on_device=False), 4, acc_offset=acc_offset)
 
 
 def test_group_overlap_on_two_streams(dev, oracle_mod):
