@@ -51,6 +51,18 @@ constexpr int kAccNone = 0, kAccFirst = 1, kAccMid = 2, kAccLast = 3;
 // per lane (the rows a dispatch writes, the rows a combine sums, with their
 // weights).  partner() is called by all 32 lanes of a warp with the same u;
 // live is false for a u past the end, which yields no partners.
+//
+// The lookup has two halves so that a mover can run it one unit ahead:
+// raw() issues the loads of unit u's partners without using their values,
+// resolve() turns them into (row, weight) when they are needed.  partner()
+// is the two in a row.  Routes whose lookup needs its own values at once
+// (a relay row's token, a token's hosts) do it all in raw().
+
+struct RawPartner {
+    int row;    // partner row as loaded (-1: none)
+    float w;    // its weight
+    int key;    // route-specific: the slot's expert (GroupSlotRoute)
+};
 
 // Flat: unit = token t; lane j < k: receive row pos[t, j], gate weight w[t, j].
 struct SlotRoute {
@@ -60,15 +72,21 @@ struct SlotRoute {
     int rows;        // receive rows: T * k
     __device__ __forceinline__ long long units() const { return T; }
     __device__ __forceinline__ int self_row(long long u) const { return (int)u; }
-    __device__ __forceinline__ void partner(long long u, bool live, int lane, int& row, float& wt) const {
-        row = -1;
-        wt = 0.0f;
+    __device__ __forceinline__ RawPartner raw(long long u, bool live, int lane) const {
+        RawPartner r{-1, 0.0f, 0};
         if (live && lane < k) {
             const size_t i = (size_t)u * k + lane;
-            row = pos[i];
-            if (w != nullptr) wt = w[i];
-            if (row < 0 || row >= rows) row = -1;
+            r.row = pos[i];
+            if (w != nullptr) r.w = w[i];
         }
+        return r;
+    }
+    __device__ __forceinline__ void resolve(const RawPartner& r, int& row, float& wt) const {
+        row = (r.row < 0 || r.row >= rows) ? -1 : r.row;
+        wt = r.w;
+    }
+    __device__ __forceinline__ void partner(long long u, bool live, int lane, int& row, float& wt) const {
+        resolve(raw(u, live, lane), row, wt);
     }
 };
 
@@ -100,6 +118,15 @@ struct HostRoute {
         const int vlo = __shfl_sync(kAll, lo, from), vhi = __shfl_sync(kAll, hi, from);
         row = lane < n ? (lane < nlo ? vlo : vhi) : -1;
         wt = row >= 0 ? 1.0f : 0.0f;
+    }
+    __device__ __forceinline__ RawPartner raw(long long u, bool live, int lane) const {
+        RawPartner r{-1, 0.0f, 0};
+        partner(u, live, lane, r.row, r.w);
+        return r;
+    }
+    __device__ __forceinline__ void resolve(const RawPartner& r, int& row, float& wt) const {
+        row = r.row;
+        wt = r.w;
     }
 };
 
@@ -133,7 +160,9 @@ struct TokenRelayRoute {
 };
 
 // One expert group of the flat path: unit = token t; lane j < k: receive row
-// pos[t, j] with weight w[t, j] when expert ids[t, j] is in group g.
+// pos[t, j] with weight w[t, j] when expert ids[t, j] is in group g.  raw()
+// loads the id, the row and the weight side by side (the row and weight of a
+// slot outside the group are loaded too, and dropped by resolve()).
 struct GroupSlotRoute {
     const int32_t* pos;
     const float* w;             // NULL for dispatch
@@ -144,18 +173,23 @@ struct GroupSlotRoute {
     int rows;                   // receive rows: T * k
     __device__ __forceinline__ long long units() const { return T; }
     __device__ __forceinline__ int self_row(long long u) const { return (int)u; }
-    __device__ __forceinline__ void partner(long long u, bool live, int lane, int& row, float& wt) const {
-        row = -1;
-        wt = 0.0f;
+    __device__ __forceinline__ RawPartner raw(long long u, bool live, int lane) const {
+        RawPartner r{-1, 0.0f, -1};
         if (live && lane < k) {
             const size_t i = (size_t)u * k + lane;
-            const int e = ids[i];
-            if (e >= 0 && e < E && group[e] == g) {
-                row = pos[i];
-                if (w != nullptr) wt = w[i];
-                if (row < 0 || row >= rows) row = -1;
-            }
+            r.key = ids[i];
+            r.row = pos[i];
+            if (w != nullptr) r.w = w[i];
         }
+        return r;
+    }
+    __device__ __forceinline__ void resolve(const RawPartner& r, int& row, float& wt) const {
+        const bool in = r.key >= 0 && r.key < E && __ldg(group + r.key) == g;
+        row = (in && r.row >= 0 && r.row < rows) ? r.row : -1;
+        wt = in ? r.w : 0.0f;
+    }
+    __device__ __forceinline__ void partner(long long u, bool live, int lane, int& row, float& wt) const {
+        resolve(raw(u, live, lane), row, wt);
     }
 };
 
@@ -191,6 +225,15 @@ struct RelaySlotRoute {
                 }
             }
         }
+    }
+    __device__ __forceinline__ RawPartner raw(long long u, bool live, int lane) const {
+        RawPartner r{-1, 0.0f, 0};
+        partner(u, live, lane, r.row, r.w);
+        return r;
+    }
+    __device__ __forceinline__ void resolve(const RawPartner& r, int& row, float& wt) const {
+        row = r.row;
+        wt = r.w;
     }
 };
 
@@ -515,19 +558,31 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
     }
 }
 
-// Packed combine: a stage always holds kPackSlots pieces of kPiece bytes,
-// filled with as many column pieces of the unit's partners as fit.  A unit is
-// (output row, span of kPackSlots pieces); with n partners each stage takes
-// floor(kPackSlots / n) pieces of every partner (a round), so a unit with one
-// or two partners fills its stages as fully as one with eight.  Rounds are
-// issued in order through the warp's stages; the partners of the next unit
-// are looked up while the current unit's rounds are in flight.  ACC carries an
-// fp32 chain across launches (kAcc*); a round reads and writes the chain's
-// values directly (bringing them through the stage left fewer slots for the
-// partners and measured slower).  At most kPackSlots partners (compacted,
-// ascending lane order, so each sum keeps the route's partner order).
+// Packed combine: a stage holds kPackSlots pieces of kPiece bytes, filled
+// with as many column pieces of the unit's partners as fit.  A unit is
+// (output row, span of kPackSlots pieces); with n partners a round takes
+// `per` pieces of every partner (per = floor(kPackSlots / n)), so a unit with
+// one or two partners fills its stages as fully as one with eight.  Rounds
+// flow in order through the warp's stages; the partners of the next unit are
+// looked up while the current unit's rounds are in flight.
+//
+// ACC carries an fp32 chain across launches (kAcc*): the first group writes
+// it, middle groups read and write it, the last reads it and writes the bf16
+// row.  Chain values are read from registers' view of 32 contiguous bytes a
+// lane and written as 32-byte stores (16-byte halves when the chain is only
+// 16-byte aligned).  Bringing them through the stage (a separate chain area
+// after the y slots, so half the stages fit an SM) and prefetching a whole
+// round into registers (two CTAs of 8 warps instead of three) both measured
+// slower.  At most kPackSlots partners (compacted, ascending lane order, so
+// each sum keeps the route's partner order).
 constexpr int kPiece = 512, kPackSlots = 8;
-constexpr int kCombCtasPerSmPacked = 3;  // registers capped so that 3 CTAs of 8 warps fit an SM
+constexpr int kCombCtasPerSmPacked = 3;  // first group: registers capped so that 3 CTAs of 8 warps fit an SM
+
+template <int ACC> struct PackedShape {
+    static constexpr bool kChainIn = ACC == kAccMid || ACC == kAccLast;
+    static constexpr int kWarps = 8, kStages = 2, kCtasPerSm = kCombCtasPerSmPacked;
+    static constexpr int kStageBytes = kPackSlots * kPiece;
+};
 
 __device__ __forceinline__ void compact_partners(int lane, int p, float w, int& cp, float& cw, int& n) {
     const unsigned m = __ballot_sync(kAll, p >= 0);
@@ -543,11 +598,14 @@ __device__ __forceinline__ void compact_partners(int lane, int p, float w, int& 
     }
 }
 
-template <int WARPS, int STAGES, int ACC, class Route>
-__global__ void __launch_bounds__(WARPS * 32, kCombCtasPerSmPacked)
+template <int ACC, class Route>
+__global__ void __launch_bounds__(PackedShape<ACC>::kWarps * 32, PackedShape<ACC>::kCtasPerSm)
 combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __restrict__ out, int row_bytes,
                       float* __restrict__ acc_rows, bool acc_v8) {
-    constexpr int STAGE_BYTES = kPackSlots * kPiece;
+    using Sh = PackedShape<ACC>;
+    constexpr int WARPS = Sh::kWarps, STAGES = Sh::kStages, STAGE_BYTES = Sh::kStageBytes;
+    constexpr bool CHAIN_IN = Sh::kChainIn;
+    constexpr bool CHAIN_AHEAD = ACC == kAccMid;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[WARPS][STAGES];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -566,6 +624,7 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
     const long long units = rt.units() * nspan;
     const long long nw = (long long)gridDim.x * WARPS;
     const long long gw = (long long)blockIdx.x * WARPS + warp;
+    const size_t chain_row = (size_t)(row_bytes / 2);           // floats of a chain row
 
     // The unit whose rounds are being issued, and the next one.
     struct Meta {
@@ -648,14 +707,42 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
             if (!pending[s] || failed) continue;
+            const int n = sn[s];
+            const long long orow = rt.self_row(su[s] / nspan);
+            // Middle groups load the chain values of the round's first piece
+            // before the wait for the stage, and those of piece i + 1 before
+            // piece i is summed and stored, so each load's latency overlaps other
+            // work (G = 4 at prefill-fp8 on GB300: the two middle groups 208.9 and
+            // 213.0 -> 196.6 and 204.8 us).  The last group, with about twice the
+            // partners, loads each piece's values straight into its sums inside
+            // the lane guard (ahead, or loaded outside the guard, it took 319.5
+            // instead of 303-305 us).  The piece loop is left to the compiler:
+            // unrolled over pieces and partners the code outgrows the instruction
+            // cache (a first group ran 1.6 times slower).
+            const float* chain0 = acc_rows + (size_t)orow * chain_row + 8 * lane;
+            auto load_chain = [&](int piece, float (&c)[8]) {
+                if (lane < min(kPiece, row_bytes - piece * kPiece) / 16) {
+                    const float* a = chain0 + (size_t)piece * (kPiece / 2);
+                    if (acc_v8) {
+                        ld_stream_v8f(a, c);
+                    } else {
+                        const uint4 a0 = ld_stream_v4(reinterpret_cast<const uint4*>(a));
+                        const uint4 a1 = ld_stream_v4(reinterpret_cast<const uint4*>(a + 4));
+                        c[0] = __uint_as_float(a0.x); c[1] = __uint_as_float(a0.y);
+                        c[2] = __uint_as_float(a0.z); c[3] = __uint_as_float(a0.w);
+                        c[4] = __uint_as_float(a1.x); c[5] = __uint_as_float(a1.y);
+                        c[6] = __uint_as_float(a1.z); c[7] = __uint_as_float(a1.w);
+                    }
+                }
+            };
+            float chain_next[8];
+            if constexpr (CHAIN_AHEAD) load_chain(sp0[s], chain_next);
             if (!__all_sync(kAll, mbar_wait_bounded(bar0 + 8 * s, ph[s] & 1u, kWaitLimitNs))) {
                 failed = true;
                 continue;
             }
             ph[s] += 1;
             pending[s] = false;
-            const int n = sn[s];
-            const long long orow = rt.self_row(su[s] / nspan);
             const uint32_t st = stage0 + s * STAGE_BYTES;
             float wj[kPackSlots];
 #pragma unroll
@@ -664,16 +751,15 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
                 const int piece = sp0[s] + i;
                 const int pb = min(kPiece, row_bytes - piece * kPiece);
                 uint4* o = reinterpret_cast<uint4*>(out + (size_t)orow * row_bytes + (size_t)piece * kPiece);
-                float* arow = ACC == kAccNone ? nullptr
-                                              : acc_rows + (size_t)orow * (row_bytes / 2) + (size_t)piece * (kPiece / 2);
-                // Lane v's 8 chain values are 32 contiguous bytes.  With a 32-byte
-                // aligned chain they move as one 256-bit access, so a warp request
-                // covers 1 KB of whole sectors; otherwise as two 16-byte halves 32
-                // bytes apart (each request then half-fills the sectors it touches).
+                float* arow = ACC == kAccNone ? nullptr : acc_rows + (size_t)orow * chain_row + (size_t)piece * (kPiece / 2);
+                float acc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] = CHAIN_AHEAD ? chain_next[q] : 0.0f;
+                if (CHAIN_AHEAD && i + 1 < scnt[s]) load_chain(piece + 1, chain_next);
+                // Lane v's 8 chain values are 32 contiguous bytes.
                 if (lane < pb / 16) {
                     const int v = lane;
-                    float acc[8];
-                    if constexpr (ACC == kAccMid || ACC == kAccLast) {
+                    if (CHAIN_IN && !CHAIN_AHEAD) {
                         if (acc_v8) {
                             ld_stream_v8f(arow + 8 * v, acc);
                         } else {
@@ -684,14 +770,13 @@ combine_packed_kernel(const Route rt, const uint8_t* __restrict__ y, uint8_t* __
                             acc[4] = __uint_as_float(a1.x); acc[5] = __uint_as_float(a1.y);
                             acc[6] = __uint_as_float(a1.z); acc[7] = __uint_as_float(a1.w);
                         }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
                     }
 #pragma unroll
                     for (int j = 0; j < kPackSlots; ++j)
                         if (j < n) fma_bf16x8(acc, wj[j], lds_v4(st + (i * n + j) * kPiece + v * 16));
                     if constexpr (ACC == kAccFirst || ACC == kAccMid) {
+                        // with a 32-byte aligned chain, one 256-bit store: a warp
+                        // request covers 1 KB of whole sectors
                         if (acc_v8) {
                             st_v8f(arow + 8 * v, acc);
                         } else {
@@ -917,15 +1002,16 @@ dispatch_vec_kernel(const Route rt, const int nspan, const uint8_t* __restrict__
     const long long units = rt.units() * nspan;
     const long long nw = (long long)gridDim.x * WPB;
     long long u = (long long)blockIdx.x * WPB + (threadIdx.x >> 5);
-    float unused;
-    int pnext;  // partners of the warp's next unit, looked up one unit ahead
-    rt.partner(u / nspan, u < units, lane, pnext, unused);
+    // partners of the warp's next unit, looked up one unit ahead: the loads
+    // go out a unit early and are used only when that unit's turn comes
+    RawPartner next = rt.raw(u / nspan, u < units, lane);
     for (; u < units; u += nw) {
         const long long ui = u / nspan;
         const int c = (int)(u - ui * nspan);
-        const int p = pnext;
-        // the next unit's lookup goes out now; its loads overlap this unit's stores
-        rt.partner((u + nw) / nspan, u + nw < units, lane, pnext, unused);
+        int p;
+        float unused;
+        rt.resolve(next, p, unused);
+        next = rt.raw((u + nw) / nspan, u + nw < units, lane);
         const unsigned pm = __ballot_sync(kAll, p >= 0);
         if (pm == 0u) continue;  // nothing to write
         const size_t srow = (size_t)rt.self_row(ui);
@@ -1113,22 +1199,22 @@ cudaError_t launch_combine_route(const Route& rt, long long max_units, int nvec,
 template <int ACC, class Route>
 cudaError_t launch_combine_packed(const Route& rt, long long max_units, int nvec, const void* y, void* out,
                                   const MoveShape& sh, cudaStream_t stream, float* acc = nullptr) {
+    using Sh = PackedShape<ACC>;
     const int row_bytes = nvec * 16;
     const int nspan = ((row_bytes + kPiece - 1) / kPiece + kPackSlots - 1) / kPackSlots;
     const long long units = max_units * nspan;
     if (units == 0) return cudaSuccess;
-    constexpr int W = kCombWarps, S = kCombStages;
-    auto kern = combine_packed_kernel<W, S, ACC, Route>;
-    const size_t smem = (size_t)W * S * kPackSlots * kPiece;
+    auto kern = combine_packed_kernel<ACC, Route>;
+    const size_t smem = (size_t)Sh::kWarps * Sh::kStages * Sh::kStageBytes;
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    const int per_sm = sh.combine_ctas > 0 ? sh.combine_ctas : kCombCtasPerSmPacked;
-    const int grid = capped_grid(units, W, mover_sms(sh.combine_sms), per_sm);
+    const int per_sm = sh.combine_ctas > 0 ? min(sh.combine_ctas, Sh::kCtasPerSm) : Sh::kCtasPerSm;
+    const int grid = capped_grid(units, Sh::kWarps, mover_sms(sh.combine_sms), per_sm);
     // Every chain piece starts at a multiple of 1 KB from the row start and a
     // row is 4h bytes (h % 8 == 0), so a 32-byte aligned base aligns them all.
     const bool acc_v8 = (reinterpret_cast<uintptr_t>(acc) & 31) == 0;
-    kern<<<grid, W * 32, smem, stream>>>(rt, static_cast<const uint8_t*>(y), static_cast<uint8_t*>(out), row_bytes,
-                                         acc, acc_v8);
+    kern<<<grid, Sh::kWarps * 32, smem, stream>>>(rt, static_cast<const uint8_t*>(y), static_cast<uint8_t*>(out),
+                                                  row_bytes, acc, acc_v8);
     return cudaGetLastError();
 }
 
