@@ -107,6 +107,22 @@ WsLayout ws_layout(const Dims& d) { return moe::make_ws_layout(d.T, d.E, d.R, d.
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+int64_t row_bytes(const Dims& d);
+
+// The layout kernels' arguments for a problem and workspace (ids and outputs
+// are the caller's to fill in).
+moe::LayoutArgs layout_args(const moe_problem* problem, const Dims& d, const void* workspace) {
+    moe::LayoutArgs a{};
+    a.expert_to_rank = problem->expert_to_rank;
+    a.src_offsets = problem->src_rank_offsets;
+    a.T = d.T; a.k = d.k; a.E = d.E; a.R = d.R; a.P = d.P; a.H = d.H; a.Rs = d.Rs;
+    a.h = d.h;
+    a.row_bytes = row_bytes(d);
+    a.ws = static_cast<uint8_t*>(const_cast<void*>(workspace));
+    a.wl = ws_layout(d);
+    return a;
+}
+
 // The code a set of device status bits stands for (timeouts first).
 int code_of_status(uint32_t bits) {
     if (bits & MOE_STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
@@ -150,15 +166,8 @@ int moe_layout(const moe_problem* problem, const int32_t* ids, void* workspace,
     if (!layout_complete(layout, d.T) || workspace == nullptr || (d.T > 0 && ids == nullptr))
         return MOE_ERR_INVALID;
     if (!aligned(workspace, 256) || !aligned(ids, 4) || !aligned(layout->stats, 8)) return MOE_ERR_ALIGN;
-    moe::LayoutArgs a{};
+    moe::LayoutArgs a = layout_args(problem, d, workspace);
     a.ids = ids;
-    a.expert_to_rank = problem->expert_to_rank;
-    a.src_offsets = problem->src_rank_offsets;
-    a.T = d.T; a.k = d.k; a.E = d.E; a.R = d.R; a.P = d.P; a.H = d.H; a.Rs = d.Rs;
-    a.h = d.h;
-    a.row_bytes = row_bytes(d);
-    a.ws = static_cast<uint8_t*>(workspace);
-    a.wl = ws_layout(d);
     a.out = *layout;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     rc = cuda_status(cudaMemsetAsync(workspace, 0, a.wl.acc_bytes, s));
@@ -173,17 +182,22 @@ int moe_stats(const moe_problem* problem, const moe_layout_t* layout, const void
     const int rc = check_problem(problem, &d);
     if (rc != MOE_OK) return rc;
     if (layout == nullptr || host_stats == nullptr) return MOE_ERR_INVALID;
-    const WsLayout wl = ws_layout(d);
-    // The layout call left the finished record in the workspace and, when
-    // asked, in layout->stats as well.
-    const void* src = layout->stats;
-    if (src == nullptr) {
-        if (workspace == nullptr) return MOE_ERR_INVALID;
-        if (!aligned(workspace, 256)) return MOE_ERR_ALIGN;
-        src = static_cast<const uint8_t*>(workspace) + wl.stats;
-    }
-    if (!aligned(src, 8) || !aligned(host_stats, 8)) return MOE_ERR_ALIGN;
+    if (!aligned(host_stats, 8)) return MOE_ERR_ALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const WsLayout wl = ws_layout(d);
+    const void* src = nullptr;
+    if (workspace != nullptr) {
+        // the record, made now from the counters the layout left in the workspace
+        if (!aligned(workspace, 256)) return MOE_ERR_ALIGN;
+        moe::LayoutArgs a = layout_args(problem, d, workspace);
+        if (moe::launch_stats_compute(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+        src = static_cast<const uint8_t*>(workspace) + wl.stats;
+    } else {
+        // no workspace (moe_layout_noalloc): the record the layout wrote itself
+        if (layout->stats == nullptr) return MOE_ERR_INVALID;
+        if (!aligned(layout->stats, 8)) return MOE_ERR_ALIGN;
+        src = layout->stats;
+    }
     cudaError_t e = cudaMemcpyAsync(host_stats, src, 8 * wl.stats_words, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -198,10 +212,9 @@ int moe_stats_device(const moe_problem* problem, const void* workspace, int64_t*
     if (rc != MOE_OK) return rc;
     if (workspace == nullptr || device_stats == nullptr) return MOE_ERR_INVALID;
     if (!aligned(workspace, 256) || !aligned(device_stats, 8)) return MOE_ERR_ALIGN;
-    // The layout kernels leave the finished record in the workspace.
-    const WsLayout wl = ws_layout(d);
-    return cuda_status(moe::launch_stats_copy(static_cast<const uint8_t*>(workspace), wl, device_stats,
-                                              reinterpret_cast<cudaStream_t>(stream)));
+    moe::LayoutArgs a = layout_args(problem, d, workspace);
+    a.out.stats = device_stats;
+    return cuda_status(moe::launch_stats_compute(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_dispatch(const moe_problem* problem, const moe_layout_t* layout, const void* x,

@@ -417,7 +417,7 @@ inline int blocks_per_sm(const void* kernel, int threads, size_t smem) {
 // ---- launchers (defined in the kernel files) -----------------------------
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s);
-cudaError_t launch_stats_copy(const uint8_t* ws, const WsLayout& wl, int64_t* out, cudaStream_t s);
+cudaError_t launch_stats_compute(const LayoutArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch(const MoveArgs& m, const void* x, const float* xs, void* recv,
                             float* rs, int groups, cudaStream_t s);
 cudaError_t launch_combine(const MoveArgs& m, const void* y, const float* w, void* out,

@@ -20,8 +20,10 @@
 //         parallel: no block waits on another.  Every block derives the
 //         expert totals (the sum of the group rows) and the expert and rank
 //         offsets itself (cheap: O(E + R)).  One extra block writes the counts
-//         and offsets out, and the statistics record into the workspace (so
-//         moe_stats is a plain copy), while the others write positions.
+//         and offsets out -- and, when the caller passes layout->stats, the
+//         statistics record -- while the others write positions.  Without
+//         layout->stats the record comes later from stats_compute_kernel,
+//         which needs only the counters left in the workspace.
 //
 // Where the whole grid fits on the GPU at once, both phases run in one
 // cooperative kernel: each block counts, ranks its own slots (ids only),
@@ -722,7 +724,10 @@ __device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b) {
             if (lane == 31) a.out.host_offset[a.H] = low_total + x1;
         }
         __syncthreads();
-        write_stats(a, sm.tot, sm.rfill, stat_in);
+        // The statistics record only when the caller asked for it with the
+        // layout; otherwise the kernel ends with its slot blocks and
+        // stats_compute_kernel can make the record later, beside the dispatch.
+        if (a.out.stats != nullptr) write_stats(a, sm.tot, sm.rfill, stat_in);
         return;
     }
 
@@ -795,12 +800,33 @@ __global__ void layout_empty_kernel(const LayoutArgs a) {
     write_stats(a, a.out.expert_count, a.out.rank_count, in);
 }
 
-// Copies the statistics record out of the workspace (one small block; it
-// starts under programmatic dependent launch and waits for the layout).
-__global__ void __launch_bounds__(256) stats_copy_kernel(const int64_t* rec, int64_t* out, int words) {
-    pdl_launch_dependents();
-    pdl_wait();
-    for (int i = threadIdx.x; i < words; i += blockDim.x) out[i] = __ldcg(rec + i);
+// The statistics record of the last layout made with the workspace, from the
+// counters that layout left there (one block): expert totals are the sums of
+// the group rows, rank slots the sums of their experts' totals.  Writes the
+// record to the workspace and, when a.out.stats is set, there too.  It reads
+// nothing the dispatch or combine write, so it can run beside them.
+__global__ void __launch_bounds__(kRankThreads) stats_compute_kernel(const LayoutArgs a) {
+    extern __shared__ int32_t smem[];
+    int32_t* tot = smem;           // [E]
+    int32_t* rcount = smem + a.E;  // [R]
+    const int tid = threadIdx.x;
+    const int32_t* g_group = reinterpret_cast<const int32_t*>(a.ws + a.wl.group);
+    StatIn in;
+    load_stat_inputs(a, in);  // counters: their loads overlap the sums below
+    for (int e = tid; e < a.E; e += blockDim.x) {
+        int t = 0;
+        for (int g = 0; g < a.wl.groups; ++g) t += __ldcg(g_group + (size_t)g * a.E + e);
+        tot[e] = t;
+    }
+    for (int r = tid; r < a.R; r += blockDim.x) rcount[r] = 0;
+    __syncthreads();
+    uint32_t st_unused = 0;
+    for (int e = tid; e < a.E; e += blockDim.x) {
+        const int c = tot[e];
+        if (c) atomicAdd(&rcount[rank_of_expert(a, e, &st_unused)], c);
+    }
+    __syncthreads();
+    write_stats(a, tot, rcount, in);
 }
 
 template <typename K>
@@ -851,9 +877,12 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
     return a.k <= 8 ? launch_layout_k<8>(a, stream) : launch_layout_k<32>(a, stream);
 }
 
-cudaError_t launch_stats_copy(const uint8_t* ws, const WsLayout& wl, int64_t* out, cudaStream_t stream) {
-    return launch_pdl(stats_copy_kernel, dim3(1), dim3(256), 0, stream,
-                      reinterpret_cast<const int64_t*>(ws + wl.stats), out, (int)wl.stats_words);
+cudaError_t launch_stats_compute(const LayoutArgs& a, cudaStream_t stream) {
+    const size_t smem = sizeof(int32_t) * ((size_t)a.E + a.R);
+    const cudaError_t e = allow_smem(stats_compute_kernel, smem);
+    if (e != cudaSuccess) return e;
+    stats_compute_kernel<<<1, kRankThreads, smem, stream>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -165,8 +165,12 @@ typedef struct moe_layout_t {
     int32_t* pos;            /* [T, k] receive row of slot (t, j) */
     int32_t* recv_src;       /* [T*k]  t*k + j of the slot held by each row */
     int64_t* stats;          /* optional [moe_stats_words()] int64: when not
-                                NULL, moe_layout also writes the statistics
-                                record here (what moe_stats would copy out) */
+                                NULL, moe_layout also computes the statistics
+                                record and writes it here (one more block of
+                                the layout kernel, which then ends when the
+                                record is written); when NULL, the layout
+                                skips it and moe_stats_device / moe_stats
+                                compute it later from the workspace */
 } moe_layout_t;
 
 /* Bytes of workspace needed for a problem ("Balancing and Beyond" section
@@ -180,7 +184,8 @@ int moe_workspace_bytes(const moe_problem* problem, size_t* bytes);
  *   ids: device int32 [T, k], k distinct experts per token
  *        ("Balancing and Beyond" section 3.2: k distinct experts).
  *   workspace: device, moe_workspace_bytes() bytes, 256-byte aligned; it also
- *        keeps the counters moe_stats reads, until the next moe_layout.
+ *        keeps the counters the statistics record is made from, until the
+ *        next moe_layout with it.
  * The mask implements Mode 2 de-redundancy (section 3.2): one copy per token
  * and host, relayed through the same-index GPU of that host. */
 int moe_layout(const moe_problem* problem, const int32_t* ids, void* workspace,
@@ -241,10 +246,11 @@ enum { MOE_DST_SLOTS = 0, MOE_DST_TOKENS, MOE_DST_SELF, MOE_DST_LOCAL, MOE_DST_R
  * The quantities are those of "Balancing and Beyond", sections 1 (bytes that
  * leave each rank: tokens x k x h x 2 B) and 2 (imbalance ratio), with the
  * Mode 0/1/2 copy counts of section 3.2; the record format is above.
- *   layout: the layout made by moe_layout; when layout->stats is set, the
- *     record is read from there (so a moe_layout_noalloc caller, which has no
- *     workspace, passes workspace = NULL), otherwise from the workspace.
- *   workspace: the workspace that moe_layout used, or NULL (see layout).
+ *   layout: the layout made by moe_layout.
+ *   workspace: the workspace that moe_layout used: the record is computed
+ *     from the counters it holds (one small kernel), then copied.  Or NULL
+ *     (a moe_layout_noalloc caller has none): the record is copied from
+ *     layout->stats, which must then have been set for the layout call.
  *   host_stats: host int64 [moe_stats_words()] (pageable or pinned).
  * Returns, after the copy, what moe_status would return for the record's
  * status word (MOE_ST_STATUS): MOE_OK, MOE_ERR_BAD_IDS, MOE_ERR_INVALID,
@@ -255,9 +261,13 @@ int moe_stats(const moe_problem* problem, const moe_layout_t* layout,
               const void* workspace, int64_t* host_stats, moe_stream_t stream);
 
 /* The record of "Balancing and Beyond", sections 1 and 2, as for moe_stats,
- * copied to DEVICE memory, asynchronously (one small kernel
- * on the stream; it can be captured in a CUDA graph).  The layout's own
- * layout->stats pointer gives the same record without this call.
+ * computed on the device, asynchronously (one block on the stream; it can be
+ * captured in a CUDA graph), from the counters the last moe_layout with this
+ * workspace left there.  It reads nothing that moe_dispatch or moe_combine
+ * write, so with layout->stats left NULL a caller can run it on a second
+ * stream beside them, off the dispatch's critical path (the layout kernel
+ * then ends when the positions are written); it must finish before the
+ * workspace's next moe_layout.
  *   workspace: the workspace of the moe_layout call; device_stats: device
  *   int64 [moe_stats_words()], 8-byte aligned. */
 int moe_stats_device(const moe_problem* problem, const void* workspace, int64_t* device_stats,

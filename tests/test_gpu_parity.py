@@ -326,3 +326,54 @@ def test_host_stats_reports_bad_ids(dev):
     case.run(dispatch=False, combine=False, stats=False)
     rc, rec = moe.moe_stats(case.prob, case.lay, case.ws)
     assert rc == moe.MOE_ERR_BAD_IDS and rec[moe.MOE_ST_STATUS] == moe.MOE_STATUS_ID_RANGE
+
+
+@pytest.mark.parametrize("name", ["prefill-fp8", "decode-EP32-r8"])
+def test_stats_beside_the_movers(dev, oracle_mod, name):
+    """Without layout.stats the layout kernel ends with its positions and
+    moe_stats_device makes the record on a second stream while dispatch and
+    combine run on the first: the record equals the oracle's, and the moved
+    rows are those of the plain order of calls (full workload size, also
+    replayed from a CUDA graph)."""
+    import torch
+    import combine_moe_layout_04_gb300 as moe
+    w = mw.WORKLOADS[name]
+    case = Case(w, dev, y_on_device=True)
+    main, side = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    prob, keep = oracle_problem(oracle_mod, w)
+    ref = oracle_mod.stats(prob, case.ids)
+
+    def step(s):
+        moe.moe_layout(case.prob, case.ids_d, case.ws, case.lay, s)
+        side.wait_stream(s)
+        moe.moe_stats_device(case.prob, case.ws, case.stats, side)
+        moe.moe_dispatch(case.prob, case.lay, case.x_d, case.xs_d, case.recv, case.recv_s, s)
+        moe.moe_combine(case.prob, case.lay, case.y_d, case.gates_d, case.out, s)
+        s.wait_stream(side)
+
+    def check():
+        got = case.stats_host()
+        assert got["status"] == 0
+        for field, val in ref.items():
+            assert np.array_equal(np.asarray(got[field]), np.asarray(val)), f"stats {field} differs"
+
+    case.poison()
+    case.stats.fill_(-1)
+    main.wait_stream(torch.cuda.current_stream())  # after the poison, which runs on the current stream
+    step(main)
+    torch.cuda.synchronize()
+    check()
+    out0, recv0 = case.out.clone(), case.recv.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(main):
+        g.capture_begin()
+        step(main)
+        g.capture_end()
+    case.poison()
+    case.stats.fill_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    check()
+    assert torch.equal(case.out.view(torch.int16), out0.view(torch.int16))
+    assert torch.equal(case.recv.view(torch.uint8), recv0.view(torch.uint8))
+    assert moe.moe_move_faults() == 0
