@@ -303,6 +303,34 @@ def workload_config(w):
 
 # ----------------------------------------------------------------- GPU arm
 
+def reference_rates(dev, nbytes, reps=5):
+    """HBM rates of two plain library kernels on the same GPU in the same run,
+    as references for the row movers: torch's fill (writes only) and copy (one
+    read and one write per byte) over `nbytes`, timed with CUDA events (median
+    of `reps` after two warm-ups)."""
+    import statistics as st
+    import torch
+    buf = torch.empty(2 * nbytes, dtype=torch.uint8, device=dev)
+    a, b = buf[:nbytes], buf[nbytes:]
+    out = {}
+    for name, fn, moved in (("fill_write_only", lambda: a.fill_(7), nbytes),
+                            ("copy_read_write", lambda: b.copy_(a), 2 * nbytes)):
+        times = []
+        for i in range(reps + 2):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                times.append(e0.elapsed_time(e1) * 1e3)
+        us = st.median(times)
+        out[name] = {"us": round(us, 2), "gbs": round(moved / (us * 1e-6) / 1e9, 1)}
+    del buf
+    out["bytes"] = nbytes
+    return out
+
+
 def relay_bytes(w, n_relay):
     """Mode 2 relay on one buffer: dispatch reads each token row, writes and
     reads back its relay rows, writes k receive rows; combine reads k expert
@@ -651,6 +679,8 @@ def run_ours(args, w):
         moe.moe_stats_device(prob, ws, stats, stream)
         ratios.append(moe.decode_stats(prob, stats.cpu().numpy())["imbalance_ratio"])
 
+    refs = reference_rates(dev, recv.numel() * recv.element_size())
+
     relay = relay_measure(args, w, moe, prob, lay, ws, ids_d, x_d, xs_d, recv, recv_s, y_d, gates_d, out,
                           stream, world, dev)
 
@@ -773,6 +803,10 @@ def run_ours(args, w):
         "roofline": {"bound": "hbm", "kernel": "combine_kernel", "achieved": round(comb_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(comb_gbs / peak, 4),
                      "traffic": traffic, "peak_source": peak_src},
+        "reference_kernels": dict(refs, note="torch's own fill and copy kernels over the receive buffer's "
+                                             "bytes, same GPU and run: the write-only and the 1:1 copy rate"),
+        "dispatch_gbs": round(d_bytes / (dispatch_us * 1e-6) / 1e9, 1),
+        "dispatch_frac_of_peak": round(d_bytes / (dispatch_us * 1e-6) / 1e9 / peak, 4),
         "e2e": {"value": round(world * (d_bytes + c_bytes) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
