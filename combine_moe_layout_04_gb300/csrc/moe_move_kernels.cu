@@ -327,6 +327,118 @@ combine_kernel(const Route rt, const MoveArgs m, int nl, const uint4* __restrict
     }
 }
 
+// Lane i < n takes the i-th partner (ascending lane order) of p / w; n partners.
+__device__ __forceinline__ void compact_partners(int lane, int p, float w, int& cp, float& cw, int& n) {
+    const unsigned m = __ballot_sync(kAll, p >= 0);
+    n = __popc(m);
+    unsigned mm = m;
+    for (int i = 0; i < lane && i < n; ++i) mm &= mm - 1;  // lane-th partner
+    const int from = lane < n ? __ffs(mm) - 1 : 0;
+    cp = __shfl_sync(kAll, p, from);
+    cw = __shfl_sync(kAll, w, from);
+    if (lane >= n) {
+        cp = -1;
+        cw = 0.0f;
+    }
+}
+
+// ---- vector chain combine ----------------------------------------------------
+//
+// One expert group's combine through registers: one warp per (token, span of
+// 32 x kChainU runs of 8 columns), on a grid of several times the resident
+// CTAs.  Lane L holds runs L, L + 32, ... of the span: their fp32 chain
+// values (32-byte loads and stores) and, for each partner, the matching 16
+// bytes of bf16 y.  The partners are compacted in ascending lane order and
+// summed kChainKB at a time, every load of a round issued before any is used,
+// so each chain value takes its fma steps in the route's partner order.  Any
+// number of partners (k <= 32).  Two runs a lane and three partners a round,
+// from a sweep on GB300 (G = 4 group combines at prefill-fp8, sum of the four):
+// U, KB = 2, 3: 699 us (63 registers, four CTAs an SM); 2, 2: 706; 1, 1 to
+// 1, 4: 736-775; 2, 4: 738; 4, 2: 775; 4, 4: 718; 8, 2: 851; the packed
+// shared-memory pipeline: 870.
+constexpr int kChainU = 2, kChainKB = 3;
+
+template <int ACC, class Route>
+__global__ void __launch_bounds__(kMoveThreads)
+combine_chain_vec_kernel(const Route rt, const int nvec, const int nspan, const uint4* __restrict__ y,
+                         uint4* __restrict__ out, float* __restrict__ acc_rows, bool acc_v8) {
+    const int lane = threadIdx.x & 31;
+    const long long units = rt.units() * nspan;
+    const long long nw = (long long)gridDim.x * kMoveWarps;
+    const uint64_t ypol = l2_evict_first_policy();  // y rows are read once
+    for (long long u = (long long)blockIdx.x * kMoveWarps + (threadIdx.x >> 5); u < units; u += nw) {
+        const long long ui = u / nspan;
+        const int c = (int)(u - ui * nspan);
+        int p, cp, n;
+        float w, cw;
+        rt.partner(ui, true, lane, p, w);
+        compact_partners(lane, p, w, cp, cw, n);
+        if (ACC == kAccMid && n == 0) continue;  // nothing to add: the chain stays
+        const int v0 = c * 32 * kChainU + lane;  // this lane's first 16-byte run of the row
+        const size_t row = (size_t)rt.self_row(ui);
+        float* arow = acc_rows + row * (size_t)nvec * 8;
+        float acc[kChainU][8];
+#pragma unroll
+        for (int i = 0; i < kChainU; ++i) {
+            const int vi = v0 + 32 * i;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[i][q] = 0.0f;
+            if ((ACC == kAccMid || ACC == kAccLast) && vi < nvec) {
+                if (acc_v8) {
+                    ld_stream_v8f(arow + 8 * vi, acc[i]);
+                } else {
+                    const uint4 a0 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * vi));
+                    const uint4 a1 = ld_stream_v4(reinterpret_cast<const uint4*>(arow + 8 * vi + 4));
+                    acc[i][0] = __uint_as_float(a0.x); acc[i][1] = __uint_as_float(a0.y);
+                    acc[i][2] = __uint_as_float(a0.z); acc[i][3] = __uint_as_float(a0.w);
+                    acc[i][4] = __uint_as_float(a1.x); acc[i][5] = __uint_as_float(a1.y);
+                    acc[i][6] = __uint_as_float(a1.z); acc[i][7] = __uint_as_float(a1.w);
+                }
+            }
+        }
+        for (int jb = 0; jb < n; jb += kChainKB) {
+            uint4 v[kChainKB][kChainU];
+            float wj[kChainKB];
+#pragma unroll
+            for (int j = 0; j < kChainKB; ++j) {
+                const int pj = __shfl_sync(kAll, cp, (jb + j) & 31);
+                wj[j] = __shfl_sync(kAll, cw, (jb + j) & 31);
+                const bool use = jb + j < n;
+                const uint4* src = y + (size_t)(use ? pj : 0) * nvec;
+#pragma unroll
+                for (int i = 0; i < kChainU; ++i) {
+                    v[j][i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (use && v0 + 32 * i < nvec) v[j][i] = ld_stream_v4_hint(src + v0 + 32 * i, ypol);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kChainKB; ++j) {
+                if (jb + j >= n) break;
+#pragma unroll
+                for (int i = 0; i < kChainU; ++i) fma_bf16x8(acc[i], wj[j], v[j][i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kChainU; ++i) {
+            const int vi = v0 + 32 * i;
+            if (vi >= nvec) continue;
+            if constexpr (ACC == kAccFirst || ACC == kAccMid) {
+                if (acc_v8) {
+                    st_v8f(arow + 8 * vi, acc[i]);
+                } else {
+                    uint4* a4 = reinterpret_cast<uint4*>(arow + 8 * vi);
+                    st_v4(a4, make_uint4(__float_as_uint(acc[i][0]), __float_as_uint(acc[i][1]),
+                                         __float_as_uint(acc[i][2]), __float_as_uint(acc[i][3])));
+                    st_v4(a4 + 1, make_uint4(__float_as_uint(acc[i][4]), __float_as_uint(acc[i][5]),
+                                             __float_as_uint(acc[i][6]), __float_as_uint(acc[i][7])));
+                }
+            } else {
+                st_v4(out + row * (size_t)nvec + vi, pack_bf16x8(acc[i]));
+            }
+        }
+    }
+}
+
 // ---- quantise-in-dispatch ----------------------------------------------------
 
 // bf16 rows in, e4m3 rows + fp32 scales out, one scale per 128 columns: the
@@ -601,19 +713,6 @@ template <int ACC> struct PackedShape {
     static constexpr int kStageBytes = kPackSlots * kPiece;
 };
 
-__device__ __forceinline__ void compact_partners(int lane, int p, float w, int& cp, float& cw, int& n) {
-    const unsigned m = __ballot_sync(kAll, p >= 0);
-    n = __popc(m);
-    unsigned mm = m;
-    for (int i = 0; i < lane && i < n; ++i) mm &= mm - 1;  // lane-th partner
-    const int from = lane < n ? __ffs(mm) - 1 : 0;
-    cp = __shfl_sync(kAll, p, from);
-    cw = __shfl_sync(kAll, w, from);
-    if (lane >= n) {
-        cp = -1;
-        cw = 0.0f;
-    }
-}
 
 template <int ACC, class Route>
 __global__ void __launch_bounds__(PackedShape<ACC>::kWarps * 32, PackedShape<ACC>::kCtasPerSm)
@@ -1195,6 +1294,24 @@ cudaError_t launch_combine_t(const Route& rt, long long max_units, int nvec, int
     return cudaGetLastError();
 }
 
+template <int ACC, class Route>
+cudaError_t launch_combine_chain_vec(const Route& rt, long long max_units, int nvec, const void* y, void* out,
+                                     const MoveShape& sh, cudaStream_t stream, float* acc) {
+    const int nspan = (nvec + 32 * kChainU - 1) / (32 * kChainU);
+    const long long units = max_units * nspan;
+    if (units == 0) return cudaSuccess;
+    auto kern = combine_chain_vec_kernel<ACC, Route>;
+    const int occ = blocks_per_sm(reinterpret_cast<const void*>(kern), kMoveThreads, 0);
+    // like the vector dispatch: several times the resident CTAs unless the
+    // tuning sets the combine's SMs or CTAs per SM
+    const bool persistent = sh.combine_sms > 0 || sh.combine_ctas > 0;
+    const int per_sm = persistent ? (sh.combine_ctas > 0 ? min(sh.combine_ctas, occ) : occ) : occ * kVecOversubscribe;
+    const bool acc_v8 = (reinterpret_cast<uintptr_t>(acc) & 31) == 0;
+    kern<<<capped_grid(units, kMoveWarps, mover_sms(sh.combine_sms), per_sm), kMoveThreads, 0, stream>>>(
+        rt, nvec, nspan, static_cast<const uint4*>(y), static_cast<uint4*>(out), acc, acc_v8);
+    return cudaGetLastError();
+}
+
 // Sums at most nl partner rows per unit.  The bulk pipeline's stage holds
 // kCombStageBytes: 8 partners x 512 B, or fewer partners with longer pieces
 // so that a warp keeps the same bytes in flight; more than 8 partners, or a
@@ -1272,18 +1389,18 @@ cudaError_t launch_combine_group(const MoveArgs& m, const GroupArgs& ga, const v
     const GroupSlotRoute rt{m.pos, w, ga.ids, ga.group, ga.g, m.T, m.k, ga.E, m.T * m.k};
     const MoveShape& sh = m.shape;
     if (ga.G == 1) return launch_combine_route(rt, m.T, m.nvec, m.k, y, out, sh, stream);
-    if (m.k <= kPackSlots && sh.combine_kind != MOE_MOVE_VECTOR) {
-        // a group holds about k / G of a token's slots: pack the stages
+    if (m.k <= kPackSlots && sh.combine_kind == MOE_MOVE_BULK) {
+        // the shared-memory pipeline, packed: a group holds about k / G of a token's slots
         if (ga.g == 0) return launch_combine_packed<kAccFirst>(rt, m.T, m.nvec, y, out, sh, stream, acc);
         if (ga.g == ga.G - 1) return launch_combine_packed<kAccLast>(rt, m.T, m.nvec, y, out, sh, stream, acc);
         return launch_combine_packed<kAccMid>(rt, m.T, m.nvec, y, out, sh, stream, acc);
     }
-    // more than 8 slots per token (or a vector combine asked for): the LSU kernel carries the chain
-    if (ga.g == 0)
-        return launch_combine_t<8, 1, GroupSlotRoute, kAccFirst>(rt, m.T, m.nvec, m.k, y, out, sh, stream, acc);
-    if (ga.g == ga.G - 1)
-        return launch_combine_t<8, 1, GroupSlotRoute, kAccLast>(rt, m.T, m.nvec, m.k, y, out, sh, stream, acc);
-    return launch_combine_t<8, 1, GroupSlotRoute, kAccMid>(rt, m.T, m.nvec, m.k, y, out, sh, stream, acc);
+    // By default the chain goes through registers: at G = 4 on the prefill-fp8
+    // workload the four group combines took 699 us against 870 us for the
+    // packed pipeline (decode-EP32-r8: 201 against 286 us).
+    if (ga.g == 0) return launch_combine_chain_vec<kAccFirst>(rt, m.T, m.nvec, y, out, sh, stream, acc);
+    if (ga.g == ga.G - 1) return launch_combine_chain_vec<kAccLast>(rt, m.T, m.nvec, y, out, sh, stream, acc);
+    return launch_combine_chain_vec<kAccMid>(rt, m.T, m.nvec, y, out, sh, stream, acc);
 }
 
 cudaError_t launch_relay_dispatch(const MoveArgs& m, const RelayArgs& r, const void* x, const float* xs, void* relay,

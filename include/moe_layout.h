@@ -105,9 +105,11 @@ typedef enum {
  *     warps per CTA (1 .. 16), shared-memory stages per warp (1 .. 8) and
  *     bytes of a source row per stage (a multiple of 16, 256 .. 32768); their
  *     product must fit in 220 KB of shared memory.
- *   combine_kind: MOE_MOVE_AUTO (default), MOE_MOVE_BULK (partner pieces
- *     gathered into shared memory by bulk copies; at most 8 partners, more
- *     fall back to vector) or MOE_MOVE_VECTOR (16-byte vector loads).
+ *   combine_kind: MOE_MOVE_AUTO (default: bulk for moe_combine and the relay,
+ *     vector for the expert-group chain of moe_combine_group), MOE_MOVE_BULK
+ *     (partner pieces gathered into shared memory by bulk copies; at most 8
+ *     partners, more fall back to vector) or MOE_MOVE_VECTOR (rows through
+ *     registers with vector loads).
  *   combine_ctas_per_sm: bulk combine CTAs per SM, 1 .. 3. */
 #define MOE_MOVE_AUTO   0
 #define MOE_MOVE_VECTOR 1
