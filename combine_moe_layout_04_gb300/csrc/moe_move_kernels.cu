@@ -4,24 +4,28 @@
 // B300 GPUs": dispatch_with_permute / combine_with_unpermute), so they are
 // written for bytes in flight, not for arithmetic.
 //
-//  * bulk pipelines (every dispatch; combine with at most 8 partners): the
-//    Blackwell bulk-copy engine (cp.async.bulk, "TMA") moves the rows.  Each
-//    warp runs its own pipeline of shared-memory stages guarded by mbarriers.
-//    Combine gathers the partner pieces of one unit into a stage and reduces
-//    it from shared memory (combine_bulk_kernel; combine_packed_kernel packs
-//    several column pieces per partner into a stage when a unit has few
-//    partners); dispatch loads one source chunk and writes it to its partner
-//    rows with bulk stores.  Bytes in flight are bounded by shared memory
-//    (about 190 KB per SM), not by registers.  Every barrier wait has a
-//    wall-time limit; a kernel that gives up records a fault bit, drains its
-//    own copies and returns.
-//  * LSU combine (more than 8 partners): one warp per (unit, column chunk)
-//    with 16-byte vector loads, every load of a round issued before any is
-//    used.  Quantise-in-dispatch also uses plain vector loads and stores.
+//  * register movers (the default dispatch, quantise-in-dispatch, the
+//    expert-group combine, and every combine with more than 8 partners): one
+//    warp per (unit, column span), every load of the span issued before any
+//    is used, 256-bit loads and stores where rows and bases allow; the grid
+//    holds several times the CTAs that fit at once, so CTAs turn over instead
+//    of looping.  On GB300 this kept the DRAM write stream fuller than the
+//    shared-memory pipelines for the dispatch (read 1, write k) and for the
+//    group combine's fp32 chain.
+//  * bulk pipelines (the flat and relay combines with at most 8 partners; the
+//    dispatch and the group combine on request): the Blackwell bulk-copy
+//    engine (cp.async.bulk, "TMA") moves the rows.  Each warp runs its own
+//    pipeline of shared-memory stages guarded by mbarriers.  Combine gathers
+//    the partner pieces of one unit into a stage and reduces it from shared
+//    memory (combine_bulk_kernel; combine_packed_kernel packs several column
+//    pieces per partner into a stage when a unit has few partners); dispatch
+//    loads one source chunk and writes it to its partner rows with bulk
+//    stores.  Every barrier wait has a wall-time limit; a kernel that gives
+//    up records a fault bit, drains its own copies and returns.
 //
-// All walk a persistent grid over units x chunks.  Which rows a unit touches is a route (below): the flat path
-// pairs a token with its k receive rows; the two hops of the Mode 2 relay pair
-// a token with its relay rows, and a relay row with the receive rows it feeds.
+// Which rows a unit touches is a route (below): the flat path pairs a token
+// with its k receive rows; the two hops of the Mode 2 relay pair a token with
+// its relay rows, and a relay row with the receive rows it feeds.
 // A partner row outside its buffer is skipped (dispatch) or contributes
 // nothing (combine), so a bad layout cannot write out of bounds.
 
@@ -256,77 +260,6 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
     return make_uint4(q[0], q[1], q[2], q[3]);
 }
 
-// KB partners are gathered per round (all KB x U loads issued first), then
-// accumulated in ascending lane order; more than KB partners take several
-// rounds.  Lanes >= nl carry no partner.
-template <int KB, int U, class Route, int ACC>
-__global__ void __launch_bounds__(kMoveThreads)
-combine_kernel(const Route rt, const MoveArgs m, int nl, const uint4* __restrict__ y,
-               uint4* __restrict__ out, float* __restrict__ acc_rows) {
-    const int lane = threadIdx.x & 31;
-    const int gwarp = blockIdx.x * kMoveWarps + (threadIdx.x >> 5);
-    const int nwarps = gridDim.x * kMoveWarps;
-    const long long units = rt.units() * m.nchunks;
-    const uint64_t ypol = l2_evict_first_policy();  // y rows are read once
-    for (long long u = gwarp; u < units; u += nwarps) {
-        const long long ui = u / m.nchunks;
-        const int c = (int)(u - ui * m.nchunks);
-        int p;
-        float wt;
-        rt.partner(ui, true, lane, p, wt);
-        if (ACC == kAccMid && __ballot_sync(kAll, p >= 0) == 0u) continue;  // acc stays
-        const int v0 = c * m.chunk_vecs + lane;
-        const int vend = min(m.nvec, (c + 1) * m.chunk_vecs);
-        float* arow = ACC == kAccNone ? nullptr : acc_rows + (size_t)rt.self_row(ui) * m.nvec * 8;
-        float acc[U][8];
-#pragma unroll
-        for (int i = 0; i < U; ++i)
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[i][q] = 0.0f;
-        if constexpr (ACC == kAccMid || ACC == kAccLast) {
-#pragma unroll
-            for (int i = 0; i < U; ++i)
-                if (v0 + 32 * i < vend)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[i][q] = arow[8 * (v0 + 32 * i) + q];
-        }
-        for (int jb = 0; jb < nl; jb += KB) {
-            uint4 v[KB][U];
-            float wj[KB];
-#pragma unroll
-            for (int j = 0; j < KB; ++j) {
-                const int pj = __shfl_sync(kAll, p, (jb + j) & 31);
-                wj[j] = __shfl_sync(kAll, wt, (jb + j) & 31);
-                const bool use = (jb + j < nl) && pj >= 0;
-                const uint4* src = y + (size_t)(use ? pj : 0) * m.nvec;
-#pragma unroll
-                for (int i = 0; i < U; ++i) {
-                    v[j][i] = make_uint4(0u, 0u, 0u, 0u);
-                    if (use && v0 + 32 * i < vend) v[j][i] = ld_stream_v4_hint(src + v0 + 32 * i, ypol);
-                }
-                if (!use) wj[j] = 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < KB; ++j) {
-                if (jb + j >= nl) break;
-#pragma unroll
-                for (int i = 0; i < U; ++i) fma_bf16x8(acc[i], wj[j], v[j][i]);
-            }
-        }
-        uint4* orow = out + (size_t)rt.self_row(ui) * m.nvec;
-#pragma unroll
-        for (int i = 0; i < U; ++i) {
-            if (v0 + 32 * i >= vend) continue;
-            if constexpr (ACC == kAccFirst || ACC == kAccMid) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) arow[8 * (v0 + 32 * i) + q] = acc[i][q];
-            } else {
-                st_v4(orow + v0 + 32 * i, pack_bf16x8(acc[i]));
-            }
-        }
-    }
-}
-
 // Lane i < n takes the i-th partner (ascending lane order) of p / w; n partners.
 __device__ __forceinline__ void compact_partners(int lane, int p, float w, int& cp, float& cw, int& n) {
     const unsigned m = __ballot_sync(kAll, p >= 0);
@@ -357,8 +290,14 @@ __device__ __forceinline__ void compact_partners(int lane, int p, float w, int& 
 // 1, 4: 736-775; 2, 4: 738; 4, 2: 775; 4, 4: 718; 8, 2: 851; the packed
 // shared-memory pipeline: 870.
 constexpr int kChainU = 2, kChainKB = 3;
+// The same kernel without a chain is the vector combine of the flat and relay
+// routes (more than 8 partners, or MOE_MOVE_VECTOR).  Four runs a lane and four
+// partners a round took the flat combine 316.5 us at prefill-fp8 (the bulk
+// pipeline 313.5) and 82.1 us at decode (84.9); cold, with L2 flushed before
+// the call, the two match at decode, so the bulk pipeline stays the default.
+constexpr int kFlatVecU = 4, kFlatVecKB = 4;
 
-template <int ACC, class Route>
+template <int ACC, int U, int KB, class Route>
 __global__ void __launch_bounds__(kMoveThreads)
 combine_chain_vec_kernel(const Route rt, const int nvec, const int nspan, const uint4* __restrict__ y,
                          uint4* __restrict__ out, float* __restrict__ acc_rows, bool acc_v8) {
@@ -374,12 +313,12 @@ combine_chain_vec_kernel(const Route rt, const int nvec, const int nspan, const 
         rt.partner(ui, true, lane, p, w);
         compact_partners(lane, p, w, cp, cw, n);
         if (ACC == kAccMid && n == 0) continue;  // nothing to add: the chain stays
-        const int v0 = c * 32 * kChainU + lane;  // this lane's first 16-byte run of the row
+        const int v0 = c * 32 * U + lane;  // this lane's first 16-byte run of the row
         const size_t row = (size_t)rt.self_row(ui);
         float* arow = acc_rows + row * (size_t)nvec * 8;
-        float acc[kChainU][8];
+        float acc[U][8];
 #pragma unroll
-        for (int i = 0; i < kChainU; ++i) {
+        for (int i = 0; i < U; ++i) {
             const int vi = v0 + 32 * i;
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[i][q] = 0.0f;
@@ -396,30 +335,30 @@ combine_chain_vec_kernel(const Route rt, const int nvec, const int nspan, const 
                 }
             }
         }
-        for (int jb = 0; jb < n; jb += kChainKB) {
-            uint4 v[kChainKB][kChainU];
-            float wj[kChainKB];
+        for (int jb = 0; jb < n; jb += KB) {
+            uint4 v[KB][U];
+            float wj[KB];
 #pragma unroll
-            for (int j = 0; j < kChainKB; ++j) {
+            for (int j = 0; j < KB; ++j) {
                 const int pj = __shfl_sync(kAll, cp, (jb + j) & 31);
                 wj[j] = __shfl_sync(kAll, cw, (jb + j) & 31);
                 const bool use = jb + j < n;
                 const uint4* src = y + (size_t)(use ? pj : 0) * nvec;
 #pragma unroll
-                for (int i = 0; i < kChainU; ++i) {
+                for (int i = 0; i < U; ++i) {
                     v[j][i] = make_uint4(0u, 0u, 0u, 0u);
                     if (use && v0 + 32 * i < nvec) v[j][i] = ld_stream_v4_hint(src + v0 + 32 * i, ypol);
                 }
             }
 #pragma unroll
-            for (int j = 0; j < kChainKB; ++j) {
+            for (int j = 0; j < KB; ++j) {
                 if (jb + j >= n) break;
 #pragma unroll
-                for (int i = 0; i < kChainU; ++i) fma_bf16x8(acc[i], wj[j], v[j][i]);
+                for (int i = 0; i < U; ++i) fma_bf16x8(acc[i], wj[j], v[j][i]);
             }
         }
 #pragma unroll
-        for (int i = 0; i < kChainU; ++i) {
+        for (int i = 0; i < U; ++i) {
             const int vi = v0 + 32 * i;
             if (vi >= nvec) continue;
             if constexpr (ACC == kAccFirst || ACC == kAccMid) {
@@ -1278,29 +1217,13 @@ cudaError_t launch_dispatch_route(const Route& rt, long long max_units, int row_
     return cudaGetLastError();
 }
 
-template <int KB, int U, class Route, int ACC = kAccNone>
-cudaError_t launch_combine_t(const Route& rt, long long max_units, int nvec, int nl, const void* y, void* out,
-                             const MoveShape& sh, cudaStream_t stream, float* acc = nullptr) {
-    MoveArgs m{};
-    m.nvec = nvec;
-    m.chunk_vecs = 32 * U;
-    m.nchunks = (m.nvec + m.chunk_vecs - 1) / m.chunk_vecs;
-    const long long units = max_units * m.nchunks;
-    if (units == 0) return cudaSuccess;
-    auto kern = combine_kernel<KB, U, Route, ACC>;
-    const int occ = blocks_per_sm(reinterpret_cast<const void*>(kern), kMoveThreads, 0);
-    kern<<<capped_grid(units, kMoveWarps, mover_sms(sh.combine_sms), occ), kMoveThreads, 0, stream>>>(
-        rt, m, nl, static_cast<const uint4*>(y), static_cast<uint4*>(out), acc);
-    return cudaGetLastError();
-}
-
-template <int ACC, class Route>
+template <int ACC, class Route, int U = kChainU, int KB = kChainKB>
 cudaError_t launch_combine_chain_vec(const Route& rt, long long max_units, int nvec, const void* y, void* out,
                                      const MoveShape& sh, cudaStream_t stream, float* acc) {
-    const int nspan = (nvec + 32 * kChainU - 1) / (32 * kChainU);
+    const int nspan = (nvec + 32 * U - 1) / (32 * U);
     const long long units = max_units * nspan;
     if (units == 0) return cudaSuccess;
-    auto kern = combine_chain_vec_kernel<ACC, Route>;
+    auto kern = combine_chain_vec_kernel<ACC, U, KB, Route>;
     const int occ = blocks_per_sm(reinterpret_cast<const void*>(kern), kMoveThreads, 0);
     // like the vector dispatch: several times the resident CTAs unless the
     // tuning sets the combine's SMs or CTAs per SM
@@ -1315,7 +1238,7 @@ cudaError_t launch_combine_chain_vec(const Route& rt, long long max_units, int n
 // Sums at most nl partner rows per unit.  The bulk pipeline's stage holds
 // kCombStageBytes: 8 partners x 512 B, or fewer partners with longer pieces
 // so that a warp keeps the same bytes in flight; more than 8 partners, or a
-// vector combine asked for by the tuning, go to the LSU kernel.
+// vector combine asked for by the tuning, go to the register kernel.
 constexpr int kCombStageBytes = 8 * kCombChunk;
 
 template <class Route>
@@ -1327,7 +1250,8 @@ cudaError_t launch_combine_route(const Route& rt, long long max_units, int nvec,
         if (nl <= 4) return launch_combine_bulk<W, S, B / 4, 4, false, C, Route>(rt, max_units, nvec, y, out, sh, stream);
         if (nl <= 8) return launch_combine_bulk<W, S, B / 8, 8, false, C, Route>(rt, max_units, nvec, y, out, sh, stream);
     }
-    return launch_combine_t<8, 1, Route>(rt, max_units, nvec, nl, y, out, sh, stream);
+    return launch_combine_chain_vec<kAccNone, Route, kFlatVecU, kFlatVecKB>(rt, max_units, nvec, y, out, sh, stream,
+                                                                          nullptr);
 }
 
 template <int ACC, class Route>
