@@ -146,13 +146,19 @@ def test_group_custom_placement(dev, oracle_mod):
     _group_parity(oracle_mod, Case(w, dev, expert_to_rank=e2r, y_on_device=False), 3, e2r=e2r)
 
 
+@pytest.mark.parametrize("kind", ["auto", "bulk"])
 @pytest.mark.parametrize("acc_offset", [4, 8])
-def test_group_chain_alignment(dev, oracle_mod, acc_offset):
+def test_group_chain_alignment(dev, oracle_mod, acc_offset, kind):
     """The fp32 chain moves as 32-byte accesses when its rows are 32-byte
     aligned and as 16-byte halves otherwise: a chain 16 bytes (and 32 bytes)
-    into its allocation gives the same accumulators and output."""
+    into its allocation gives the same accumulators and output, in the
+    register combine (the default) and in the packed shared-memory one."""
+    import combine_moe_layout_04_gb300 as moe
     w = mw.scaled(mw.WORKLOADS["decode-EP32-r8"], T=640, R_src=8)
-    _group_parity(oracle_mod, Case(w, dev, y_on_device=False), 4, acc_offset=acc_offset)
+    case = Case(w, dev, y_on_device=False)
+    if kind == "bulk":
+        case.prob.tuning = moe.Tuning(combine_kind=moe.MOE_MOVE_BULK)
+    _group_parity(oracle_mod, case, 4, acc_offset=acc_offset)
 
 
 def test_group_overlap_on_two_streams(dev, oracle_mod):
