@@ -1005,9 +1005,10 @@ dispatch_bulk_kernel(const Route rt, const int nch, const int stages, const int 
 // 166-168 us against 182-184 us for the shared-memory bulk pipeline, and
 // 4096 bf16 rows in 86-88 us against 94 us: with the same bytes in flight per
 // SM, the register path keeps the DRAM write stream fuller.  fp8 scale rows travel
-// with the first span: lane L keeps words L + 32 q (rows of up to
-// 32 x kVecScaleWords groups; longer ones are copied word by word).  A unit
-// without partners loads nothing.
+// with the first span: as 32-byte pieces, one a lane, when the row is whole
+// pieces and both scale arrays are 32-byte aligned; otherwise lane L keeps
+// words L + 32 q (rows of up to 32 x kVecScaleWords groups; longer ones are
+// copied word by word).  A unit without partners loads nothing.
 constexpr int kVecThreads = 256;
 constexpr int kVecMinBlocks = 2;   // ~100 registers a thread: two 8-warp CTAs fill an SM's registers
 constexpr int kVecScaleWords = 4;
@@ -1049,7 +1050,7 @@ template <int VB> struct VecSpan { static constexpr int V = 7168 / (32 * VB); };
 template <int VB, class Route>
 __global__ void __launch_bounds__(kVecThreads, kVecMinBlocks)
 dispatch_vec_kernel(const Route rt, const int nspan, const uint8_t* __restrict__ x, const float* __restrict__ xs,
-                    uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups) {
+                    uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups, bool scale_v8) {
     constexpr int V = VecSpan<VB>::V;
     constexpr int SPAN = 32 * V * VB;
     constexpr int WPB = kVecThreads / 32;
@@ -1079,11 +1080,16 @@ dispatch_vec_kernel(const Route rt, const int nspan, const uint8_t* __restrict__
             if (off < lim) v[i].load(src + off);
         }
         const bool scales = groups > 0 && c == 0;
+        // a scale row of 32-byte pieces (groups % 8 == 0, both arrays 32-byte
+        // aligned, at most 32 pieces) moves as one 256-bit vector a lane
         const bool keep = groups <= 32 * kVecScaleWords;
+        const int svec = scale_v8 ? groups / 8 : 0;
         float sv[kVecScaleWords];
+        VecT<32> s8;
+        if (scales && scale_v8 && lane < svec) s8.load(reinterpret_cast<const uint8_t*>(xs + srow * groups) + 32 * lane);
 #pragma unroll
         for (int q = 0; q < kVecScaleWords; ++q)
-            sv[q] = (scales && keep && lane + 32 * q < groups) ? xs[srow * groups + lane + 32 * q] : 0.0f;
+            sv[q] = (scales && !scale_v8 && keep && lane + 32 * q < groups) ? xs[srow * groups + lane + 32 * q] : 0.0f;
         for (unsigned m = pm; m; m &= m - 1) {
             const int pj = __shfl_sync(kAll, p, __ffs(m) - 1);
             uint8_t* dst = recv + (size_t)pj * row_bytes + (size_t)c * SPAN;
@@ -1094,7 +1100,9 @@ dispatch_vec_kernel(const Route rt, const int nspan, const uint8_t* __restrict__
             }
             if (scales) {
                 float* srow_out = rs + (size_t)pj * groups;
-                if (keep) {
+                if (scale_v8) {
+                    if (lane < svec) s8.store(reinterpret_cast<uint8_t*>(srow_out) + 32 * lane);
+                } else if (keep) {
 #pragma unroll
                     for (int q = 0; q < kVecScaleWords; ++q)
                         if (lane + 32 * q < groups) srow_out[lane + 32 * q] = sv[q];
@@ -1183,12 +1191,15 @@ cudaError_t launch_dispatch_route(const Route& rt, long long max_units, int row_
         // fit at once (about one unit per warp at the workloads here); a tuning
         // that sets SMs or CTAs per SM gets a persistent grid of that size.
         const bool persistent = sh.dispatch_sms > 0 || sh.dispatch_ctas > 0;
+        const bool scale_v8 = groups > 0 && groups % 8 == 0 && groups / 8 <= 32 &&
+                              (reinterpret_cast<uintptr_t>(xs) & 31) == 0 && (reinterpret_cast<uintptr_t>(ds) & 31) == 0;
         auto launch = [&](auto kern) {
             const int occ = blocks_per_sm(reinterpret_cast<const void*>(kern), kVecThreads, 0);
             const int per_sm = persistent ? (sh.dispatch_ctas > 0 ? min(sh.dispatch_ctas, occ) : occ)
                                           : occ * kVecOversubscribe;
             kern<<<capped_grid(units, kVecThreads / 32, sms, per_sm), kVecThreads, 0, stream>>>(
-                rt, nspan, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(dst), ds, row_bytes, groups);
+                rt, nspan, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(dst), ds, row_bytes, groups,
+                scale_v8);
         };
         if (v32)
             launch(dispatch_vec_kernel<32, Route>);
