@@ -38,6 +38,7 @@ MOE_STATS_HEADER_WORDS = 32
 MOE_ST_STATUS = 0  # header word holding the device status bits
 MOE_FAULT_WAIT_TIMEOUT = 1
 MOE_MOVE_AUTO, MOE_MOVE_VECTOR, MOE_MOVE_BULK = 0, 1, 2
+MOE_LAYOUT_AUTO, MOE_LAYOUT_SPLIT, MOE_LAYOUT_FUSED, MOE_LAYOUT_TWO_KERNELS = 0, 1, 2, 3
 
 # Header word names in index order (include/moe_layout.h, MOE_ST_*).
 STATS_HEADER = ("status", "T", "slots", "row_bytes", "max_expert_count", "argmax_expert",
@@ -68,11 +69,11 @@ class MoeError(RuntimeError):
 
 
 _TUNING_FIELDS = ("dispatch_kind", "dispatch_sms", "dispatch_ctas_per_sm", "dispatch_warps", "dispatch_stages",
-                  "dispatch_chunk_bytes", "combine_kind", "combine_sms", "combine_ctas_per_sm")
+                  "dispatch_chunk_bytes", "combine_kind", "combine_sms", "combine_ctas_per_sm", "layout_kind")
 
 
 class _TuningC(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in _TUNING_FIELDS] + [("reserved", ctypes.c_int32 * 7)]
+    _fields_ = [(n, ctypes.c_int32) for n in _TUNING_FIELDS] + [("reserved", ctypes.c_int32 * 6)]
 
 
 class _ProblemC(ctypes.Structure):
@@ -85,8 +86,9 @@ class _ProblemC(ctypes.Structure):
 
 @dataclass
 class Tuning:
-    """Launch shapes of the row movers (moe_tuning in include/moe_layout.h);
-    0 keeps the library's default.  Shapes change speed only, never results."""
+    """Launch shapes of the layout and the row movers (moe_tuning in
+    include/moe_layout.h); 0 keeps the library's default.  Shapes change
+    speed only, never results."""
     dispatch_kind: int = MOE_MOVE_AUTO
     dispatch_sms: int = 0
     dispatch_ctas_per_sm: int = 0
@@ -96,6 +98,7 @@ class Tuning:
     combine_kind: int = MOE_MOVE_AUTO
     combine_sms: int = 0
     combine_ctas_per_sm: int = 0
+    layout_kind: int = MOE_LAYOUT_AUTO
 
     def c(self) -> _TuningC:
         return _TuningC(*[int(getattr(self, n)) for n in _TUNING_FIELDS])
@@ -106,13 +109,17 @@ class Tuning:
     @classmethod
     def from_env(cls, environ=None) -> "Tuning":
         """MOE_DISPATCH_KIND, MOE_DISPATCH_SMS, ... (upper-case field names
-        with a MOE_ prefix; kinds also as "auto", "vector" or "bulk")."""
+        with a MOE_ prefix; mover kinds also as "auto", "vector" or "bulk",
+        the layout kind as "auto", "split", "fused" or "two_kernels")."""
         env = os.environ if environ is None else environ
-        kinds = {"auto": MOE_MOVE_AUTO, "vector": MOE_MOVE_VECTOR, "bulk": MOE_MOVE_BULK}
+        move = {"auto": MOE_MOVE_AUTO, "vector": MOE_MOVE_VECTOR, "bulk": MOE_MOVE_BULK}
+        layout = {"auto": MOE_LAYOUT_AUTO, "split": MOE_LAYOUT_SPLIT, "fused": MOE_LAYOUT_FUSED,
+                  "two_kernels": MOE_LAYOUT_TWO_KERNELS}
         vals = {}
         for n in _TUNING_FIELDS:
             v = env.get("MOE_" + n.upper())
             if v is not None and v != "":
+                kinds = layout if n == "layout_kind" else move
                 vals[n] = kinds[v.lower()] if v.lower() in kinds else int(v)
         return cls(**vals)
 

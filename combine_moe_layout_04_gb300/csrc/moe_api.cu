@@ -32,6 +32,7 @@ int check_tuning(const moe_tuning* t, moe::MoveShape* sh) {
         return MOE_ERR_INVALID;
     if (!in(t->dispatch_chunk_bytes, 256, 32768) || t->dispatch_chunk_bytes % 16 != 0) return MOE_ERR_INVALID;
     if (!in(t->combine_ctas_per_sm, 1, 3)) return MOE_ERR_INVALID;
+    if (!in(t->layout_kind, MOE_LAYOUT_SPLIT, MOE_LAYOUT_TWO_KERNELS)) return MOE_ERR_INVALID;
     for (int r : t->reserved)
         if (r != 0) return MOE_ERR_INVALID;
     // the bulk dispatch's stages must fit in shared memory (the larger of the
@@ -49,6 +50,7 @@ int check_tuning(const moe_tuning* t, moe::MoveShape* sh) {
     sh->combine_kind = t->combine_kind;
     sh->combine_sms = t->combine_sms;
     sh->combine_ctas = t->combine_ctas_per_sm;
+    sh->layout_kind = t->layout_kind;
     return MOE_OK;
 }
 
@@ -120,6 +122,7 @@ moe::LayoutArgs layout_args(const moe_problem* problem, const Dims& d, const voi
     a.row_bytes = row_bytes(d);
     a.ws = static_cast<uint8_t*>(const_cast<void*>(workspace));
     a.wl = ws_layout(d);
+    a.kind = d.shape.layout_kind;
     return a;
 }
 

@@ -42,7 +42,7 @@ constexpr int kLayoutGroup = 16;
 // every layout; the per-block table follows.
 struct WsLayout {
     size_t status;                                  // u32 device status bits
-    size_t barrier;                                 // u32 grid-barrier arrivals
+    size_t barrier;                                 // u32 [2] grid-barrier arrivals
     size_t hcount;                                  // int32 [H]
     size_t src_tokens, src_mode0, src_mode1, src_mode2;            // int32 [R_src]
     size_t dst_tokens, dst_self, dst_local, dst_remote, dst_relay;  // int32 [R]
@@ -76,7 +76,7 @@ inline WsLayout make_ws_layout(int T, int E, int R, int H, int Rs) {
     w.blocks = T > 0 ? (T + kLayoutTokensPerBlock - 1) / kLayoutTokensPerBlock : 1;
     w.groups = (w.blocks + kLayoutGroup - 1) / kLayoutGroup;
     w.status = take(4);
-    w.barrier = take(4);
+    w.barrier = take(8);  // two u32 arrival counters
     w.hcount = take(4 * (size_t)H);
     // The four per-source and the five per-destination arrays are contiguous.
     w.src_tokens = take(4 * 4 * (size_t)Rs);
@@ -110,12 +110,14 @@ struct LayoutArgs {
     uint8_t* ws;
     WsLayout wl;
     moe_layout_t out;
+    int kind;             // MOE_LAYOUT_* (MOE_LAYOUT_AUTO: the fastest form that fits)
 };
 
-// Launch shapes of the row movers from a moe_tuning (0 = the default).
+// Launch shapes from a moe_tuning (0 = the default).
 struct MoveShape {
     int dispatch_kind, dispatch_sms, dispatch_ctas, dispatch_warps, dispatch_stages, dispatch_chunk;
     int combine_kind, combine_sms, combine_ctas;
+    int layout_kind;
 };
 
 struct MoveArgs {
@@ -271,28 +273,37 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
-// Arrival at a grid-wide barrier whose counter starts at zero; every block of
-// a cooperative launch calls it once.  Gives up after limit_ns (returns false)
-// instead of spinning forever.
-__device__ __forceinline__ bool grid_barrier(uint32_t* counter, uint64_t limit_ns) {
-    __shared__ int s_ok;
-    __threadfence();  // every thread's published results before the arrival
+// Arrival at a grid-wide barrier whose counter starts at zero: every thread's
+// earlier global writes are made visible, then the block adds one.  All
+// threads of the block call it.
+__device__ __forceinline__ void grid_arrive(uint32_t* counter) {
+    __threadfence();
     __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(counter, 1u);
+}
+
+// Waits until target blocks have arrived at the counter.  Gives up after
+// limit_ns (returns false) instead of spinning forever.  All threads of the
+// block call it; afterwards they see what the arrived blocks wrote.
+__device__ __forceinline__ bool grid_wait(const uint32_t* counter, uint32_t target, uint64_t limit_ns) {
+    bool ok = true;
     if (threadIdx.x == 0) {
-        atomicAdd(counter, 1u);
-        bool ok = true;
         const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(counter) < gridDim.x) {
+        while (ld_acquire_gpu(counter) < target) {
             __nanosleep(32);
             if (globaltimer_ns() - t0 > limit_ns) {
                 ok = false;
                 break;
             }
         }
-        s_ok = ok;
     }
-    __syncthreads();
-    return s_ok != 0;
+    return __syncthreads_and(ok) != 0;
+}
+
+// Both halves at once, every block of a cooperative launch arriving once.
+__device__ __forceinline__ bool grid_barrier(uint32_t* counter, uint64_t limit_ns) {
+    grid_arrive(counter);
+    return grid_wait(counter, gridDim.x, limit_ns);
 }
 
 // Global -> shared bulk copy completing on a barrier (bytes: multiple of 16,

@@ -25,14 +25,22 @@
 //         layout->stats the record comes later from stats_compute_kernel,
 //         which needs only the counters left in the workspace.
 //
-// Where the whole grid fits on the GPU at once, both phases run in one
-// cooperative kernel: each block counts, ranks its own slots (ids only),
-// publishes its counts and meets the others at one grid barrier before the
-// rest of the rank phase.  The barrier's counter is cleared with the other
-// accumulators before the launch, and its wait gives up after one second
-// (status bit MOE_STATUS_TIMEOUT) instead of spinning forever.  Otherwise the
-// phases run as two kernels, the second launched under programmatic dependent
-// launch so that its id-only ranking overlaps the first.
+// Three forms, the first whose grid fits on the GPU at once (or the one the
+// caller's tuning names):
+//  split  one cooperative kernel of 2B + 1 blocks.  Positions depend only on
+//         the expert histograms, so B blocks rank their slots, publish the
+//         histogram and meet at one grid barrier, while B other blocks count
+//         the same tokens for the statistics and only arrive at a second
+//         barrier, which the extra block alone waits for.  The positions no
+//         longer wait for the per-token counting.
+//  fused  one cooperative kernel of B + 1 blocks: each block ranks its slots,
+//         counts its tokens and publishes both, then meets the others at one
+//         grid barrier before the rest of the rank phase.
+//  two kernels, the second launched under programmatic dependent launch so
+//         that its id-only ranking overlaps the first.
+// The barriers' counters are cleared with the other accumulators before the
+// launch, and their waits give up after one second (status bit
+// MOE_STATUS_TIMEOUT) instead of spinning forever.
 
 #include <cuda_runtime.h>
 
@@ -42,6 +50,7 @@ namespace moe {
 namespace {
 
 constexpr int kHostSlots = 64;  // shared-memory slots for per-host counters
+constexpr uint64_t kLayoutWaitNs = 1000000000ull;  // grid-barrier waits give up after one second
 constexpr unsigned kFull = 0xffffffffu;
 
 // Exclusive scan of data[0, n) in shared memory by the whole block; returns
@@ -314,12 +323,26 @@ __device__ inline CountSmem carve_count(const LayoutArgs& a, int32_t* base) {
     return m;
 }
 
+// Publishes block b's expert histogram: its row of the [B][E] table, and
+// added to the totals of its group of kLayoutGroup blocks.
+__device__ __forceinline__ void publish_hist(const LayoutArgs& a, const int32_t* hist, int b) {
+    int32_t* g_agg = reinterpret_cast<int32_t*>(a.ws + a.wl.agg) + (size_t)b * a.E;
+    int32_t* g_group = reinterpret_cast<int32_t*>(a.ws + a.wl.group) + (size_t)(b / kLayoutGroup) * a.E;
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        const int v = hist[e];
+        g_agg[e] = v;
+        if (v) atomicAdd(&g_group[e], v);
+    }
+}
+
 // Counts the block's 128 tokens (threads 0..127 hold one token each; any
-// further threads take part in the collectives with no token) and publishes
-// the block's expert histogram and counters.  All threads of the block call
-// it.  With HIST the expert histogram is counted here; without, sm.hist
-// already holds it (the rank prologue counted the same slots).
-template <int KMAX, bool HIST>
+// further threads take part in the collectives with no token) and adds its
+// counters to the totals.  All threads of the block call it.  With HIST the
+// expert histogram is counted here; without, sm.hist already holds it (the
+// rank prologue counted the same slots).  With PUB the histogram is also
+// published (publish_hist); without, another block of the same 128 tokens
+// publishes it.
+template <int KMAX, bool HIST, bool PUB>
 __device__ void count_phase(const LayoutArgs& a, const CountSmem& sm, int b) {
     __shared__ uint32_t s_status;
     __shared__ int s_rs0;
@@ -474,13 +497,7 @@ __device__ void count_phase(const LayoutArgs& a, const CountSmem& sm, int b) {
     }
 
     // Publish this block's histogram; add the counters to the totals.
-    int32_t* g_agg = reinterpret_cast<int32_t*>(a.ws + a.wl.agg) + (size_t)b * a.E;
-    int32_t* g_group = reinterpret_cast<int32_t*>(a.ws + a.wl.group) + (size_t)(b / kLayoutGroup) * a.E;
-    for (int e = tid; e < a.E; e += blockDim.x) {
-        const int v = sm.hist[e];
-        g_agg[e] = v;
-        if (v) atomicAdd(&g_group[e], v);
-    }
+    if (PUB) publish_hist(a, sm.hist, b);
     int32_t* g_hcount = reinterpret_cast<int32_t*>(a.ws + a.wl.hcount);
     for (int hh = tid; hh < a.H; hh += blockDim.x)
         if (sm.hc[hh]) atomicAdd(&g_hcount[hh], sm.hc[hh]);
@@ -586,14 +603,16 @@ __device__ void rank_prologue(const LayoutArgs& a, const RankSmem& sm, int b) {
     __syncthreads();
 }
 
-// The rest of the rank phase, once every block's counts are published:
-// totals, offsets, this block's prefix, outputs, statistics (block 0) and
-// the positions of the block's slots.
-__device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b) {
+// The rest of the rank phase, once every block's expert histogram is
+// published: totals, offsets, this block's prefix, outputs, statistics (the
+// extra block, b == B) and the positions of the block's slots.  counted:
+// NULL when the per-token counters are complete too; otherwise the arrival
+// counter of the blocks that add them, which the extra block waits for.
+__device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b, const uint32_t* counted) {
     __shared__ int32_t s_warp[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     StatIn stat_in = {};
-    if (b == a.wl.blocks) load_stat_inputs(a, stat_in);  // complete: every block's counts are published
+    if (b == a.wl.blocks && counted == nullptr) load_stat_inputs(a, stat_in);  // complete already
     const int S = a.T * a.k;
     const SlotRange sr = slot_range(a, b);
     const int32_t* g_group = reinterpret_cast<const int32_t*>(a.ws + a.wl.group);
@@ -687,6 +706,13 @@ __device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b) {
     if (b == a.wl.blocks) {
         // The extra block: counts, offsets and statistics (the slot blocks
         // write positions meanwhile).
+        if (counted != nullptr) {
+            if (!grid_wait(counted, a.wl.blocks, kLayoutWaitNs)) {
+                if (tid == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), MOE_STATUS_TIMEOUT);
+                return;
+            }
+            load_stat_inputs(a, stat_in);  // their latency overlaps the stores below
+        }
         for (int i = tid; i < a.E; i += blockDim.x) {
             const int e = sm.order[i];
             a.out.expert_count[e] = sm.tot[e];
@@ -747,7 +773,7 @@ template <int KMAX>
 __global__ void __launch_bounds__(kCountThreads) layout_count_kernel(const LayoutArgs a) {
     extern __shared__ int32_t smem[];
     pdl_launch_dependents();  // the rank kernel's prologue only reads ids
-    count_phase<KMAX, true>(a, carve_count(a, smem), blockIdx.x);
+    count_phase<KMAX, true, true>(a, carve_count(a, smem), blockIdx.x);
 }
 
 __global__ void __launch_bounds__(kRankThreads) layout_rank_kernel(const LayoutArgs a) {
@@ -756,9 +782,15 @@ __global__ void __launch_bounds__(kRankThreads) layout_rank_kernel(const LayoutA
     const RankSmem sm = carve_rank(a, smem);
     if (blockIdx.x < a.wl.blocks) rank_prologue(a, sm, blockIdx.x);
     pdl_wait();  // from here on the count kernel's tables are needed
-    rank_finish(a, sm, blockIdx.x);
+    rank_finish(a, sm, blockIdx.x, nullptr);
 }
 
+__device__ __forceinline__ void set_timeout(const LayoutArgs& a) {
+    if (threadIdx.x == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), MOE_STATUS_TIMEOUT);
+}
+
+// One cooperative kernel: every slot block ranks and counts its tokens, and
+// all meet at one grid barrier before the rest of the rank phase.
 template <int KMAX>
 __global__ void __launch_bounds__(kRankThreads) layout_fused_kernel(const LayoutArgs a) {
     extern __shared__ int32_t smem[];
@@ -771,13 +803,47 @@ __global__ void __launch_bounds__(kRankThreads) layout_fused_kernel(const Layout
         rank_prologue(a, rsm, b);
         csm.hist = rsm.tot;
         csm.eid = rsm.eid;
-        count_phase<KMAX, false>(a, csm, b);
+        count_phase<KMAX, false, true>(a, csm, b);
     }
-    if (!grid_barrier(reinterpret_cast<uint32_t*>(a.ws + a.wl.barrier), 1000000000ull)) {
-        if (threadIdx.x == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), MOE_STATUS_TIMEOUT);
+    if (!grid_barrier(reinterpret_cast<uint32_t*>(a.ws + a.wl.barrier), kLayoutWaitNs)) {
+        set_timeout(a);
         return;
     }
-    rank_finish(a, rsm, b);
+    rank_finish(a, rsm, b, nullptr);
+}
+
+// One cooperative kernel of 2B + 1 blocks.  Positions need only the expert
+// histograms, so the per-token counting of the statistics moves off their
+// path:
+//   blocks [0, B)   rank their 128 tokens' slots, publish the histogram,
+//                   arrive at barrier 0, wait for all B and write positions;
+//   blocks [B, 2B)  count the same 128 tokens per rank and host (mask, Mode
+//                   0/1/2 copies), add the counters and arrive at barrier 1;
+//   block 2B        waits at barrier 0, derives counts and offsets, then
+//                   waits at barrier 1 and writes the statistics.
+template <int KMAX>
+__global__ void __launch_bounds__(kRankThreads) layout_split_kernel(const LayoutArgs a) {
+    extern __shared__ int32_t smem[];
+    const int B = a.wl.blocks;
+    const int b = blockIdx.x;
+    uint32_t* ranked = reinterpret_cast<uint32_t*>(a.ws + a.wl.barrier);
+    uint32_t* counted = ranked + 1;
+    if (b >= B && b < 2 * B) {
+        count_phase<KMAX, true, false>(a, carve_count(a, smem), b - B);
+        grid_arrive(counted);
+        return;
+    }
+    const RankSmem rsm = carve_rank(a, smem);
+    if (b < B) {
+        rank_prologue(a, rsm, b);
+        publish_hist(a, rsm.tot, b);
+        grid_arrive(ranked);
+    }
+    if (!grid_wait(ranked, B, kLayoutWaitNs)) {
+        set_timeout(a);
+        return;
+    }
+    rank_finish(a, rsm, b < B ? b : B, counted);
 }
 
 // Layout with no tokens: counts and offsets are all zero.
@@ -834,37 +900,59 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
     return ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), bytes);
 }
 
+cudaError_t launch_cooperative(void (*kernel)(LayoutArgs), int blocks, size_t smem, cudaStream_t stream,
+                               const LayoutArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kRankThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// Whether a cooperative grid of `blocks` blocks of the kernel fits on the GPU
+// at once (err set on a CUDA error).
+bool fits(void (*kernel)(LayoutArgs), int blocks, size_t smem, cudaError_t* err) {
+    *err = allow_smem(kernel, smem);
+    if (*err != cudaSuccess) return false;
+    const int per_sm = blocks_per_sm(reinterpret_cast<const void*>(kernel), kRankThreads, smem);
+    return blocks <= per_sm * device_sm_count();
+}
+
+// The layout in the form a.kind asks for, or the next form whose grid fits:
+// split (2B + 1 blocks), fused (B + 1), then two kernels.  Every grid has one
+// block more than the slot blocks: it writes counts, offsets and statistics
+// while the others write positions.
 template <int KMAX>
 cudaError_t launch_layout_k(const LayoutArgs& a, cudaStream_t stream) {
-    cudaError_t err;
+    cudaError_t err = cudaSuccess;
     const size_t smem_count = sizeof(int32_t) * count_smem_words(a.E, a.R, a.Rs);
     const size_t smem_rank = sizeof(int32_t) * rank_smem_words(a.E, a.R, a.k);
-    // One cooperative kernel when every block of the grid can be resident.
-    auto fused = layout_fused_kernel<KMAX>;
-    const size_t smem_fused = smem_rank + smem_count;
-    if ((err = allow_smem(fused, smem_fused)) != cudaSuccess) return err;
-    const int per_sm = blocks_per_sm(reinterpret_cast<const void*>(fused), kRankThreads, smem_fused);
-    // Grids have one block more than slot blocks: it writes counts, offsets
-    // and statistics while the others write positions.
-    if (a.wl.blocks + 1 <= per_sm * device_sm_count()) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(a.wl.blocks + 1);
-        cfg.blockDim = dim3(kRankThreads);
-        cfg.dynamicSmemBytes = smem_fused;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, fused, a);
+    const int B = a.wl.blocks;
+    if (a.kind == MOE_LAYOUT_AUTO || a.kind == MOE_LAYOUT_SPLIT) {
+        // count blocks carve their tables from the start of the same memory
+        const size_t smem = smem_rank > smem_count ? smem_rank : smem_count;
+        if (fits(layout_split_kernel<KMAX>, 2 * B + 1, smem, &err))
+            return launch_cooperative(layout_split_kernel<KMAX>, 2 * B + 1, smem, stream, a);
+        if (err != cudaSuccess) return err;
+    }
+    if (a.kind != MOE_LAYOUT_TWO_KERNELS) {
+        const size_t smem = smem_rank + smem_count;
+        if (fits(layout_fused_kernel<KMAX>, B + 1, smem, &err))
+            return launch_cooperative(layout_fused_kernel<KMAX>, B + 1, smem, stream, a);
+        if (err != cudaSuccess) return err;
     }
     auto count = layout_count_kernel<KMAX>;
     if ((err = allow_smem(count, smem_count)) != cudaSuccess) return err;
     if ((err = allow_smem(layout_rank_kernel, smem_rank)) != cudaSuccess) return err;
-    count<<<a.wl.blocks, kCountThreads, smem_count, stream>>>(a);
+    count<<<B, kCountThreads, smem_count, stream>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    return launch_pdl(layout_rank_kernel, dim3(a.wl.blocks + 1), dim3(kRankThreads), smem_rank, stream, a);
+    return launch_pdl(layout_rank_kernel, dim3(B + 1), dim3(kRankThreads), smem_rank, stream, a);
 }
 
 }  // namespace

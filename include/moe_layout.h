@@ -87,7 +87,7 @@ typedef enum {
 #define MOE_MAX_HIDDEN   (1 << 20)  /* columns of a row: row bytes stay far inside int32 */
 #define MOE_FP8_GROUP    128   /* columns per fp32 scale */
 
-/* Launch shapes of the row movers.  The pages' HybridEP issue lists the
+/* Launch shapes of the layout and the row movers.  The pages' HybridEP issue lists the
  * knobs of that library ("Poor HybridEP performance on dual-node 16x B300
  * GPUs": NUM_OF_TOKENS_PER_CHUNK_*, NUM_SMS_DISPATCH / NUM_SMS_COMBINE,
  * NUM_BLOCKS_PERMUTE / NUM_BLOCKS_UNPERMUTE); these are their counterparts on
@@ -110,10 +110,23 @@ typedef enum {
  *     (partner pieces gathered into shared memory by bulk copies; at most 8
  *     partners, more fall back to vector) or MOE_MOVE_VECTOR (rows through
  *     registers with vector loads).
- *   combine_ctas_per_sm: bulk combine CTAs per SM, 1 .. 3. */
+ *   combine_ctas_per_sm: bulk combine CTAs per SM, 1 .. 3.
+ *   layout_kind: the form of moe_layout's kernels.  MOE_LAYOUT_AUTO (default:
+ *     the first of the three below whose grid fits on the GPU at once),
+ *     MOE_LAYOUT_SPLIT (one cooperative kernel whose position blocks wait only
+ *     for the expert histograms, while separate blocks count tokens per rank
+ *     and host for the statistics; 2B + 1 blocks of 128 tokens),
+ *     MOE_LAYOUT_FUSED (one cooperative kernel, each block counting and then
+ *     ranking its tokens; B + 1 blocks) or MOE_LAYOUT_TWO_KERNELS (a counting
+ *     kernel, then a ranking kernel; any T).  A form whose grid does not fit
+ *     gives way to the next one. */
 #define MOE_MOVE_AUTO   0
 #define MOE_MOVE_VECTOR 1
 #define MOE_MOVE_BULK   2
+#define MOE_LAYOUT_AUTO        0
+#define MOE_LAYOUT_SPLIT       1
+#define MOE_LAYOUT_FUSED       2
+#define MOE_LAYOUT_TWO_KERNELS 3
 typedef struct moe_tuning {
     int32_t dispatch_kind;
     int32_t dispatch_sms;
@@ -124,7 +137,8 @@ typedef struct moe_tuning {
     int32_t combine_kind;
     int32_t combine_sms;
     int32_t combine_ctas_per_sm;
-    int32_t reserved[7];          /* must be 0 */
+    int32_t layout_kind;
+    int32_t reserved[6];          /* must be 0 */
 } moe_tuning;
 
 /* The problem, fixed for one layer.  Sizes:

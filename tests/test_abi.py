@@ -208,7 +208,7 @@ def test_host_stats_rejected_on_host(moe):
 
 
 def test_tuning_checked_on_host(moe):
-    """moe_tuning (launch shapes of the movers): every out-of-range field is
+    """moe_tuning (launch shapes of the layout and the movers): every out-of-range field is
     rejected by every call before anything is enqueued; defaults pass."""
     import ctypes
     p = _p(moe)
@@ -216,13 +216,15 @@ def test_tuning_checked_on_host(moe):
     for good in (dict(), dict(dispatch_kind=moe.MOE_MOVE_BULK, dispatch_warps=16, dispatch_stages=3,
                               dispatch_chunk_bytes=4096),
                  dict(dispatch_kind=moe.MOE_MOVE_VECTOR, dispatch_sms=1, dispatch_ctas_per_sm=8),
-                 dict(combine_kind=moe.MOE_MOVE_VECTOR, combine_sms=152, combine_ctas_per_sm=3)):
+                 dict(combine_kind=moe.MOE_MOVE_VECTOR, combine_sms=152, combine_ctas_per_sm=3),
+                 dict(layout_kind=moe.MOE_LAYOUT_SPLIT), dict(layout_kind=moe.MOE_LAYOUT_TWO_KERNELS)):
         p.tuning = moe.Tuning(**good)
         assert moe.moe_workspace_bytes(p) == base
     for bad in (dict(dispatch_kind=3), dict(combine_kind=-1), dict(dispatch_sms=-1), dict(combine_sms=-4),
                 dict(dispatch_ctas_per_sm=9), dict(dispatch_warps=17), dict(dispatch_stages=9),
                 dict(dispatch_chunk_bytes=100), dict(dispatch_chunk_bytes=1000), dict(dispatch_chunk_bytes=32784),
-                dict(dispatch_warps=16, dispatch_stages=8, dispatch_chunk_bytes=7168), dict(combine_ctas_per_sm=4)):
+                dict(dispatch_warps=16, dispatch_stages=8, dispatch_chunk_bytes=7168), dict(combine_ctas_per_sm=4),
+                dict(layout_kind=4), dict(layout_kind=-1)):
         p.tuning = moe.Tuning(**bad)
         with pytest.raises(moe.MoeError) as ei:
             moe.moe_workspace_bytes(p)
@@ -240,3 +242,7 @@ def test_tuning_from_environment(moe):
                              "MOE_COMBINE_KIND": "vector", "UNRELATED": "1"})
     assert t.dispatch_kind == moe.MOE_MOVE_BULK and t.dispatch_warps == 6
     assert t.combine_kind == moe.MOE_MOVE_VECTOR and t.combine_sms == 76 and t.dispatch_sms == 0
+    assert t.layout_kind == moe.MOE_LAYOUT_AUTO
+    for name, kind in (("split", moe.MOE_LAYOUT_SPLIT), ("FUSED", moe.MOE_LAYOUT_FUSED),
+                       ("two_kernels", moe.MOE_LAYOUT_TWO_KERNELS), ("2", moe.MOE_LAYOUT_FUSED)):
+        assert moe.Tuning.from_env({"MOE_LAYOUT_KIND": name}).layout_kind == kind
