@@ -123,6 +123,9 @@ moe::LayoutArgs layout_args(const moe_problem* problem, const Dims& d, const voi
     a.ws = static_cast<uint8_t*>(const_cast<void*>(workspace));
     a.wl = ws_layout(d);
     a.kind = d.shape.layout_kind;
+    // the layer means T*k/E and T*k/R, each rounded once as the record defines them
+    a.mean_expert = (double)((int64_t)d.T * d.k) / (double)d.E;
+    a.mean_rank = (double)((int64_t)d.T * d.k) / (double)d.R;
     return a;
 }
 

@@ -111,6 +111,8 @@ struct LayoutArgs {
     WsLayout wl;
     moe_layout_t out;
     int kind;             // MOE_LAYOUT_* (MOE_LAYOUT_AUTO: the fastest form that fits)
+    double mean_expert;   // (double)(T*k) / E, the imbalance ratio's denominator
+    double mean_rank;     // (double)(T*k) / R
 };
 
 // Launch shapes from a moe_tuning (0 = the default).

@@ -27,11 +27,11 @@
 //
 // Three forms, the first whose grid fits on the GPU at once (or the one the
 // caller's tuning names):
-//  split  one cooperative kernel of 2B + 1 blocks.  Positions depend only on
+//  split  one cooperative kernel of 2B + 2 blocks.  Positions depend only on
 //         the expert histograms, so B blocks rank their slots, publish the
 //         histogram and meet at one grid barrier, while B other blocks count
 //         the same tokens for the statistics and only arrive at a second
-//         barrier, which the extra block alone waits for.  The positions no
+//         barrier, which one extra block alone waits for.  The positions no
 //         longer wait for the per-token counting.
 //  fused  one cooperative kernel of B + 1 blocks: each block ranks its slots,
 //         counts its tokens and publishes both, then meets the others at one
@@ -135,10 +135,7 @@ __device__ __forceinline__ unsigned long long warp_sum_small(unsigned long long 
     return __reduce_add_sync(kFull, (unsigned)v);
 }
 
-// Reductions of the statistics: maxima (of key values) and sums.
-enum { RMAX_EXPERT = 0, RMAX_EXPERT_MIN, RMAX_SRC_M1, RMAX_SRC_M2, RMAX_SLOTS, RMAX_TOKENS,
-       RMAX_REMOTE, RMAX_RELAY, RSUM_TOK, RSUM_M0, RSUM_M1, RSUM_M2, R_COUNT };
-constexpr int kMaxStatWarps = 32;
+constexpr int kMaxStatWarps = 32;  // warps of a block that writes the statistics record
 
 // Counters of the statistics record that thread tid reads from the workspace
 // (source rank tid, destination rank tid, and for warp 0 the host counts of
@@ -164,133 +161,170 @@ __device__ __forceinline__ void load_stat_inputs(const LayoutArgs& a, StatIn& in
     in.hc1 = tid < 32 && lane + 32 < a.H ? __ldcg(hc + lane + 32) : 0;
 }
 
-// The statistics record of a layout, written into the workspace by one whole
-// block once the counters are complete.  ecount / rcount: expert and rank
-// slot counts (any memory the block can read); in: load_stat_inputs.
-__device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const int32_t* rcount, const StatIn& in) {
-    __shared__ unsigned long long s_red[R_COUNT][kMaxStatWarps];
+// The statistics record of a layout, written into the workspace and, when
+// the caller asked for it, into a.out.stats as well.  Two parts, each written
+// by one whole block, with disjoint header words, so that two blocks can
+// write them side by side:
+//   stats_slots     from the expert and rank slot counts alone: the maxima,
+//                   the minimum, the two imbalance ratios, the per-rank slot
+//                   words, the sizes, and zeros in the unused header words;
+//   stats_counters  from the per-token counters (load_stat_inputs): the
+//                   status bits, tokens and Mode 0/1/2 copies per source
+//                   rank, receive counts per destination rank, their sums
+//                   and maxima.
+__device__ __forceinline__ void put_stat(const LayoutArgs& a, size_t i, int64_t val) {
+    reinterpret_cast<int64_t*>(a.ws + a.wl.stats)[i] = val;
+    if (a.out.stats != nullptr) a.out.stats[i] = val;
+}
+
+__device__ void stats_slots(const LayoutArgs& a, const int32_t* ecount, const int32_t* rcount) {
+    __shared__ unsigned long long s_red[3][kMaxStatWarps];
+    __shared__ unsigned long long s_fin[3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = (blockDim.x + 31) >> 5;
-    unsigned long long v[R_COUNT];
-#pragma unroll
-    for (int i = 0; i < R_COUNT; ++i) v[i] = 0ull;
-    auto ws32 = [&](size_t off) { return reinterpret_cast<const int32_t*>(a.ws + off); };
-    // The status word for the record: its load overlaps the work below.
-    const unsigned status = tid == 0 ? __ldcg(reinterpret_cast<const unsigned*>(a.ws + a.wl.status)) : 0u;
-
+    for (int i = MOE_ST_NUM_HOSTS + 1 + tid; i < MOE_STATS_HEADER_WORDS; i += blockDim.x) put_stat(a, i, 0);
+    unsigned long long kmax = 0ull, kmin = 0ull, smax = 0ull;
     for (int e = tid; e < a.E; e += blockDim.x) {
         const unsigned long long c = (unsigned)ecount[e];
         const unsigned long long key = (c << 32) | (unsigned)(a.E - 1 - e);  // ties -> smallest e
-        v[RMAX_EXPERT] = key > v[RMAX_EXPERT] ? key : v[RMAX_EXPERT];
+        kmax = key > kmax ? key : kmax;
         const unsigned long long nkey = ~((c << 32) | (unsigned)e);          // minimum via complement
-        v[RMAX_EXPERT_MIN] = nkey > v[RMAX_EXPERT_MIN] ? nkey : v[RMAX_EXPERT_MIN];
+        kmin = nkey > kmin ? nkey : kmin;
     }
-    // The record goes to the workspace and, when the caller asked for it, to
-    // a.out.stats as well: every word is stored to both from registers.
-    int64_t* rec = reinterpret_cast<int64_t*>(a.ws + a.wl.stats);
-    int64_t* const copy = a.out.stats;
-    auto put = [&](size_t i, int64_t val) {
-        rec[i] = val;
-        if (copy != nullptr) copy[i] = val;
-    };
+    const size_t dst = MOE_STATS_HEADER_WORDS + (size_t)MOE_SRC_FIELDS * a.Rs;
+    for (int r = tid; r < a.R; r += blockDim.x) {
+        const int64_t slots = rcount[r];
+        put_stat(a, dst + MOE_DST_SLOTS * a.R + r, slots);
+        smax = max(smax, (unsigned long long)slots);
+    }
+    kmax = warp_max_key(kmax);
+    kmin = warp_max_key(kmin);
+    smax = warp_max_key(smax);
+    if (lane == 0) {
+        s_red[0][warp] = kmax;
+        s_red[1][warp] = kmin;
+        s_red[2][warp] = smax;
+    }
+    __syncthreads();
+    if (tid < 3) {
+        unsigned long long x = 0ull;
+        for (int w = 0; w < nwarps; ++w) x = max(x, s_red[tid][w]);
+        s_fin[tid] = x;
+    }
+    __syncthreads();
+    if (tid < 2) {
+        // Imbalance ratios, one per thread: busiest expert over the layer mean
+        // T*k/E ("Balancing and Beyond", section 2), and the same for ranks.
+        // The means come from the host (LayoutArgs), so one division remains.
+        const int64_t S = (int64_t)a.T * a.k;
+        if (tid == 0) {
+            put_stat(a, MOE_ST_TOKENS, a.T);
+            put_stat(a, MOE_ST_SLOTS, S);
+            put_stat(a, MOE_ST_ROW_BYTES, a.row_bytes);
+            put_stat(a, MOE_ST_MAX_EXPERT, (int64_t)(s_fin[0] >> 32));
+            put_stat(a, MOE_ST_ARGMAX_EXPERT, a.E - 1 - (int64_t)(s_fin[0] & 0xffffffffull));
+            put_stat(a, MOE_ST_MIN_EXPERT, (int64_t)(~s_fin[1] >> 32));
+            put_stat(a, MOE_ST_MAX_RANK_SLOTS, (int64_t)s_fin[2]);
+            put_stat(a, MOE_ST_NUM_HOSTS, a.H);
+        }
+        const double top = tid == 0 ? (double)(int64_t)(s_fin[0] >> 32) : (double)s_fin[2];
+        const double mean = tid == 0 ? a.mean_expert : a.mean_rank;
+        put_stat(a, tid == 0 ? MOE_ST_IMBALANCE_RATIO : MOE_ST_RANK_IMBALANCE,
+                 __double_as_longlong(S > 0 ? top / mean : 0.0));
+    }
+}
+
+// Reductions of the counter part: maxima and sums.
+enum { CMAX_SRC_M1 = 0, CMAX_SRC_M2, CMAX_TOKENS, CMAX_REMOTE, CMAX_RELAY, CSUM_TOK, CSUM_M0, CSUM_M1, CSUM_M2,
+       C_COUNT };
+
+__device__ void stats_counters(const LayoutArgs& a, const StatIn& in) {
+    __shared__ unsigned long long s_red[C_COUNT][kMaxStatWarps];
+    __shared__ unsigned long long s_fin[C_COUNT];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    unsigned long long v[C_COUNT];
+#pragma unroll
+    for (int i = 0; i < C_COUNT; ++i) v[i] = 0ull;
+    auto ws32 = [&](size_t off) { return reinterpret_cast<const int32_t*>(a.ws + off); };
+    // The status word for the record: its load overlaps the work below.
+    const unsigned status = tid == 0 ? __ldcg(reinterpret_cast<const unsigned*>(a.ws + a.wl.status)) : 0u;
     const size_t src = MOE_STATS_HEADER_WORDS;
     const size_t dst = src + (size_t)MOE_SRC_FIELDS * a.Rs;
-    __shared__ int64_t s_hdr[MOE_STATS_HEADER_WORDS];
-    for (int i = tid; i < MOE_STATS_HEADER_WORDS; i += blockDim.x) s_hdr[i] = 0;
     for (int r = tid; r < a.Rs; r += blockDim.x) {
         const bool mine = r == tid;  // loaded by load_stat_inputs
         const int64_t tok = mine ? in.src[0] : __ldcg(ws32(a.wl.src_tokens) + r);
         const int64_t m0 = mine ? in.src[1] : __ldcg(ws32(a.wl.src_mode0) + r);
         const int64_t m1 = mine ? in.src[2] : __ldcg(ws32(a.wl.src_mode1) + r);
         const int64_t m2 = mine ? in.src[3] : __ldcg(ws32(a.wl.src_mode2) + r);
-        put(src + MOE_SRC_TOKENS * a.Rs + r, tok);
-        put(src + MOE_SRC_COPIES * a.Rs + r, tok * a.k);
-        put(src + MOE_SRC_MODE0 * a.Rs + r, m0);
-        put(src + MOE_SRC_MODE1 * a.Rs + r, m1);
-        put(src + MOE_SRC_MODE2 * a.Rs + r, m2);
+        put_stat(a, src + MOE_SRC_TOKENS * a.Rs + r, tok);
+        put_stat(a, src + MOE_SRC_COPIES * a.Rs + r, tok * a.k);
+        put_stat(a, src + MOE_SRC_MODE0 * a.Rs + r, m0);
+        put_stat(a, src + MOE_SRC_MODE1 * a.Rs + r, m1);
+        put_stat(a, src + MOE_SRC_MODE2 * a.Rs + r, m2);
         // "tokens x k x h x 2 B" per rank and direction ("Balancing and
         // Beyond", section 1); copies x row bytes per mode (section 3.2).
-        put(src + MOE_SRC_NAIVE_BYTES * a.Rs + r, tok * a.k * (int64_t)a.h * 2);
-        put(src + MOE_SRC_MODE0_BYTES * a.Rs + r, m0 * a.row_bytes);
-        put(src + MOE_SRC_MODE1_BYTES * a.Rs + r, m1 * a.row_bytes);
-        put(src + MOE_SRC_MODE2_BYTES * a.Rs + r, m2 * a.row_bytes);
-        v[RSUM_TOK] += tok;
-        v[RSUM_M0] += m0;
-        v[RSUM_M1] += m1;
-        v[RSUM_M2] += m2;
-        v[RMAX_SRC_M1] = max(v[RMAX_SRC_M1], (unsigned long long)m1);
-        v[RMAX_SRC_M2] = max(v[RMAX_SRC_M2], (unsigned long long)m2);
+        put_stat(a, src + MOE_SRC_NAIVE_BYTES * a.Rs + r, tok * a.k * (int64_t)a.h * 2);
+        put_stat(a, src + MOE_SRC_MODE0_BYTES * a.Rs + r, m0 * a.row_bytes);
+        put_stat(a, src + MOE_SRC_MODE1_BYTES * a.Rs + r, m1 * a.row_bytes);
+        put_stat(a, src + MOE_SRC_MODE2_BYTES * a.Rs + r, m2 * a.row_bytes);
+        v[CSUM_TOK] += tok;
+        v[CSUM_M0] += m0;
+        v[CSUM_M1] += m1;
+        v[CSUM_M2] += m2;
+        v[CMAX_SRC_M1] = max(v[CMAX_SRC_M1], (unsigned long long)m1);
+        v[CMAX_SRC_M2] = max(v[CMAX_SRC_M2], (unsigned long long)m2);
     }
     for (int r = tid; r < a.R; r += blockDim.x) {
         const bool mine = r == tid;  // loaded by load_stat_inputs
-        const int64_t slots = rcount[r];
         const int64_t tok = mine ? in.dst[0] : __ldcg(ws32(a.wl.dst_tokens) + r);
         const int64_t self = mine ? in.dst[1] : __ldcg(ws32(a.wl.dst_self) + r);
         const int64_t local = mine ? in.dst[2] : __ldcg(ws32(a.wl.dst_local) + r);
         const int64_t rem = mine ? in.dst[3] : __ldcg(ws32(a.wl.dst_remote) + r);
         const int64_t rel = mine ? in.dst[4] : __ldcg(ws32(a.wl.dst_relay) + r);
-        put(dst + MOE_DST_SLOTS * a.R + r, slots);
-        put(dst + MOE_DST_TOKENS * a.R + r, tok);
-        put(dst + MOE_DST_SELF * a.R + r, self);
-        put(dst + MOE_DST_LOCAL * a.R + r, local);
-        put(dst + MOE_DST_REMOTE * a.R + r, rem);
-        put(dst + MOE_DST_RELAY * a.R + r, rel);
-        v[RMAX_SLOTS] = max(v[RMAX_SLOTS], (unsigned long long)slots);
-        v[RMAX_TOKENS] = max(v[RMAX_TOKENS], (unsigned long long)tok);
-        v[RMAX_REMOTE] = max(v[RMAX_REMOTE], (unsigned long long)rem);
-        v[RMAX_RELAY] = max(v[RMAX_RELAY], (unsigned long long)rel);
+        put_stat(a, dst + MOE_DST_TOKENS * a.R + r, tok);
+        put_stat(a, dst + MOE_DST_SELF * a.R + r, self);
+        put_stat(a, dst + MOE_DST_LOCAL * a.R + r, local);
+        put_stat(a, dst + MOE_DST_REMOTE * a.R + r, rem);
+        put_stat(a, dst + MOE_DST_RELAY * a.R + r, rel);
+        v[CMAX_TOKENS] = max(v[CMAX_TOKENS], (unsigned long long)tok);
+        v[CMAX_REMOTE] = max(v[CMAX_REMOTE], (unsigned long long)rem);
+        v[CMAX_RELAY] = max(v[CMAX_RELAY], (unsigned long long)rel);
     }
 #pragma unroll
-    for (int i = 0; i < R_COUNT; ++i) {
-        const unsigned long long w = i < RSUM_TOK ? warp_max_key(v[i]) : warp_sum_small(v[i]);
+    for (int i = 0; i < C_COUNT; ++i) {
+        const unsigned long long w = i < CSUM_TOK ? warp_max_key(v[i]) : warp_sum_small(v[i]);
         if (lane == 0) s_red[i][warp] = w;
     }
     __syncthreads();
-    __shared__ unsigned long long s_fin[R_COUNT];
-    if (tid < R_COUNT) {
+    if (tid < C_COUNT) {
         unsigned long long x = 0ull;
-        for (int w = 0; w < nwarps; ++w) x = tid < RSUM_TOK ? max(x, s_red[tid][w]) : x + s_red[tid][w];
+        for (int w = 0; w < nwarps; ++w) x = tid < CSUM_TOK ? max(x, s_red[tid][w]) : x + s_red[tid][w];
         s_fin[tid] = x;
     }
     __syncthreads();
-    const int64_t S = (int64_t)a.T * a.k;
-    if (tid < 2) {
-        // Imbalance ratios, one per thread: busiest expert over the layer mean
-        // T*k/E ("Balancing and Beyond", section 2), and the same for ranks.
-        const double top = tid == 0 ? (double)(int64_t)(s_fin[RMAX_EXPERT] >> 32) : (double)s_fin[RMAX_SLOTS];
-        const double parts = tid == 0 ? (double)a.E : (double)a.R;
-        const double ratio = S > 0 ? top / ((double)S / parts) : 0.0;
-        s_hdr[tid == 0 ? MOE_ST_IMBALANCE_RATIO : MOE_ST_RANK_IMBALANCE] = __double_as_longlong(ratio);
-    }
     if (tid == 0) {
         const unsigned long long* r = s_fin;
-        int64_t* rec = s_hdr;  // the header is built in shared memory
-        const int64_t emax = (int64_t)(r[RMAX_EXPERT] >> 32);
-        const unsigned long long minkey = ~r[RMAX_EXPERT_MIN];
-        rec[MOE_ST_STATUS] = (int64_t)status;
-        rec[MOE_ST_TOKENS] = a.T;
-        rec[MOE_ST_SLOTS] = S;
-        rec[MOE_ST_ROW_BYTES] = a.row_bytes;
-        rec[MOE_ST_MAX_EXPERT] = emax;
-        rec[MOE_ST_ARGMAX_EXPERT] = a.E - 1 - (int64_t)(r[RMAX_EXPERT] & 0xffffffffull);
-        rec[MOE_ST_MIN_EXPERT] = (int64_t)(minkey >> 32);
-        rec[MOE_ST_MAX_RANK_SLOTS] = (int64_t)r[RMAX_SLOTS];
-        rec[MOE_ST_MAX_RANK_TOKENS] = (int64_t)r[RMAX_TOKENS];
-        rec[MOE_ST_SUM_MODE0] = (int64_t)r[RSUM_M0];
-        rec[MOE_ST_SUM_MODE1] = (int64_t)r[RSUM_M1];
-        rec[MOE_ST_SUM_MODE2] = (int64_t)r[RSUM_M2];
-        rec[MOE_ST_MAX_SRC_MODE1] = (int64_t)r[RMAX_SRC_M1];
-        rec[MOE_ST_MAX_SRC_MODE2] = (int64_t)r[RMAX_SRC_M2];
-        rec[MOE_ST_MAX_RECV_REMOTE] = (int64_t)r[RMAX_REMOTE];
-        rec[MOE_ST_MAX_RECV_RELAY] = (int64_t)r[RMAX_RELAY];
-        rec[MOE_ST_SUM_NAIVE_BYTES] = (int64_t)r[RSUM_TOK] * a.k * (int64_t)a.h * 2;
-        rec[MOE_ST_SUM_MODE0_BYTES] = (int64_t)r[RSUM_M0] * a.row_bytes;
-        rec[MOE_ST_SUM_MODE1_BYTES] = (int64_t)r[RSUM_M1] * a.row_bytes;
-        rec[MOE_ST_SUM_MODE2_BYTES] = (int64_t)r[RSUM_M2] * a.row_bytes;
-        rec[MOE_ST_NUM_HOSTS] = a.H;
+        put_stat(a, MOE_ST_STATUS, (int64_t)status);
+        put_stat(a, MOE_ST_MAX_RANK_TOKENS, (int64_t)r[CMAX_TOKENS]);
+        put_stat(a, MOE_ST_SUM_MODE0, (int64_t)r[CSUM_M0]);
+        put_stat(a, MOE_ST_SUM_MODE1, (int64_t)r[CSUM_M1]);
+        put_stat(a, MOE_ST_SUM_MODE2, (int64_t)r[CSUM_M2]);
+        put_stat(a, MOE_ST_MAX_SRC_MODE1, (int64_t)r[CMAX_SRC_M1]);
+        put_stat(a, MOE_ST_MAX_SRC_MODE2, (int64_t)r[CMAX_SRC_M2]);
+        put_stat(a, MOE_ST_MAX_RECV_REMOTE, (int64_t)r[CMAX_REMOTE]);
+        put_stat(a, MOE_ST_MAX_RECV_RELAY, (int64_t)r[CMAX_RELAY]);
+        put_stat(a, MOE_ST_SUM_NAIVE_BYTES, (int64_t)r[CSUM_TOK] * a.k * (int64_t)a.h * 2);
+        put_stat(a, MOE_ST_SUM_MODE0_BYTES, (int64_t)r[CSUM_M0] * a.row_bytes);
+        put_stat(a, MOE_ST_SUM_MODE1_BYTES, (int64_t)r[CSUM_M1] * a.row_bytes);
+        put_stat(a, MOE_ST_SUM_MODE2_BYTES, (int64_t)r[CSUM_M2] * a.row_bytes);
     }
-    __syncthreads();
-    for (int i = tid; i < MOE_STATS_HEADER_WORDS; i += blockDim.x) put(i, s_hdr[i]);
+}
+
+// Both parts at once, for a block whose counters are all complete.
+__device__ void write_stats(const LayoutArgs& a, const int32_t* ecount, const int32_t* rcount, const StatIn& in) {
+    stats_slots(a, ecount, rcount);
+    stats_counters(a, in);
 }
 
 // ---- count phase -----------------------------------------------------------
@@ -603,16 +637,52 @@ __device__ void rank_prologue(const LayoutArgs& a, const RankSmem& sm, int b) {
     __syncthreads();
 }
 
+// Host counts and offsets, and the counter part of the statistics record
+// (when the caller asked for it), from the complete per-token counters.  One
+// whole block; in: load_stat_inputs.
+__device__ void counter_outputs(const LayoutArgs& a, const StatIn& in) {
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {
+        // host counts and their exclusive scan: lane L holds hosts L and L + 32
+        const int c0 = in.hc0, c1 = in.hc1;
+        int x0 = c0, x1 = c1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u0 = __shfl_up_sync(kFull, x0, off), u1 = __shfl_up_sync(kFull, x1, off);
+            if (lane >= off) { x0 += u0; x1 += u1; }
+        }
+        const int low_total = __shfl_sync(kFull, x0, 31);
+        if (lane < a.H) {
+            a.out.host_count[lane] = c0;
+            a.out.host_offset[lane] = x0 - c0;
+        }
+        if (lane + 32 < a.H) {
+            a.out.host_count[lane + 32] = c1;
+            a.out.host_offset[lane + 32] = low_total + x1 - c1;
+        }
+        if (lane == 31) a.out.host_offset[a.H] = low_total + x1;
+    }
+    // The record only when the caller asked for it with the layout; otherwise
+    // stats_compute_kernel can make it later, beside the dispatch.
+    if (a.out.stats != nullptr) stats_counters(a, in);
+}
+
+// Records that a grid-barrier wait gave up (status bit MOE_STATUS_TIMEOUT).
+__device__ __forceinline__ void set_timeout(const LayoutArgs& a) {
+    if (threadIdx.x == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), MOE_STATUS_TIMEOUT);
+}
+
 // The rest of the rank phase, once every block's expert histogram is
 // published: totals, offsets, this block's prefix, outputs, statistics (the
-// extra block, b == B) and the positions of the block's slots.  counted:
-// NULL when the per-token counters are complete too; otherwise the arrival
-// counter of the blocks that add them, which the extra block waits for.
-__device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b, const uint32_t* counted) {
+// extra block, b == B) and the positions of the block's slots.  With
+// counters_here the per-token counters are complete too and the extra block
+// also writes what is made from them (counter_outputs); otherwise another
+// block does that.
+__device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b, bool counters_here) {
     __shared__ int32_t s_warp[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     StatIn stat_in = {};
-    if (b == a.wl.blocks && counted == nullptr) load_stat_inputs(a, stat_in);  // complete already
+    if (b == a.wl.blocks && counters_here) load_stat_inputs(a, stat_in);  // complete already
     const int S = a.T * a.k;
     const SlotRange sr = slot_range(a, b);
     const int32_t* g_group = reinterpret_cast<const int32_t*>(a.ws + a.wl.group);
@@ -641,8 +711,13 @@ __device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b, cons
                     tot += v;
                     pre += g < sb ? v : 0;
                 }
-#pragma unroll 8
-                for (int p = tail0 + part; p < b; p += parts) pre += __ldcg(g_agg + (size_t)p * a.E + slot);
+                // at most kLayoutGroup - 1 block rows before b in its group:
+                // every load in flight at once
+#pragma unroll
+                for (int q = 0; q < kLayoutGroup - 1; ++q) {
+                    const int p = tail0 + part + q * parts;
+                    if (p < b) pre += __ldcg(g_agg + (size_t)p * a.E + slot);
+                }
             }
             sm.part[tid] = active ? tot : 0;
             sm.part[kRankThreads + tid] = active ? pre : 0;
@@ -706,13 +781,6 @@ __device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b, cons
     if (b == a.wl.blocks) {
         // The extra block: counts, offsets and statistics (the slot blocks
         // write positions meanwhile).
-        if (counted != nullptr) {
-            if (!grid_wait(counted, a.wl.blocks, kLayoutWaitNs)) {
-                if (tid == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), MOE_STATUS_TIMEOUT);
-                return;
-            }
-            load_stat_inputs(a, stat_in);  // their latency overlaps the stores below
-        }
         for (int i = tid; i < a.E; i += blockDim.x) {
             const int e = sm.order[i];
             a.out.expert_count[e] = sm.tot[e];
@@ -729,31 +797,12 @@ __device__ void rank_finish(const LayoutArgs& a, const RankSmem& sm, int b, cons
             a.out.expert_offset[a.E] = total;
             a.out.rank_offset[a.R] = total;
         }
-        if (warp == 0) {
-            // host counts and their exclusive scan: lane L holds hosts L and L + 32
-            const int c0 = stat_in.hc0, c1 = stat_in.hc1;
-            int x0 = c0, x1 = c1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int u0 = __shfl_up_sync(kFull, x0, off), u1 = __shfl_up_sync(kFull, x1, off);
-                if (lane >= off) { x0 += u0; x1 += u1; }
-            }
-            const int low_total = __shfl_sync(kFull, x0, 31);
-            if (lane < a.H) {
-                a.out.host_count[lane] = c0;
-                a.out.host_offset[lane] = x0 - c0;
-            }
-            if (lane + 32 < a.H) {
-                a.out.host_count[lane + 32] = c1;
-                a.out.host_offset[lane + 32] = low_total + x1 - c1;
-            }
-            if (lane == 31) a.out.host_offset[a.H] = low_total + x1;
-        }
         __syncthreads();
         // The statistics record only when the caller asked for it with the
         // layout; otherwise the kernel ends with its slot blocks and
         // stats_compute_kernel can make the record later, beside the dispatch.
-        if (a.out.stats != nullptr) write_stats(a, sm.tot, sm.rfill, stat_in);
+        if (a.out.stats != nullptr) stats_slots(a, sm.tot, sm.rfill);
+        if (counters_here) counter_outputs(a, stat_in);
         return;
     }
 
@@ -782,11 +831,7 @@ __global__ void __launch_bounds__(kRankThreads) layout_rank_kernel(const LayoutA
     const RankSmem sm = carve_rank(a, smem);
     if (blockIdx.x < a.wl.blocks) rank_prologue(a, sm, blockIdx.x);
     pdl_wait();  // from here on the count kernel's tables are needed
-    rank_finish(a, sm, blockIdx.x, nullptr);
-}
-
-__device__ __forceinline__ void set_timeout(const LayoutArgs& a) {
-    if (threadIdx.x == 0) atomicOr(reinterpret_cast<uint32_t*>(a.ws + a.wl.status), MOE_STATUS_TIMEOUT);
+    rank_finish(a, sm, blockIdx.x, true);
 }
 
 // One cooperative kernel: every slot block ranks and counts its tokens, and
@@ -809,18 +854,20 @@ __global__ void __launch_bounds__(kRankThreads) layout_fused_kernel(const Layout
         set_timeout(a);
         return;
     }
-    rank_finish(a, rsm, b, nullptr);
+    rank_finish(a, rsm, b, true);
 }
 
-// One cooperative kernel of 2B + 1 blocks.  Positions need only the expert
+// One cooperative kernel of 2B + 2 blocks.  Positions need only the expert
 // histograms, so the per-token counting of the statistics moves off their
 // path:
 //   blocks [0, B)   rank their 128 tokens' slots, publish the histogram,
 //                   arrive at barrier 0, wait for all B and write positions;
 //   blocks [B, 2B)  count the same 128 tokens per rank and host (mask, Mode
 //                   0/1/2 copies), add the counters and arrive at barrier 1;
-//   block 2B        waits at barrier 0, derives counts and offsets, then
-//                   waits at barrier 1 and writes the statistics.
+//   block 2B        waits at barrier 0 and writes the expert and rank counts
+//                   and offsets and the slot part of the statistics;
+//   block 2B + 1    waits at barrier 1 and writes the host counts and
+//                   offsets and the counter part of the statistics.
 template <int KMAX>
 __global__ void __launch_bounds__(kRankThreads) layout_split_kernel(const LayoutArgs a) {
     extern __shared__ int32_t smem[];
@@ -833,6 +880,16 @@ __global__ void __launch_bounds__(kRankThreads) layout_split_kernel(const Layout
         grid_arrive(counted);
         return;
     }
+    if (b == 2 * B + 1) {
+        if (!grid_wait(counted, B, kLayoutWaitNs)) {
+            set_timeout(a);
+            return;
+        }
+        StatIn in;
+        load_stat_inputs(a, in);
+        counter_outputs(a, in);
+        return;
+    }
     const RankSmem rsm = carve_rank(a, smem);
     if (b < B) {
         rank_prologue(a, rsm, b);
@@ -843,7 +900,7 @@ __global__ void __launch_bounds__(kRankThreads) layout_split_kernel(const Layout
         set_timeout(a);
         return;
     }
-    rank_finish(a, rsm, b < B ? b : B, counted);
+    rank_finish(a, rsm, b < B ? b : B, false);
 }
 
 // Layout with no tokens: counts and offsets are all zero.
@@ -925,8 +982,8 @@ bool fits(void (*kernel)(LayoutArgs), int blocks, size_t smem, cudaError_t* err)
 }
 
 // The layout in the form a.kind asks for, or the next form whose grid fits:
-// split (2B + 1 blocks), fused (B + 1), then two kernels.  Every grid has one
-// block more than the slot blocks: it writes counts, offsets and statistics
+// split (2B + 2 blocks), fused (B + 1), then two kernels.  Every grid has
+// blocks beyond the slot blocks that write counts, offsets and statistics
 // while the others write positions.
 template <int KMAX>
 cudaError_t launch_layout_k(const LayoutArgs& a, cudaStream_t stream) {
@@ -937,8 +994,8 @@ cudaError_t launch_layout_k(const LayoutArgs& a, cudaStream_t stream) {
     if (a.kind == MOE_LAYOUT_AUTO || a.kind == MOE_LAYOUT_SPLIT) {
         // count blocks carve their tables from the start of the same memory
         const size_t smem = smem_rank > smem_count ? smem_rank : smem_count;
-        if (fits(layout_split_kernel<KMAX>, 2 * B + 1, smem, &err))
-            return launch_cooperative(layout_split_kernel<KMAX>, 2 * B + 1, smem, stream, a);
+        if (fits(layout_split_kernel<KMAX>, 2 * B + 2, smem, &err))
+            return launch_cooperative(layout_split_kernel<KMAX>, 2 * B + 2, smem, stream, a);
         if (err != cudaSuccess) return err;
     }
     if (a.kind != MOE_LAYOUT_TWO_KERNELS) {

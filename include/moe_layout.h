@@ -115,7 +115,8 @@ typedef enum {
  *     the first of the three below whose grid fits on the GPU at once),
  *     MOE_LAYOUT_SPLIT (one cooperative kernel whose position blocks wait only
  *     for the expert histograms, while separate blocks count tokens per rank
- *     and host for the statistics; 2B + 1 blocks of 128 tokens),
+ *     and host for the statistics; B blocks of 128 tokens, B more that count
+ *     them, and 2 that write counts, offsets and statistics),
  *     MOE_LAYOUT_FUSED (one cooperative kernel, each block counting and then
  *     ranking its tokens; B + 1 blocks) or MOE_LAYOUT_TWO_KERNELS (a counting
  *     kernel, then a ranking kernel; any T).  A form whose grid does not fit
