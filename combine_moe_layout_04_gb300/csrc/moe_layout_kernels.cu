@@ -6,12 +6,12 @@
 // host, relayed through the same-index GPU).  Two phases:
 //
 //  count  one thread per token, 128 tokens per block.  A token's k ids stay in
-//         registers.  Every counter is aggregated across the warp before it
-//         touches shared memory: __match_any_sync groups equal expert ids,
-//         ballots count the tokens per rank and per host, one hardware warp
-//         reduction each sums the per-source-rank counts.  Each block publishes its expert
-//         histogram to a [B][E] table and adds it to the totals of its group
-//         of 16 blocks (16 atomics per counter instead of B).
+//         registers.  Ballots count the tokens per rank and per host, one
+//         hardware warp reduction each sums the per-source-rank counts; the
+//         expert histogram, where this phase counts it, takes one shared
+//         atomic per slot.  Each block publishes its expert histogram to a
+//         [B][E] table and adds it to the totals of its group of 16 blocks
+//         (16 atomics per counter instead of B).
 //  rank   256 threads per 128-token block.  Each warp ranks a contiguous run
 //         of slots with __match_any_sync + popc (a stable rank inside the
 //         warp); warps are combined by an exclusive scan in shared memory.  A
@@ -111,12 +111,6 @@ __device__ __forceinline__ int src_rank_of(const LayoutArgs& a, const int32_t* s
 }
 
 __device__ __forceinline__ int clamp_id(int e, int E) { return (e < 0 || e >= E) ? 0 : e; }
-
-// One atomic per group of lanes holding the same non-negative key; -1 skips.
-__device__ __forceinline__ void warp_count(int32_t* counters, int key) {
-    const unsigned same = __match_any_sync(kFull, key);
-    if (key >= 0 && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&counters[key], __popc(same));
-}
 
 // ---- statistics ----------------------------------------------------------
 
@@ -381,6 +375,18 @@ __device__ void count_phase(const LayoutArgs& a, const CountSmem& sm, int b) {
     __shared__ uint32_t s_status;
     __shared__ int s_rs0;
     const int tid = threadIdx.x, lane = tid & 31;
+    const int t = b * kLayoutTokensPerBlock + tid;
+    const bool valid = tid < kLayoutTokensPerBlock && t < a.T;
+    // The token's ids first: their loads are in flight while the tables are
+    // set up.  Validated, then clamped into [0, E), below.
+    int ev[KMAX], rv[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        ev[j] = -1;
+        rv[j] = -1;
+        if (j < a.k && valid)
+            ev[j] = sm.eid ? sm.eid[tid * a.k + j] : a.ids[(size_t)t * a.k + j];
+    }
     if (tid == 0) s_status = 0;
     uint32_t st = 0;
     for (int e = tid; e < a.E; e += blockDim.x) {
@@ -402,8 +408,6 @@ __device__ void count_phase(const LayoutArgs& a, const CountSmem& sm, int b) {
         if (tid == 0 && (sm.soff[0] != 0 || sm.soff[a.Rs] != a.T)) st |= MOE_STATUS_SRC_OFFSET;
     }
 
-    const int t = b * kLayoutTokensPerBlock + tid;
-    const bool valid = tid < kLayoutTokensPerBlock && t < a.T;
     const int rs = valid ? min(max(src_rank_of(a, sm.soff, t), 0), a.Rs - 1) : 0;
     const int own = rs / a.P;
     // Token b*128 always exists: its source rank is the block's first.
@@ -414,15 +418,6 @@ __device__ void count_phase(const LayoutArgs& a, const CountSmem& sm, int b) {
     const bool block_one_src = __syncthreads_and(!valid || rs == rs_first);
     const bool small_r = a.R <= 64;  // a token's ranks fit a 64-bit mask
 
-    // The token's ids, validated, then clamped into [0, E).
-    int ev[KMAX], rv[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-        ev[j] = -1;
-        rv[j] = -1;
-        if (j < a.k && valid)
-            ev[j] = sm.eid ? sm.eid[tid * a.k + j] : a.ids[(size_t)t * a.k + j];
-    }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
         if (j < a.k && valid) {
@@ -442,7 +437,7 @@ __device__ void count_phase(const LayoutArgs& a, const CountSmem& sm, int b) {
     for (int j = 0; j < KMAX; ++j) {
         if (j >= a.k) break;  // a.k is the same for the whole warp
         const int e = ev[j];  // -1 for tokens past T
-        if (HIST) warp_count(sm.hist, e);
+        if (HIST && e >= 0) atomicAdd(&sm.hist[e], 1);  // shared-memory atomics: few lanes collide
         if (e >= 0) {
             const int r = sm.rank[e];
             const int hh = sm.host[e];
