@@ -378,26 +378,58 @@ combine_chain_vec_kernel(const Route rt, const int nvec, const int nspan, const 
     }
 }
 
+// 32- or 16-byte pieces of a row, moved through registers.
+template <int VB> struct VecT;
+template <> struct VecT<32> {
+    uint32_t w[8];
+    __device__ __forceinline__ void load(const uint8_t* p) {
+        asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                       "=r"(w[7])
+                     : "l"(p));
+    }
+    __device__ __forceinline__ void store(uint8_t* p) const {
+        asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                     :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                        "r"(w[7])
+                     : "memory");
+    }
+};
+template <> struct VecT<16> {
+    uint32_t w[4];
+    __device__ __forceinline__ void load(const uint8_t* p) {
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p));
+    }
+    __device__ __forceinline__ void store(uint8_t* p) const {
+        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                     :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+    }
+};
+
 // ---- quantise-in-dispatch ----------------------------------------------------
 
 // bf16 rows in, e4m3 rows + fp32 scales out, one scale per 128 columns: the
 // dispatch kernel converts to FP8 on its way ("Balancing and Beyond", section
-// 3.1).  A warp takes one (token, span of kQuantChunks chunks of 512 columns)
-// unit and loads the whole span before it converts any of it: in chunk c,
-// lane L holds columns 512c + 16L .. 512c + 16L + 15, so lanes 8g .. 8g+7
-// share scale group g of the chunk.  Per group: scale = amax / 448 (1 for an
-// all-zero group), code = e4m3(x / scale) with round-to-nearest-even and
-// saturation; the 16 codes of a lane go to every receive row of the token as
-// one 16-byte store.
-// Four chunks a warp, with a grid of several times the resident CTAs: the
-// prefill-fp8 quantise-in-dispatch (16384 tokens, 1204 MB) took 193 us on GB300,
-// against 216 us with one chunk a warp and a persistent grid, and 210 us with
-// a whole row (7 chunks, 100 registers) a warp.
-constexpr int kQuantChunks = 4;
+// 3.1).  A warp takes one (token, span of 2048 columns) unit, two chunks of
+// 1024 columns, and loads the whole span before it converts any of it: in
+// chunk c, lane L holds columns 1024c + 32L .. 1024c + 32L + 31, so the four
+// lanes 4g .. 4g+3 share scale group g of the chunk.  Per group: scale =
+// amax / 448 (1 for an all-zero group), code = e4m3(x / scale) with
+// round-to-nearest-even and saturation.  A lane's 32 codes go to every
+// receive row of the token as one 32-byte store (two 16-byte ones when the
+// rows are only 16-byte aligned), and the span's 16 scales as one request,
+// lane g holding group g's.
+constexpr int kQuantSpanCols = 2048;
+constexpr int kQuantChunkCols = 1024;
 
+template <int VB>
 __global__ void __launch_bounds__(kMoveThreads)
-dispatch_quant_kernel(const MoveArgs m, const uint4* __restrict__ x, uint8_t* __restrict__ recv,
+dispatch_quant_kernel(const MoveArgs m, const uint8_t* __restrict__ x, uint8_t* __restrict__ recv,
                       float* __restrict__ rs, int h) {
+    constexpr int NIN = 64 / VB;   // pieces of a lane's 32 bf16 inputs
+    constexpr int NOUT = 32 / VB;  // pieces of its 32 codes
+    constexpr unsigned kAll = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     const int gwarp = blockIdx.x * kMoveWarps + (threadIdx.x >> 5);
     const int nwarps = gridDim.x * kMoveWarps;
@@ -412,53 +444,67 @@ dispatch_quant_kernel(const MoveArgs m, const uint4* __restrict__ x, uint8_t* __
             p = m.pos[(size_t)t * m.k + lane];
             if (p < 0 || p >= S) p = -1;
         }
-        uint4 v[kQuantChunks][2];
+        VecT<VB> v[2][NIN];
 #pragma unroll
-        for (int c = 0; c < kQuantChunks; ++c) {
-            const int col = (span * kQuantChunks + c) * 512 + lane * 16;  // first of this lane's 16 columns
-            v[c][0] = v[c][1] = make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < 2; ++c) {
+            const int col = span * kQuantSpanCols + c * kQuantChunkCols + lane * 32;
             if (col < h) {  // h % 128 == 0: groups are whole
-                const uint4* src = x + ((size_t)t * h + col) / 8;
-                v[c][0] = ld_stream_v4(src);
-                v[c][1] = ld_stream_v4(src + 1);
+                const uint8_t* src = x + ((size_t)t * h + col) * 2;
+#pragma unroll
+                for (int i = 0; i < NIN; ++i) v[c][i].load(src + i * VB);
+            } else {
+#pragma unroll
+                for (int i = 0; i < NIN; ++i)
+#pragma unroll
+                    for (int w = 0; w < VB / 4; ++w) v[c][i].w[w] = 0u;
             }
         }
+        float my_scale = 1.0f;  // lanes 0..15: the scale of the span's group `lane`
 #pragma unroll
-        for (int c = 0; c < kQuantChunks; ++c) {
-            const int col = (span * kQuantChunks + c) * 512 + lane * 16;
+        for (int c = 0; c < 2; ++c) {
+            const int col = span * kQuantSpanCols + c * kQuantChunkCols + lane * 32;
             const bool active = col < h;
-            if (!__any_sync(0xffffffffu, active)) break;  // past the row's end for the whole warp
-            float f[16];
-            const uint32_t q[8] = {v[c][0].x, v[c][0].y, v[c][0].z, v[c][0].w,
-                                   v[c][1].x, v[c][1].y, v[c][1].z, v[c][1].w};
+            if (!__any_sync(kAll, active)) break;  // past the row's end for the whole warp
+            float f[32];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                f[2 * i] = __uint_as_float(q[i] << 16);
-                f[2 * i + 1] = __uint_as_float(q[i] & 0xffff0000u);
-            }
+            for (int i = 0; i < NIN; ++i)
+#pragma unroll
+                for (int w = 0; w < VB / 4; ++w) {
+                    const uint32_t q = v[c][i].w[w];
+                    f[2 * (i * (VB / 4) + w)] = __uint_as_float(q << 16);
+                    f[2 * (i * (VB / 4) + w) + 1] = __uint_as_float(q & 0xffff0000u);
+                }
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-            for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 2));
             const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
-            uint32_t packed[4];
+            // lane c*8 + g keeps the scale of the chunk's group g (held by lanes 4g .. 4g+3)
+            const float sg = __shfl_sync(kAll, scale, 4 * (lane & 7));
+            if ((lane >> 3) == c) my_scale = sg;
+            VecT<VB> codes[NOUT];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
                     make_float2(f[4 * i] / scale, f[4 * i + 1] / scale), __NV_SATFINITE, __NV_E4M3);
                 const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
                     make_float2(f[4 * i + 2] / scale, f[4 * i + 3] / scale), __NV_SATFINITE, __NV_E4M3);
-                packed[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+                codes[i / (VB / 4)].w[i % (VB / 4)] = (uint32_t)lo | ((uint32_t)hi << 16);
             }
-            const uint4 codes = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            const int group = col / 128;
             for (int j = 0; j < m.k; ++j) {
-                const int pj = __shfl_sync(0xffffffffu, p, j);
+                const int pj = __shfl_sync(kAll, p, j);
                 if (pj < 0 || !active) continue;
-                st_v4(reinterpret_cast<uint4*>(recv + (size_t)pj * h + col), codes);
-                if ((lane & 7) == 0) rs[(size_t)pj * groups + group] = scale;
+                uint8_t* dst = recv + (size_t)pj * h + col;
+#pragma unroll
+                for (int i = 0; i < NOUT; ++i) codes[i].store(dst + i * VB);
             }
+        }
+        const int g = span * (kQuantSpanCols / 128) + lane;  // the span's group `lane`
+        const bool has_group = lane < kQuantSpanCols / 128 && g < groups;
+        for (int j = 0; j < m.k; ++j) {
+            const int pj = __shfl_sync(kAll, p, j);
+            if (pj >= 0 && has_group) rs[(size_t)pj * groups + g] = my_scale;
         }
     }
 }
@@ -1017,34 +1063,6 @@ constexpr int kVecScaleWords = 4;
 // exactly the resident CTAs looping over the units took 185 us.
 constexpr int kVecOversubscribe = 8;
 
-template <int VB> struct VecT;
-template <> struct VecT<32> {
-    uint32_t w[8];
-    __device__ __forceinline__ void load(const uint8_t* p) {
-        asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
-                       "=r"(w[7])
-                     : "l"(p));
-    }
-    __device__ __forceinline__ void store(uint8_t* p) const {
-        asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-                     :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                        "r"(w[7])
-                     : "memory");
-    }
-};
-template <> struct VecT<16> {
-    uint32_t w[4];
-    __device__ __forceinline__ void load(const uint8_t* p) {
-        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p));
-    }
-    __device__ __forceinline__ void store(uint8_t* p) const {
-        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
-                     :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
-    }
-};
-
 template <int VB> struct VecSpan { static constexpr int V = 7168 / (32 * VB); };
 
 template <int VB, class Route>
@@ -1374,10 +1392,13 @@ cudaError_t launch_relay_combine(const MoveArgs& m, const RelayArgs& r, const vo
 cudaError_t launch_dispatch_quant(const MoveArgs& m0, const void* x, void* recv, float* rs, int h,
                                   cudaStream_t stream) {
     MoveArgs m = m0;
-    m.nchunks = (h + 512 * kQuantChunks - 1) / (512 * kQuantChunks);  // spans per row
+    m.nchunks = (h + kQuantSpanCols - 1) / kQuantSpanCols;  // spans per row
     const long long units = (long long)m.T * m.nchunks;
     if (units == 0) return cudaSuccess;
-    auto kern = dispatch_quant_kernel;
+    // 32-byte pieces where both row arrays allow them (rows are multiples of
+    // 256 bytes of input and 128 of codes), else 16-byte ones
+    const bool v32 = (reinterpret_cast<uintptr_t>(x) & 31) == 0 && (reinterpret_cast<uintptr_t>(recv) & 31) == 0;
+    auto kern = v32 ? dispatch_quant_kernel<32> : dispatch_quant_kernel<16>;
     // like the vector dispatch: a grid of several times the resident CTAs
     // (a tuning that sets SMs or CTAs per SM gets a persistent one)
     const MoveShape& sh = m.shape;
@@ -1385,7 +1406,7 @@ cudaError_t launch_dispatch_quant(const MoveArgs& m0, const void* x, void* recv,
     const bool persistent = sh.dispatch_sms > 0 || sh.dispatch_ctas > 0;
     const int per_sm = persistent ? (sh.dispatch_ctas > 0 ? min(sh.dispatch_ctas, occ) : occ) : occ * kVecOversubscribe;
     kern<<<capped_grid(units, kMoveWarps, mover_sms(sh.dispatch_sms), per_sm), kMoveThreads, 0, stream>>>(
-        m, static_cast<const uint4*>(x), static_cast<uint8_t*>(recv), rs, h);
+        m, static_cast<const uint8_t*>(x), static_cast<uint8_t*>(recv), rs, h);
     return cudaGetLastError();
 }
 
