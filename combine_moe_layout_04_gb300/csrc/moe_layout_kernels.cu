@@ -19,9 +19,10 @@
 //         before its group and of at most 15 single-block counts, loaded in
 //         parallel: no block waits on another.  Every block derives the
 //         expert totals (the sum of the group rows) and the expert and rank
-//         offsets itself (cheap: O(E + R)).  One extra block writes the counts
-//         and offsets out -- and, when the caller passes layout->stats, the
-//         statistics record -- while the others write positions.  Without
+//         offsets itself (cheap: O(E + R)).  Record blocks beside the slot
+//         blocks write the counts and offsets out -- and, when the caller
+//         passes layout->stats, the statistics record -- while the slot
+//         blocks write positions.  Without
 //         layout->stats the record comes later from stats_compute_kernel,
 //         which needs only the counters left in the workspace.
 //
@@ -31,11 +32,15 @@
 //         the expert histograms, so B blocks rank their slots, publish the
 //         histogram and meet at one grid barrier, while B other blocks count
 //         the same tokens for the statistics and only arrive at a second
-//         barrier, which one extra block alone waits for.  The positions no
-//         longer wait for the per-token counting.
+//         barrier.  One record block waits at the first barrier and writes
+//         the expert and rank counts and offsets and the slot part of the
+//         record, another waits at the second and writes the host counts and
+//         offsets and the counter part.  The positions never wait for the
+//         per-token counting.
 //  fused  one cooperative kernel of B + 1 blocks: each block ranks its slots,
 //         counts its tokens and publishes both, then meets the others at one
-//         grid barrier before the rest of the rank phase.
+//         grid barrier before the rest of the rank phase; one record block
+//         writes counts, offsets and the whole record.
 //  two kernels, the second launched under programmatic dependent launch so
 //         that its id-only ranking overlaps the first.
 // The barriers' counters are cleared with the other accumulators before the
@@ -133,8 +138,8 @@ constexpr int kMaxStatWarps = 32;  // warps of a block that writes the statistic
 
 // Counters of the statistics record that thread tid reads from the workspace
 // (source rank tid, destination rank tid, and for warp 0 the host counts of
-// lanes L and L + 32).  The statistics block loads them as soon as they are
-// complete, so that their latency overlaps its other loads; counters of
+// lanes L and L + 32).  The block that writes them loads them as soon as they
+// are complete, so that their latency overlaps its other work; counters of
 // ranks past the block size are read where they are used.
 struct StatIn {
     int32_t src[4];  // tokens, mode 0, 1, 2 copies of source rank tid

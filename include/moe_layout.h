@@ -183,9 +183,10 @@ typedef struct moe_layout_t {
     int32_t* recv_src;       /* [T*k]  t*k + j of the slot held by each row */
     int64_t* stats;          /* optional [moe_stats_words()] int64: when not
                                 NULL, moe_layout also computes the statistics
-                                record and writes it here (one more block of
-                                the layout kernel, which then ends when the
-                                record is written); when NULL, the layout
+                                record and writes it here (blocks of the
+                                layout kernel beside those that write
+                                positions; the kernel ends when the record
+                                is written); when NULL, the layout
                                 skips it and moe_stats_device / moe_stats
                                 compute it later from the workspace */
 } moe_layout_t;
