@@ -664,8 +664,11 @@ def run_ours(args, w):
                         "p10_p50_p90": [round(float(v), 2) for v in np.percentile(cold[:, i], [10, 50, 90])]}
                  for i, name in enumerate(names)},
         "warm_steps": args.steps, "cold_steps": n_cold, "l2_flush_bytes": 2 * l2,
-        "note": ("warm: calls back to back (the statistics record on a side stream, not timed alone); "
-                 "cold: a write of 2x L2 before each call, outside its events"),
+        "note": ("warm: calls back to back ("
+                 + ("the layout writes the statistics record itself" if args.stats == "inline" else
+                    "the statistics record on a side stream, not timed alone")
+                 + "); cold: a write of 2x L2 before each call, outside its events; "
+                 "cold stats: the record made apart from the layout (moe_stats_device)"),
     }
     step(j=j_graph)
     if not torch.equal(out.view(torch.int16), out_graph.view(torch.int16)):
