@@ -839,6 +839,7 @@ __global__ void __launch_bounds__(kRankThreads) layout_rank_kernel(const LayoutA
 template <int KMAX>
 __global__ void __launch_bounds__(kRankThreads) layout_fused_kernel(const LayoutArgs a) {
     extern __shared__ int32_t smem[];
+    pdl_launch_dependents();  // the dispatch's CTAs may take free SM room now; they wait for the end
     const int b = blockIdx.x;
     const RankSmem rsm = carve_rank(a, smem);
     CountSmem csm = carve_count(a, smem + rank_smem_words(a.E, a.R, a.k));
@@ -873,6 +874,7 @@ __global__ void __launch_bounds__(kRankThreads) layout_split_kernel(const Layout
     extern __shared__ int32_t smem[];
     const int B = a.wl.blocks;
     const int b = blockIdx.x;
+    pdl_launch_dependents();  // the dispatch's CTAs may take free SM room now; they wait for the end
     uint32_t* ranked = reinterpret_cast<uint32_t*>(a.ws + a.wl.barrier);
     uint32_t* counted = ranked + 1;
     if (b >= B && b < 2 * B) {

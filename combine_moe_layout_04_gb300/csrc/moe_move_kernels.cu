@@ -1069,6 +1069,10 @@ template <int VB, class Route>
 __global__ void __launch_bounds__(kVecThreads, kVecMinBlocks)
 dispatch_vec_kernel(const Route rt, const int nspan, const uint8_t* __restrict__ x, const float* __restrict__ xs,
                     uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups, bool scale_v8) {
+    // Launched under programmatic dependent launch: the CTAs may become
+    // resident while the previous kernel (the layout) finishes; every read of
+    // its positions comes after this wait.
+    pdl_wait();
     constexpr int V = VecSpan<VB>::V;
     constexpr int SPAN = 32 * V * VB;
     constexpr int WPB = kVecThreads / 32;
@@ -1215,15 +1219,13 @@ cudaError_t launch_dispatch_route(const Route& rt, long long max_units, int row_
             const int occ = blocks_per_sm(reinterpret_cast<const void*>(kern), kVecThreads, 0);
             const int per_sm = persistent ? (sh.dispatch_ctas > 0 ? min(sh.dispatch_ctas, occ) : occ)
                                           : occ * kVecOversubscribe;
-            kern<<<capped_grid(units, kVecThreads / 32, sms, per_sm), kVecThreads, 0, stream>>>(
-                rt, nspan, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(dst), ds, row_bytes, groups,
-                scale_v8);
+            // programmatic dependent launch: the CTAs may become resident while
+            // the previous kernel in the stream (the layout) finishes
+            return launch_pdl(kern, dim3(capped_grid(units, kVecThreads / 32, sms, per_sm)), dim3(kVecThreads), 0,
+                              stream, rt, nspan, static_cast<const uint8_t*>(x), xs, static_cast<uint8_t*>(dst), ds,
+                              row_bytes, groups, scale_v8);
         };
-        if (v32)
-            launch(dispatch_vec_kernel<32, Route>);
-        else
-            launch(dispatch_vec_kernel<16, Route>);
-        return cudaGetLastError();
+        return v32 ? launch(dispatch_vec_kernel<32, Route>) : launch(dispatch_vec_kernel<16, Route>);
     }
     const int warps = sh.dispatch_warps > 0 ? sh.dispatch_warps : (few ? kFewWarps : kDispWarps);
     const int stages = sh.dispatch_stages > 0 ? sh.dispatch_stages : (few ? kFewStages : kDispStages);
