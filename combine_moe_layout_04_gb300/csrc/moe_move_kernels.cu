@@ -548,6 +548,10 @@ combine_bulk_kernel(const Route rt, const int nch, const uint8_t* __restrict__ y
         for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_mbar_init();
     }
+    // Launched under programmatic dependent launch: the CTAs may become
+    // resident while the previous kernel drains; nothing it writes (rows,
+    // positions) is read before this wait.
+    pdl_wait();
     __syncwarp();
 
     const long long units = rt.units() * nch;
@@ -1071,8 +1075,11 @@ dispatch_vec_kernel(const Route rt, const int nspan, const uint8_t* __restrict__
                     uint8_t* __restrict__ recv, float* __restrict__ rs, int row_bytes, int groups, bool scale_v8) {
     // Launched under programmatic dependent launch: the CTAs may become
     // resident while the previous kernel (the layout) finishes; every read of
-    // its positions comes after this wait.
+    // its positions comes after this wait.  A CTA that has started lets the
+    // next kernel (the combine) be scheduled: its CTAs take the room of
+    // finished ones in the last wave and wait for this grid's end.
     pdl_wait();
+    pdl_launch_dependents();
     constexpr int V = VecSpan<VB>::V;
     constexpr int SPAN = 32 * V * VB;
     constexpr int WPB = kVecThreads / 32;
@@ -1188,9 +1195,8 @@ cudaError_t launch_combine_bulk(const Route& rt, long long max_units, int nvec, 
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int grid = capped_grid(units, WARPS, mover_sms(sh.combine_sms), sh.combine_ctas > 0 ? sh.combine_ctas : PER_SM);
-    kern<<<grid, WARPS * 32, smem, stream>>>(rt, nch, static_cast<const uint8_t*>(y), static_cast<uint8_t*>(out),
-                                             row_bytes);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(WARPS * 32), smem, stream, rt, nch, static_cast<const uint8_t*>(y),
+                      static_cast<uint8_t*>(out), row_bytes);
 }
 
 // The dispatch pipelines for one route.  kind: MOE_MOVE_VECTOR or
