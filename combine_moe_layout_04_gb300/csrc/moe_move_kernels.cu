@@ -301,6 +301,11 @@ template <int ACC, int U, int KB, class Route>
 __global__ void __launch_bounds__(kMoveThreads)
 combine_chain_vec_kernel(const Route rt, const int nvec, const int nspan, const uint4* __restrict__ y,
                          uint4* __restrict__ out, float* __restrict__ acc_rows, bool acc_v8) {
+    // Launched under programmatic dependent launch: nothing the previous
+    // kernel writes (rows, the chain, positions) is read before this wait; a
+    // CTA that has started lets the next kernel be scheduled.
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const long long units = rt.units() * nspan;
     const long long nw = (long long)gridDim.x * kMoveWarps;
@@ -427,6 +432,10 @@ template <int VB>
 __global__ void __launch_bounds__(kMoveThreads)
 dispatch_quant_kernel(const MoveArgs m, const uint8_t* __restrict__ x, uint8_t* __restrict__ recv,
                       float* __restrict__ rs, int h) {
+    // Launched under programmatic dependent launch: the positions are read
+    // after this wait; a CTA that has started lets the combine be scheduled.
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int NIN = 64 / VB;   // pieces of a lane's 32 bf16 inputs
     constexpr int NOUT = 32 / VB;  // pieces of its 32 codes
     constexpr unsigned kAll = 0xffffffffu;
@@ -1267,9 +1276,9 @@ cudaError_t launch_combine_chain_vec(const Route& rt, long long max_units, int n
     const bool persistent = sh.combine_sms > 0 || sh.combine_ctas > 0;
     const int per_sm = persistent ? (sh.combine_ctas > 0 ? min(sh.combine_ctas, occ) : occ) : occ * kVecOversubscribe;
     const bool acc_v8 = (reinterpret_cast<uintptr_t>(acc) & 31) == 0;
-    kern<<<capped_grid(units, kMoveWarps, mover_sms(sh.combine_sms), per_sm), kMoveThreads, 0, stream>>>(
-        rt, nvec, nspan, static_cast<const uint4*>(y), static_cast<uint4*>(out), acc, acc_v8);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(capped_grid(units, kMoveWarps, mover_sms(sh.combine_sms), per_sm)),
+                      dim3(kMoveThreads), 0, stream, rt, nvec, nspan, static_cast<const uint4*>(y),
+                      static_cast<uint4*>(out), acc, acc_v8);
 }
 
 // Sums at most nl partner rows per unit.  The bulk pipeline's stage holds
@@ -1413,9 +1422,9 @@ cudaError_t launch_dispatch_quant(const MoveArgs& m0, const void* x, void* recv,
     const int occ = blocks_per_sm(reinterpret_cast<const void*>(kern), kMoveThreads, 0);
     const bool persistent = sh.dispatch_sms > 0 || sh.dispatch_ctas > 0;
     const int per_sm = persistent ? (sh.dispatch_ctas > 0 ? min(sh.dispatch_ctas, occ) : occ) : occ * kVecOversubscribe;
-    kern<<<capped_grid(units, kMoveWarps, mover_sms(sh.dispatch_sms), per_sm), kMoveThreads, 0, stream>>>(
-        m, static_cast<const uint8_t*>(x), static_cast<uint8_t*>(recv), rs, h);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(capped_grid(units, kMoveWarps, mover_sms(sh.dispatch_sms), per_sm)),
+                      dim3(kMoveThreads), 0, stream, m, static_cast<const uint8_t*>(x), static_cast<uint8_t*>(recv),
+                      rs, h);
 }
 
 cudaError_t read_move_faults(uint32_t* bits, cudaStream_t stream) {
