@@ -181,6 +181,8 @@ __device__ void stats_slots(const LayoutArgs& a, const int32_t* ecount, const in
     __shared__ unsigned long long s_fin[3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = (blockDim.x + 31) >> 5;
+    // the header words past the last named one are unused: zeros, from this part
+    static_assert(MOE_ST_NUM_HOSTS + 1 <= MOE_STATS_HEADER_WORDS, "header words");
     for (int i = MOE_ST_NUM_HOSTS + 1 + tid; i < MOE_STATS_HEADER_WORDS; i += blockDim.x) put_stat(a, i, 0);
     unsigned long long kmax = 0ull, kmin = 0ull, smax = 0ull;
     for (int e = tid; e < a.E; e += blockDim.x) {

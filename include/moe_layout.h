@@ -252,7 +252,8 @@ enum {
     MOE_ST_SUM_MODE2_BYTES,
     MOE_ST_IMBALANCE_RATIO,     /* double: max expert count / (T*k/E) */
     MOE_ST_RANK_IMBALANCE,      /* double: max rank slots / (T*k/R) */
-    MOE_ST_NUM_HOSTS            /* H */
+    MOE_ST_NUM_HOSTS            /* H; stays the last named word: the words
+                                   after it are unused and read 0 */
 };
 enum { MOE_SRC_TOKENS = 0, MOE_SRC_COPIES, MOE_SRC_MODE0, MOE_SRC_MODE1, MOE_SRC_MODE2,
        MOE_SRC_NAIVE_BYTES, MOE_SRC_MODE0_BYTES, MOE_SRC_MODE1_BYTES, MOE_SRC_MODE2_BYTES,

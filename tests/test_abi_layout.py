@@ -61,3 +61,15 @@ def test_header_fields_all_mirrored():
                 m = re.search(r"(\w+)\s*(\[\s*\w+\s*\])?\s*$", part.strip())
                 names.append(m.group(1))
         assert names == [f for f, _ in cls._fields_], (cname, names)
+
+
+def test_num_hosts_is_the_last_named_header_word():
+    """The layout kernel's two record blocks write disjoint header words; the
+    one that writes the sizes also zeroes every word after MOE_ST_NUM_HOSTS,
+    so no named word may follow it."""
+    import re
+    text = open(os.path.join(ROOT, "include", "moe_layout.h")).read()
+    body = re.search(r"MOE_ST_STATUS = 0,(.*?)\};", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = [n.strip() for n in body.split(",") if n.strip()]
+    assert names[-1] == "MOE_ST_NUM_HOSTS", names[-3:]
