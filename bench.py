@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -211,20 +212,46 @@ def job_value(units_per_rank, ms_max, world):
 
 # ----------------------------------------------------------------- oracle (CPU)
 
-def oracle_pass(w, tokens, ids, gates, xin, y):
-    """One pass of the oracle over the first `tokens` tokens of a workload."""
+def oracle_pass(w, tokens, ids, gates, xin, y, times=None):
+    """One pass of the oracle over the first `tokens` tokens of a workload;
+    appends (layout + stats, dispatch, combine) seconds to `times` if given."""
     import oracle
     eb = 1 if w.dtype == "fp8" else 2
     prob, keep = oracle.make_problem(tokens, w.h, w.k, w.E, w.R, w.P, 1, eb, w.scale_group)
+    t0 = time.perf_counter()
     lay = oracle.layout(prob, ids[:tokens])
     oracle.stats(prob, ids[:tokens])
+    t1 = time.perf_counter()
     if w.quantize:
         oracle.quantize_dispatch(prob, lay["pos"], xin[:tokens])
     elif w.dtype == "fp8":
         oracle.dispatch(prob, lay["pos"], xin[0][:tokens], xin[1][:tokens])
     else:
         oracle.dispatch(prob, lay["pos"], xin[:tokens])
+    t2 = time.perf_counter()
     oracle.combine(prob, lay["pos"], y, gates[:tokens])
+    t3 = time.perf_counter()
+    if times is not None:
+        times.append((t1 - t0, t2 - t1, t3 - t2))
+
+
+def host_cpu():
+    """The host's CPU model (x86 model name, or Arm implementer and part) and
+    its logical CPU count."""
+    model = platform.machine()
+    try:
+        info = open("/proc/cpuinfo").read()
+        names = [l.split(":", 1)[1].strip() for l in info.splitlines() if l.startswith("model name")]
+        if names:
+            model = names[0]
+        else:
+            impl = [l.split(":", 1)[1].strip() for l in info.splitlines() if l.startswith("CPU implementer")]
+            part = [l.split(":", 1)[1].strip() for l in info.splitlines() if l.startswith("CPU part")]
+            if impl and part:
+                model = f"{platform.machine()} implementer {impl[0]} part {part[0]}"
+    except OSError:
+        pass
+    return {"cpu_model": model, "nproc": os.cpu_count()}
 
 
 def oracle_inputs(w, tokens):
@@ -248,13 +275,22 @@ def cpu_baseline(w, seconds=10.0):
     per_tok = (time.perf_counter() - t0) / probe
     tokens = int(max(probe, min(w.T, seconds / max(per_tok, 1e-9))))
     ids, gates, xin, y = oracle_inputs(w, tokens)
-    t0 = time.perf_counter()
+    # one warm-up pass, then the median of 5 (3 when a pass is long)
+    reps = 5 if per_tok * tokens < 4.0 else 3
     oracle_pass(w, tokens, ids, gates, xin, y)
-    dt = time.perf_counter() - t0
+    times = []
+    for _ in range(reps):
+        oracle_pass(w, tokens, ids, gates, xin, y, times)
+    import numpy as np
+    med = np.median(np.array(times), axis=0)
+    dt = float(med.sum())
     d, c = algorithmic_bytes(w, tokens)
     return {"value": round((d + c) / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {tokens} of {w.T} tokens of {w.name}: layout+stats+dispatch+combine, "
-                      f"one pass, {dt:.2f} s"}
+                      f"one warm-up pass and the median of {reps}, {dt:.2f} s a pass",
+            "per_call_s": {"layout_stats": round(float(med[0]), 4), "dispatch": round(float(med[1]), 4),
+                           "combine": round(float(med[2]), 4)},
+            "host": dict(host_cpu(), threads_used=1)}
 
 
 def run_reference(args, w):
