@@ -388,11 +388,9 @@ inline int device_sm_count() {
 }
 
 // Allows `kernel` at least `bytes` of dynamic shared memory on the current
-// device (the attribute is set only when it has to grow).
-// Raises the kernel's dynamic shared-memory limit to `bytes` (cached per
-// device).  Set whatever the size: a kernel's static shared memory counts
-// against the same 48 KB default, so a dynamic size below 48 KB can still need
-// the opt-in.
+// device (cached per device; the attribute is set only when it has to grow).
+// Set whatever the size: a kernel's static shared memory counts against the
+// same 48 KB default, so a dynamic size below 48 KB can still need the opt-in.
 inline cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
     static std::mutex mu;
     static std::unordered_map<const void*, std::unordered_map<int, size_t>> done;
